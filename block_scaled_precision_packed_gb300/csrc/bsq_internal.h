@@ -1,0 +1,59 @@
+// bsq_internal.h -- host-side plumbing shared by the libbsq translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/bsq.h"
+
+namespace bsq {
+
+// Per-device state, set up by the first call on a device (with that device
+// current): the device error word's address and the SM count.
+struct DeviceInfo {
+    uint32_t* err = nullptr;   // device address of the error word
+    int num_sms = 0;
+    int max_smem_optin = 0;
+};
+
+// Returns nullptr (and sets *st) if the current device cannot be set up.
+const DeviceInfo* device_info(bsq_status* st);
+
+void count_launch(int kernel_id);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The launch status of the kernel just enqueued.
+inline bsq_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA;
+}
+
+// cuTensorMapEncodeTiled, resolved through the runtime (no -lcuda link).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// Entry points implemented per translation unit.
+bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, uint8_t* codes,
+                              uint8_t* scales, float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
+bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,
+                                 float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
+size_t quantize_workspace_bytes(int64_t M, int64_t K);
+
+bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA, const void* W, int fw,
+                       const uint8_t* sW, const float* gW, void* Y, int out, int64_t M, int64_t N,
+                       int64_t K, bool nvfp4, cudaStream_t s);
+
+bsq_status gemv_launch(const uint16_t* x, const void* W, int fw, const uint8_t* sW, const float* gW, void* y,
+                       int out, int64_t M, int64_t N, int64_t K, bool nvfp4, cudaStream_t s);
+
+bsq_status dequant_launch(const void* codes, int fmt, const uint8_t* scales, const float* g, float* out,
+                          int64_t R, int64_t K, bool nvfp4, cudaStream_t s);
+
+// Format id for nvfp4 in the internal launchers (the MX ids are bsq_mxfmt).
+constexpr int kNvfp4 = 3;
+
+}  // namespace bsq

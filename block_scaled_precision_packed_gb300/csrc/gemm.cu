@@ -1,0 +1,387 @@
+// gemm.cu -- block-scaled GEMM on the 5th-generation tensor cores (sm_103a):
+//     Y[m, n] = gA * gW * sum_k A[m, k] * W[n, k]
+// with both operands packed minifloats and per-block scales
+// (cubecl-tile tests/tile/packed.rs, nvfp4_shaped_matmul: the block level,
+// then the tensor factor).
+//
+//   nvfp4  tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X: e2m1 x e2m1,
+//          ue4m3 scale per 16, K = 64 per instruction (32 packed bytes).
+//   MX     tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X: e3m2 / e2m3 /
+//          e4m3 on either side, UE8M0 per 32, K = 32 per instruction.
+//          Packed fp6 rows are expanded 12 -> 16 bytes per 16 codes by the TMA
+//          unit itself (CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B), which is the
+//          shared-memory form the MMA reads for 6-bit operands.
+//
+// One persistent CTA per SM, warp-specialised (192 threads):
+//   warp 0      TMA producer: A / W tiles (128-byte swizzle) and the scale
+//               atoms (plain bulk copies) into an S-stage shared-memory ring.
+//   warp 1      owns the TMEM allocation; one lane issues tcgen05.cp (scale
+//               atoms -> TMEM) and tcgen05.mma, and commits each stage back to
+//               the producer and each finished tile to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld the 128 x BN fp32 accumulator, scale by
+//               gA*gW, convert, store.
+// Every wait is bounded (2 s); a timeout records its site in the device error
+// word, drains the copies in flight, frees TMEM and returns.
+//
+// The block-scale buffers are consumed in place: their layout (128 rows x 4
+// blocks per 512-byte atom) is the one tcgen05.cp .32x128b.warpx4 moves into
+// four TMEM columns, so a stage's scales are whole atoms.
+#include <cstdio>
+#include <mutex>
+
+#include "bsq_device.cuh"
+#include "bsq_internal.h"
+
+namespace bsq {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kThreads = 192;
+constexpr int kAtom = 512;          // bytes of one 128-row x 4-block scale atom
+constexpr uint32_t kTmemCols = 512;
+
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+template <bool NVF4, int BN>
+struct Cfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kMmaPerStage = 4;                       // 4 x 32 bytes of K per row
+    static constexpr int kStageK = NVF4 ? 256 : 128;             // elements of K per stage
+    static constexpr int kAtomsPerStage = NVF4 ? 4 : 1;          // scale atoms along K per 128 rows
+    static constexpr int kRowTilesB = BN / 128;
+    static constexpr int kABytes = kBM * 128;
+    static constexpr int kBBytes = BN * 128;
+    static constexpr int kSfaBytes = kAtomsPerStage * kAtom;
+    static constexpr int kSfbBytes = kRowTilesB * kAtomsPerStage * kAtom;
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    // TMEM: accumulator columns [0, BN), then per stage SFA then SFB columns.
+    static constexpr int kSfaCols = kAtomsPerStage * 4;
+    static constexpr int kSfbCols = kRowTilesB * kAtomsPerStage * 4;
+    static constexpr int kSfColsPerStage = kSfaCols + kSfbCols;
+    static_assert(BN + kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM budget");
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+struct GemmArgs {
+    const uint8_t* sA;
+    const uint8_t* sW;
+    const float* gA;
+    const float* gW;
+    void* Y;
+    int64_t M, N, K;
+    int64_t cpd4;          // scale atoms along K per 128-row tile (pad4(blocks)/4)
+    int out_bf16;
+    uint32_t idesc;        // instruction descriptor without the scale-id fields
+    uint32_t* err;
+};
+
+template <bool NVF4, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const GemmArgs args) {
+    using C = Cfg<NVF4, BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA_st = smem;
+    uint8_t* sB_st = sA_st + C::kStages * C::kABytes;
+    uint8_t* sSfa = sB_st + C::kStages * C::kBBytes;
+    uint8_t* sSfb = sSfa + C::kStages * C::kSfaBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sSfb + C::kStages * C::kSfbBytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::kStages;
+    uint64_t* acc_full = bars + 2 * C::kStages;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain = acc_full + 2;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(acc_full + 3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t M = args.M, N = args.N, K = args.K;
+    const int64_t num_mb = (M + kBM - 1) / kBM, num_nb = (N + BN - 1) / BN;
+    const int64_t num_tiles = num_mb * num_nb;
+    const int64_t nks = (K + C::kStageK - 1) / C::kStageK;
+    const int64_t rt_total = pad_to(N, 128) / 128;   // 128-row scale tiles of W
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(full + s), 1);
+            mbar_init(smem_u32(empty + s), 1);
+        }
+        mbar_init(smem_u32(acc_full), 1);
+        mbar_init(smem_u32(acc_empty), 4 * 32);
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base_s;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer --
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_parity[8] = {0};
+            bool issued_any[8] = {false};
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const int64_t mb = tile % num_mb, nb = tile / num_mb;
+                for (int64_t ks = 0; ks < nks; ++ks) {
+                    if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, args.err, abort_flag, kErrGemmProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t kg = ks * C::kAtomsPerStage;             // first scale atom along K
+                    const int natoms = (int)imin64(C::kAtomsPerStage, args.cpd4 - kg);
+                    const uint32_t bytes = C::kABytes + C::kBBytes + (uint32_t)natoms * kAtom * (1 + C::kRowTilesB);
+                    const uint32_t fb = smem_u32(full + stage);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    const int32_t kx = (int32_t)(ks * (NVF4 ? 128 : C::kStageK));   // bytes (nvfp4) / elements
+                    tma_load_2d(smem_u32(sA_st + stage * C::kABytes), &tmA, fb, kx, (int32_t)(mb * kBM));
+                    tma_load_2d(smem_u32(sB_st + stage * C::kBBytes), &tmW, fb, kx, (int32_t)(nb * BN));
+                    bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), args.sA + (mb * args.cpd4 + kg) * kAtom,
+                              natoms * kAtom, fb);
+#pragma unroll
+                    for (int rt = 0; rt < C::kRowTilesB; ++rt) {
+                        int64_t wrt = nb * C::kRowTilesB + rt;
+                        if (wrt >= rt_total) wrt = nb * C::kRowTilesB;    // rows beyond N: any finite scales
+                        bulk_load(smem_u32(sSfb + stage * C::kSfbBytes + rt * C::kAtomsPerStage * kAtom),
+                                  args.sW + (wrt * args.cpd4 + kg) * kAtom, natoms * kAtom, fb);
+                    }
+                    issued_parity[stage] = phase;
+                    issued_any[stage] = true;
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (*abort_flag) {
+                // drain: every copy issued must land before the CTA retires
+                for (int s = 0; s < C::kStages; ++s) {
+                    if (!issued_any[s]) continue;
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(full + s), issued_parity[s]) && globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // --------------------------------------------------- MMA issue --
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                if (!mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, args.err, abort_flag, kErrGemmMma)) break;
+                tc_fence_after();
+                for (int64_t ks = 0; ks < nks; ++ks) {
+                    if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sf_col = (uint32_t)(BN + stage * C::kSfColsPerStage);
+                    const int64_t kg = ks * C::kAtomsPerStage;
+                    const int natoms = (int)imin64(C::kAtomsPerStage, args.cpd4 - kg);
+                    // scale atoms -> TMEM (4 columns each, replicated to all lane quarters)
+                    for (int a = 0; a < natoms; ++a) {
+                        tc_cp_scales(tmem + sf_col + 4 * a,
+                                     smem_desc(smem_u32(sSfa + stage * C::kSfaBytes + a * kAtom), 0, 128, 0));
+#pragma unroll
+                        for (int rt = 0; rt < C::kRowTilesB; ++rt)
+                            tc_cp_scales(tmem + sf_col + C::kSfaCols + (a * C::kRowTilesB + rt) * 4,
+                                         smem_desc(smem_u32(sSfb + stage * C::kSfbBytes +
+                                                            (rt * C::kAtomsPerStage + a) * kAtom), 0, 128, 0));
+                    }
+                    const uint32_t a_base = smem_u32(sA_st + stage * C::kABytes);
+                    const uint32_t b_base = smem_u32(sB_st + stage * C::kBBytes);
+                    const int n_mma = NVF4 ? (int)imin64(4, (K - ks * C::kStageK) / 64) : 4;
+                    for (int kk = 0; kk < n_mma; ++kk) {
+                        const uint64_t ad = smem_desc(a_base + 32 * kk, 16, 1024, 2);
+                        const uint64_t bd = smem_desc(b_base + 32 * kk, 16, 1024, 2);
+                        const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (NVF4) {
+                            tc_mma_mxf4nvf4(tmem, ad, bd, args.idesc, tmem + sf_col + 4 * kk,
+                                            tmem + sf_col + C::kSfaCols + kk * C::kRowTilesB * 4, acc);
+                        } else {
+                            const uint32_t id = args.idesc | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
+                            tc_mma_mxf8f6f4(tmem, ad, bd, id, tmem + sf_col, tmem + sf_col + C::kSfaCols, acc);
+                        }
+                    }
+                    tc_commit(smem_u32(empty + stage));
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(acc_full));
+                acc_phase ^= 1;
+            }
+            // every MMA issued has completed before TMEM is released
+            tc_commit(smem_u32(drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(drain), 0)) {
+                if (globaltimer() - t0 > kWaitLimitNs) { atomicCAS(args.err, 0u, (uint32_t)kErrGemmDrain); break; }
+            }
+        }
+    } else {
+        // ------------------------------------------------------- epilogue --
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const float f = __fmul_rn(args.gA ? __ldg(args.gA) : 1.0f, args.gW ? __ldg(args.gW) : 1.0f);
+        uint32_t acc_phase = 0;
+        const bool vec = args.out_bf16 ? (N % 8 == 0) : (N % 4 == 0);
+        for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int64_t mb = tile % num_mb, nb = tile / num_mb;
+            if (!mbar_wait(smem_u32(acc_full), acc_phase, args.err, abort_flag, kErrGemmEpilogue)) break;
+            tc_fence_after();
+            const int64_t row = mb * kBM + 32 * q + lane;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * c), r);
+                tc_wait_ld();
+                const int64_t col0 = nb * BN + 32 * c;
+                if (row < M && col0 < N) {
+                    if (args.out_bf16) {
+                        uint16_t* yr = static_cast<uint16_t*>(args.Y) + row * N + col0;
+                        if (vec && col0 + 32 <= N) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                uint32_t p[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float lo = __fmul_rn(__uint_as_float(r[8 * v + 2 * e]), f);
+                                    const float hi = __fmul_rn(__uint_as_float(r[8 * v + 2 * e + 1]), f);
+                                    p[e] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+                                }
+                                *reinterpret_cast<uint4*>(yr + 8 * v) = make_uint4(p[0], p[1], p[2], p[3]);
+                            }
+                        } else {
+                            for (int e = 0; e < 32 && col0 + e < N; ++e)
+                                yr[e] = f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[e]), f));
+                        }
+                    } else {
+                        float* yr = static_cast<float*>(args.Y) + row * N + col0;
+                        if (vec && col0 + 32 <= N) {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                *reinterpret_cast<float4*>(yr + 4 * v) =
+                                    make_float4(__fmul_rn(__uint_as_float(r[4 * v]), f),
+                                                __fmul_rn(__uint_as_float(r[4 * v + 1]), f),
+                                                __fmul_rn(__uint_as_float(r[4 * v + 2]), f),
+                                                __fmul_rn(__uint_as_float(r[4 * v + 3]), f));
+                        } else {
+                            for (int e = 0; e < 32 && col0 + e < N; ++e) yr[e] = __fmul_rn(__uint_as_float(r[e]), f);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(acc_empty));
+            acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host ----
+// Instruction descriptor (kind::mxf8f6f4 / kind::mxf4nvf4, dense, K-major):
+// bits 7-9 A format, 10-12 B format, 17-22 N>>3, 23 scale type (1 = UE8M0),
+// 24-28 M>>4; the scale-factor ids (bits 4-5 B, 29-30 A) are set per MMA.
+uint32_t make_idesc(bool nvf4, int fa, int fw, int bn) {
+    auto code = [](int f) -> uint32_t { return f == kE4M3 ? 0u : f == kE2M3 ? 3u : 4u; };
+    uint32_t d = 0;
+    if (nvf4) {
+        d |= 1u << 7;            // e2m1
+        d |= 1u << 10;
+    } else {
+        d |= code(fa) << 7;
+        d |= code(fw) << 10;
+        d |= 1u << 23;           // UE8M0 scales
+    }
+    d |= (uint32_t)(bn >> 3) << 17;
+    d |= (uint32_t)(kBM >> 4) << 24;
+    return d;
+}
+
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Tensor map of one operand: nvfp4 as raw bytes (K/2 per row), fp6 through
+// the 16U6_ALIGN16B unpacking type (K codes per row), e4m3 as bytes.
+bool operand_map(CUtensorMap* map, const void* p, int fmt, bool nvf4, int64_t rows, int64_t K, uint32_t box_rows) {
+    if (nvf4) return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, p, (uint64_t)(K / 2), (uint64_t)rows,
+                                (uint64_t)(K / 2), 128, box_rows);
+    if (fmt == kE4M3) return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, p, (uint64_t)K, (uint64_t)rows,
+                                        (uint64_t)K, 128, box_rows);
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B, p, (uint64_t)K, (uint64_t)rows,
+                      (uint64_t)(3 * K / 4), 128, box_rows);
+}
+
+template <bool NVF4, int BN>
+bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a,
+                       cudaStream_t s) {
+    using C = Cfg<NVF4, BN>;
+    static std::once_flag flags[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
+    bool attr_ok = true;
+    std::call_once(flags[dev], [&] {
+        attr_ok = cudaFuncSetAttribute(gemm_kernel<NVF4, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes) == cudaSuccess;
+    });
+    if (!attr_ok) return BSQ_ERR_CUDA;
+    const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
+    const int grid = (int)imin64(tiles, info->num_sms);
+    gemm_kernel<NVF4, BN><<<grid, kThreads, C::kSmemBytes, s>>>(ta, tw, a);
+    return launch_status();
+}
+
+}  // namespace
+
+bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA, const void* W, int fw,
+                       const uint8_t* sW, const float* gW, void* Y, int out, int64_t M, int64_t N, int64_t K,
+                       bool nvf4, cudaStream_t s) {
+    bsq_status st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
+    // BN = 256 when that still gives every SM a tile, else 128.
+    const int64_t tiles256 = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
+    const int bn = tiles256 >= info->num_sms ? 256 : 128;
+    CUtensorMap ta, tw;
+    if (!operand_map(&ta, A, fa, nvf4, M, K, kBM) || !operand_map(&tw, W, fw, nvf4, N, K, (uint32_t)bn))
+        return BSQ_ERR_CUDA;
+    GemmArgs a;
+    a.sA = sA; a.sW = sW; a.gA = gA; a.gW = gW; a.Y = Y;
+    a.M = M; a.N = N; a.K = K;
+    a.cpd4 = pad_to(K / (nvf4 ? 16 : 32), 4) / 4;
+    a.out_bf16 = out == BSQ_OUT_BF16;
+    a.idesc = make_idesc(nvf4, fa, fw, bn);
+    a.err = info->err;
+    bsq_status r;
+    if (nvf4) r = bn == 256 ? launch_gemm<true, 256>(info, ta, tw, a, s) : launch_gemm<true, 128>(info, ta, tw, a, s);
+    else r = bn == 256 ? launch_gemm<false, 256>(info, ta, tw, a, s) : launch_gemm<false, 128>(info, ta, tw, a, s);
+    count_launch(nvf4 ? BSQ_KERNEL_GEMM_NVFP4 : BSQ_KERNEL_GEMM_MX);
+    return r;
+}
+
+}  // namespace bsq

@@ -1,0 +1,206 @@
+/*
+ * bsq.h -- C ABI of libbsq: block-scaled packed-precision matrix products and
+ * their quantizers on one GB300 (sm_103a).
+ *
+ * The operation (cubecl-tile tests/tile/packed.rs, nvfp4_shaped_matmul and
+ * packed_matmul_rhs): c = (w (x) s_block (x) s_global) . x, written here as
+ *     Y[m, n] = gA * gW * sum_k A[m, k] * W[n, k]          (Y = A W^T)
+ * where each packed operand's element is decode(code) * block_scale.
+ *
+ * Formats (all little-endian):
+ *   nvfp4  e2m1 codes, eight per uint32 word, element 0 in bits 0..3 ("low field
+ *          first", cubecl-tile packed.rs module doc); rows of K/8 words.  One
+ *          ue4m3 scale byte per 16 elements of a row; one fp32 tensor factor.
+ *   MX     e3m2 / e2m3 codes packed four in three bytes,
+ *          bits = c0 | c1<<6 | c2<<12 | c3<<18 (b12x _lib/fp6.py,
+ *          pack_4_fp6_codes); rows of 3K/4 bytes.  e4m3 codes one byte each,
+ *          rows of K bytes.  One UE8M0 byte (2^(e-127)) per 32 elements.
+ *   block scales   a buffer of pad128(rows) * pad4(blocks) bytes, the scale of
+ *          (row r, block b) at
+ *          ((((r/128)*(pad4(blocks)/4) + b/4)*32 + r%32)*4 + (r%128)/32)*4 + b%4
+ *          (b12x _lib/fp6.py, mxfp6_swizzled_scale_offset); padding bytes zero.
+ *   tensor factor  s_global: the dequantization multiplier, a device float.
+ *          The quantizers write 1/gs (gs = 448*fmt_max/amax; 0 if amax == 0).
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     never frees them, never keeps them after the call returns, and never
+ *     modifies an input.
+ *   - Work is enqueued on `stream` (0 = the legacy default stream); nothing
+ *     synchronizes and nothing allocates on these call paths, so the calls can
+ *     be captured in a CUDA graph.  The first call on a device loads its
+ *     kernels; make one call before capturing.
+ *   - Arguments are validated on the host before any launch; a failed check
+ *     returns a status and launches nothing.
+ *   - Launch failures return BSQ_ERR_CUDA.  Device-side timeouts of bounded
+ *     waits are recorded in a device error word; read it with
+ *     bsq_get_device_error.
+ *   - Y / y are row-major [M, N], bf16 or fp32 as `out` says.
+ */
+#ifndef BSQ_H
+#define BSQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BSQ_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define BSQ_API __attribute__((visibility("default")))
+#else
+#define BSQ_API
+#endif
+
+typedef enum bsq_status {
+    BSQ_OK = 0,
+    BSQ_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad enum */
+    BSQ_ERR_UNSUPPORTED = 2,   /* shape outside what a kernel supports */
+    BSQ_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    BSQ_ERR_WORKSPACE = 4,     /* workspace missing or too small */
+    BSQ_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+    BSQ_ERR_TIMEOUT = 6,       /* a device-side bounded wait gave up */
+    BSQ_ERR_DEVICE_CHECK = 7   /* a device-side check failed */
+} bsq_status;
+
+typedef enum bsq_mxfmt { BSQ_E3M2 = 0, BSQ_E2M3 = 1, BSQ_E4M3 = 2 } bsq_mxfmt;
+typedef enum bsq_outtype { BSQ_OUT_F32 = 0, BSQ_OUT_BF16 = 1 } bsq_outtype;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+BSQ_API const char* bsq_status_string(int status);
+
+/* BSQ_ABI_VERSION of the loaded library. */
+BSQ_API int bsq_abi_version(void);
+
+/* Bytes of a block-scale buffer: pad128(rows) * pad4(n_blocks). */
+BSQ_API size_t bsq_scale_bytes(int64_t rows, int64_t n_blocks);
+
+/* Workspace the quantizers need for an [M, K] input (the per-CTA partial
+ * maxima of the tensor amax pass); 0 when M*K is small enough for the
+ * single-launch path.  Always 256-byte aligned sizes. */
+BSQ_API size_t bsq_quantize_workspace_bytes(int64_t M, int64_t K);
+
+/*
+ * bsq_quantize_mxfp6 -- bf16 [M, K] -> MX codes + UE8M0 block scales + s_global.
+ * b12x _lib/fp6.py: quantize_grouped_mxfp6_torch (one group) with the exact
+ * scale steps of fp6_block_ue8m0_exact and ue8m0_output_scale_exact:
+ *   amax = max|x|; gs = 448*fmt_max / amax (0 if amax == 0);
+ *   per 32-block: ue = ceil(log2(fl(fl(amax_b*gs)/fmt_max))) + 127 (exact, by
+ *   the f32 exponent field + (mantissa != 0)), clamped to [0, 255];
+ *   inv = gs * 2^(127-ue) (0 if ue == 0);
+ *   code = cvt.rn.satfinite(fl(x * inv)) (0 if inv == 0);
+ *   *s_global = fl(1/gs) (0 if gs == 0).
+ *   x        [M, K] bf16 bits, 16-byte aligned.  K % 32 == 0, M >= 1.
+ *   fmt      BSQ_E3M2 / BSQ_E2M3 (fp6, codes [M, 3K/4] bytes) or BSQ_E4M3
+ *            (codes [M, K] bytes).
+ *   scales   bsq_scale_bytes(M, K/32) bytes, written whole (padding = 0).
+ *   s_global one device float.
+ *   workspace/workspace_bytes  >= bsq_quantize_workspace_bytes(M, K) bytes of
+ *            device memory, 16-byte aligned (may be NULL when that is 0).
+ * Results are bit-identical to the CPU oracle.
+ */
+BSQ_API bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt fmt,
+                              uint8_t* codes, uint8_t* scales, float* s_global,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bsq_quantize_nvfp4 -- bf16 [M, K] -> e2m1 words + ue4m3 block scales + s_global.
+ * The pages give no nvfp4 recipe; this applies the MX recipe above with
+ * e2m1's maximum 6 and a round-to-nearest e4m3 block scale:
+ *   gs = 2688 / amax; s_b = e4m3_rn_satfinite(fl(fl(amax_b*gs)/6));
+ *   inv = fl(gs / s_b) (0 if s_b == 0); code = e2m1_rn_satfinite(fl(x*inv)).
+ *   codes  [M, K/8] uint32 words, low nibble first.  K % 16 == 0.
+ *   scales bsq_scale_bytes(M, K/16) bytes.
+ */
+BSQ_API bsq_status bsq_quantize_nvfp4(const uint16_t* x, int64_t M, int64_t K,
+                              uint32_t* codes, uint8_t* scales, float* s_global,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bsq_gemm_nvfp4 -- Y = gA*gW * A W^T with both operands nvfp4, on the 5th-gen
+ * tensor cores (tcgen05.mma kind::mxf4nvf4, ue4m3 scale per 16).
+ *   A [M, K/8] words + sA (bsq_scale_bytes(M, K/16)); W [N, K/8] + sW.
+ *   gA, gW  device floats (NULL = 1).  K % 64 == 0; M, N >= 1.
+ *   Y       [M, N] bf16 or fp32.
+ * fp32 accumulation; |Y - Y_exact| <= 1e-5 * sum_k |a_k w_k| (fp32 out).
+ */
+BSQ_API bsq_status bsq_gemm_nvfp4(const uint32_t* A, const uint8_t* sA, const float* gA,
+                          const uint32_t* W, const uint8_t* sW, const float* gW,
+                          void* Y, bsq_outtype out, int64_t M, int64_t N, int64_t K,
+                          cudaStream_t stream);
+
+/*
+ * bsq_gemm_mxfp6 -- Y = gA*gW * A W^T with MX operands (tcgen05.mma
+ * kind::mxf8f6f4, UE8M0 per 32).  Each side is e3m2, e2m3 (4-in-3 packed) or
+ * e4m3 (one byte per code), e.g. W6A6 e3m2 x e3m2 or W6A8 e4m3 x e2m3.
+ *   A [M, K*bits/8] bytes + sA (bsq_scale_bytes(M, K/32)); W [N, ...] + sW.
+ *   K % 128 == 0 (the packed-fp6 TMA unit); M, N >= 1.
+ */
+BSQ_API bsq_status bsq_gemm_mxfp6(const uint8_t* A, bsq_mxfmt fa, const uint8_t* sA, const float* gA,
+                          const uint8_t* W, bsq_mxfmt fw, const uint8_t* sW, const float* gW,
+                          void* Y, bsq_outtype out, int64_t M, int64_t N, int64_t K,
+                          cudaStream_t stream);
+
+/*
+ * bsq_gemv_nvfp4 -- decode product y = gW * x W^T with bf16 activations and an
+ * nvfp4 weight (cubecl-tile packed.rs, packed_one_row_product: one activation
+ * row, or a few, against packed weights streamed from HBM).
+ *   x [M, K] bf16, 1 <= M <= 32; W [N, K/8] words + sW; gW device float
+ *   (NULL = 1); K % 64 == 0; y [M, N] bf16 or fp32.
+ */
+BSQ_API bsq_status bsq_gemv_nvfp4(const uint16_t* x, const uint32_t* W, const uint8_t* sW, const float* gW,
+                          void* y, bsq_outtype out, int64_t M, int64_t N, int64_t K,
+                          cudaStream_t stream);
+
+/*
+ * bsq_gemv_mxfp6 -- the same decode product with an MX weight (e3m2 / e2m3
+ * 4-in-3 packed, or e4m3).  K % 128 == 0; 1 <= M <= 32.
+ */
+BSQ_API bsq_status bsq_gemv_mxfp6(const uint16_t* x, const uint8_t* W, bsq_mxfmt fw, const uint8_t* sW,
+                          const float* gW, void* y, bsq_outtype out, int64_t M, int64_t N, int64_t K,
+                          cudaStream_t stream);
+
+/*
+ * Dequantization (test and debugging aid; cubecl-tile packed.rs
+ * packed_scaled_copy, b12x _lib/fp6.py dequant_mxfp6_torch):
+ *   out[r, k] = decode(code) * scale(r, k/blk) * g   (fp32, [R, K])
+ * g: device float (NULL = 1).  UE8M0 byte 0 decodes as 2^-127.
+ */
+BSQ_API bsq_status bsq_dequant_nvfp4(const uint32_t* codes, const uint8_t* scales, const float* g,
+                             float* out, int64_t R, int64_t K, cudaStream_t stream);
+BSQ_API bsq_status bsq_dequant_mxfp6(const uint8_t* codes, bsq_mxfmt fmt, const uint8_t* scales,
+                             const float* g, float* out, int64_t R, int64_t K, cudaStream_t stream);
+
+/*
+ * Reads and clears the device error word of the current device (a bounded
+ * wait that timed out, or a device-side check).  Synchronizes the device.
+ * *code_out = 0 when nothing was recorded; otherwise a site id (nonzero).
+ * Returns BSQ_ERR_TIMEOUT / BSQ_ERR_DEVICE_CHECK when a code was recorded.
+ */
+BSQ_API bsq_status bsq_get_device_error(uint32_t* code_out);
+
+/* Launch counters (host side), one per kernel family, for dispatch tests and
+ * for counting launches in a timed region.  ids: see BSQ_KERNEL_*. */
+enum {
+    BSQ_KERNEL_AMAX = 0,
+    BSQ_KERNEL_QUANT_MX = 1,
+    BSQ_KERNEL_QUANT_NVFP4 = 2,
+    BSQ_KERNEL_QUANT_SMALL = 3,
+    BSQ_KERNEL_GEMM_NVFP4 = 4,
+    BSQ_KERNEL_GEMM_MX = 5,
+    BSQ_KERNEL_GEMV_NVFP4 = 6,
+    BSQ_KERNEL_GEMV_MX = 7,
+    BSQ_KERNEL_DEQUANT = 8,
+    BSQ_KERNEL_COUNT = 9
+};
+BSQ_API uint64_t bsq_launch_count(int kernel_id);
+BSQ_API void bsq_reset_launch_counts(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BSQ_H */

@@ -1,0 +1,93 @@
+"""GPU products against the oracle, output by output: the nvfp4 and MX
+decode GEMVs (mma.sync path) and the tcgen05 block-scaled GEMMs, on shapes that
+span several tiles and ragged tails in M, N and K, with fp32 and bf16 output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from block_scaled_precision_packed_gb300 import synthetic as S
+from tests.parity import check_products, dev_tensor, host_bytes
+
+pytestmark = pytest.mark.gpu
+
+# ue4m3 block scales spread over 2^-6 .. 2^7 with all mantissas
+UE4M3_CODES = list(range(0x08, 0x68))
+MX = {"e3m2": O.E3M2, "e2m3": O.E2M3, "e4m3": O.E4M3}
+
+
+def nvfp4_operand(R, K, seed):
+    W = S.random_words((R, K // 8), seed)
+    sc = S.choice_bytes(O.scale_bytes(R, K // 16), seed + 1, UE4M3_CODES)
+    return W, sc
+
+
+def mx_operand(R, K, fmt_name, seed):
+    """Quantized from bf16 by the oracle (the codes and scales a quantizer makes)."""
+    x = S.normal_bf16((R, K), 0.02, seed, outlier_frac=0.01)
+    return O.quantize_mx(x, MX[fmt_name])
+
+
+@pytest.mark.parametrize("M", [1, 5, 8, 13, 32])
+@pytest.mark.parametrize("N,K", [(256, 256), (300, 320), (129, 1024), (1, 64)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_gemv_nvfp4(bsq, M, N, K, out):
+    x = S.normal_bf16((M, K), 1.0, 7 + M)
+    W, sc = nvfp4_operand(N, K, 31 + N + K)
+    g = torch.tensor([0.375], device="cuda")
+    y = bsq.gemv_nvfp4(dev_tensor(x), dev_tensor(W), dev_tensor(sc), g, K, out_dtype=out)
+    want, s = O.gemv_nvfp4(x, W, sc, 0.375, M, N, K)
+    check_products(y, want, s, f"gemv_nvfp4 M{M} N{N} K{K}")
+
+
+def test_gemv_nvfp4_every_code_and_subnormal_scales(bsq):
+    """Every e2m1 code (both zeros, the 0.5 subnormal) against ue4m3 scales that
+    include e4m3 subnormals, so the exact in-register decode is exercised end to end."""
+    M, N, K = 3, 128, 512
+    x = S.normal_bf16((M, K), 1.0, 9)
+    codes = (np.arange(N * K) % 16).astype(np.uint32).reshape(N, K)
+    W = np.zeros((N, K // 8), dtype=np.uint32)
+    for j in range(8):
+        W |= codes[:, j::8] << np.uint32(4 * j)
+    sc = S.choice_bytes(O.scale_bytes(N, K // 16), 3, list(range(0x01, 0x7F)))
+    y = bsq.gemv_nvfp4(dev_tensor(x), dev_tensor(W), dev_tensor(sc), None, K, out_dtype=torch.float32)
+    want, s = O.gemv_nvfp4(x, W, sc, 1.0, M, N, K)
+    check_products(y, want, s, "gemv_nvfp4 all codes")
+
+
+@pytest.mark.parametrize("fmt", ["e3m2", "e2m3", "e4m3"])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (8, 300, 512), (32, 129, 384)])
+def test_gemv_mx(bsq, fmt, M, N, K):
+    x = S.normal_bf16((M, K), 1.0, 17 + M)
+    codes, sc, g = mx_operand(N, K, fmt, 41 + N)
+    gt = torch.tensor([g], device="cuda")
+    for out in (torch.float32, torch.bfloat16):
+        y = bsq.gemv_mxfp6(dev_tensor(x), dev_tensor(codes), fmt, dev_tensor(sc), gt, K, out_dtype=out)
+        want, s = O.gemv_mx(x, codes, MX[fmt], sc, g, M, N, K)
+        check_products(y, want, s, f"gemv_{fmt} M{M} N{N} K{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (200, 333, 320), (1, 256, 64), (256, 512, 1024),
+                                   (384, 1024, 512), (130, 4096, 256)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_gemm_nvfp4(bsq, M, N, K, out):
+    A, sA = nvfp4_operand(M, K, 51 + M)
+    W, sW = nvfp4_operand(N, K, 61 + N)
+    gA = torch.tensor([0.5], device="cuda")
+    gW = torch.tensor([0.25], device="cuda")
+    y = bsq.gemm_nvfp4(dev_tensor(A), dev_tensor(sA), gA, dev_tensor(W), dev_tensor(sW), gW, K, out_dtype=out)
+    want, s = O.gemm_nvfp4(A, sA, 0.5, W, sW, 0.25, M, N, K)
+    check_products(y, want, s, f"gemm_nvfp4 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fa,fw", [("e3m2", "e3m2"), ("e4m3", "e2m3"), ("e2m3", "e3m2"), ("e4m3", "e4m3"),
+                                   ("e3m2", "e4m3")])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 333, 384), (256, 1024, 1024), (1, 300, 256)])
+def test_gemm_mx(bsq, fa, fw, M, N, K):
+    A, sA, gA = mx_operand(M, K, fa, 71 + M)
+    W, sW, gW = mx_operand(N, K, fw, 81 + N)
+    for out in (torch.float32, torch.bfloat16):
+        y = bsq.gemm_mxfp6(dev_tensor(A), fa, dev_tensor(sA), torch.tensor([gA], device="cuda"),
+                           dev_tensor(W), fw, dev_tensor(sW), torch.tensor([gW], device="cuda"), K, out_dtype=out)
+        want, s = O.gemm_mx(A, MX[fa], sA, gA, W, MX[fw], sW, gW, M, N, K)
+        check_products(y, want, s, f"gemm_{fa}x{fw} {M}x{N}x{K}")
