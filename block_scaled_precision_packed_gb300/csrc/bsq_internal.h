@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/bsq.h"
+#include "bsq.h"
 
 namespace bsq {
 

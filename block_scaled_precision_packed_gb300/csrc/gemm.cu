@@ -8,9 +8,11 @@
 //          ue4m3 scale per 16, K = 64 per instruction (32 packed bytes).
 //   MX     tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X: e3m2 / e2m3 /
 //          e4m3 on either side, UE8M0 per 32, K = 32 per instruction.
-//          Packed fp6 rows are expanded 12 -> 16 bytes per 16 codes by the TMA
-//          unit itself (CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B), which is the
-//          shared-memory form the MMA reads for 6-bit operands.
+//          The MMA reads a 6-bit operand from shared memory as 16 codes packed
+//          in 12 bytes (the four-in-three rule) followed by 4 unused bytes;
+//          the TMA unit produces exactly that from the packed rows
+//          (CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B), counting the 96 packed
+//          bytes of a 128-code row toward the stage's transaction.
 //
 // One persistent CTA per SM, warp-specialised (192 threads):
 //   warp 0      TMA producer: A / W tiles (128-byte swizzle) and the scale
@@ -45,7 +47,6 @@ __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { retur
 template <bool NVF4, int BN>
 struct Cfg {
     static constexpr int kStages = BN == 256 ? 4 : 6;
-    static constexpr int kMmaPerStage = 4;                       // 4 x 32 bytes of K per row
     static constexpr int kStageK = NVF4 ? 256 : 128;             // elements of K per stage
     static constexpr int kAtomsPerStage = NVF4 ? 4 : 1;          // scale atoms along K per 128 rows
     static constexpr int kRowTilesB = BN / 128;
@@ -72,6 +73,7 @@ struct GemmArgs {
     int64_t cpd4;          // scale atoms along K per 128-row tile (pad4(blocks)/4)
     int out_bf16;
     uint32_t idesc;        // instruction descriptor without the scale-id fields
+    uint32_t tx_ab;        // TMA transaction bytes of one stage's A and W tiles
     uint32_t* err;
 };
 
@@ -140,7 +142,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     }
                     const int64_t kg = ks * C::kAtomsPerStage;             // first scale atom along K
                     const int natoms = (int)imin64(C::kAtomsPerStage, args.cpd4 - kg);
-                    const uint32_t bytes = C::kABytes + C::kBBytes + (uint32_t)natoms * kAtom * (1 + C::kRowTilesB);
+                    const uint32_t bytes = args.tx_ab + (uint32_t)natoms * kAtom * (1 + C::kRowTilesB);
                     const uint32_t fb = smem_u32(full + stage);
                     mbar_arrive_expect_tx(fb, bytes);
                     const int32_t kx = (int32_t)(ks * (NVF4 ? 128 : C::kStageK));   // bytes (nvfp4) / elements
@@ -377,6 +379,10 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
     a.out_bf16 = out == BSQ_OUT_BF16;
     a.idesc = make_idesc(nvf4, fa, fw, bn);
     a.err = info->err;
+    // A 16U6_ALIGN16B load lands 128 bytes per 128-code row in shared memory but
+    // counts the 96 packed bytes it read toward the transaction.
+    auto row_tx = [&](int f) { return (uint32_t)(nvf4 || f == kE4M3 ? 128 : 96); };
+    a.tx_ab = kBM * row_tx(fa) + (uint32_t)bn * row_tx(fw);
     bsq_status r;
     if (nvf4) r = bn == 256 ? launch_gemm<true, 256>(info, ta, tw, a, s) : launch_gemm<true, 128>(info, ta, tw, a, s);
     else r = bn == 256 ? launch_gemm<false, 256>(info, ta, tw, a, s) : launch_gemm<false, 128>(info, ta, tw, a, s);

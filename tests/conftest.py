@@ -29,3 +29,17 @@ def bsq():
     from block_scaled_precision_packed_gb300 import bsq as b
     b.load()
     return b
+
+
+@pytest.fixture(autouse=True)
+def _clean_device_error_word(request):
+    """After every GPU test: no bounded wait timed out and no device check fired."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    if not torch.cuda.is_available():
+        return
+    from block_scaled_precision_packed_gb300 import bsq as b
+    st, code = b.device_error()
+    assert st == 0 and code == 0, f"device error word set: status {st}, site 0x{code:x}"
