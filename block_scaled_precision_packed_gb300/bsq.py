@@ -51,6 +51,7 @@ def load(path: str | None = None):
             "bsq_quantize_workspace_bytes": (sz, [i64, i64]),
             "bsq_quantize_mxfp6": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_nvfp4": (i32, [vp, i64, i64, vp, vp, vp, vp, sz, vp]),
+            "bsq_quantize_mxfp6_noalloc": (i32, [vp, i64, i64, i32, vp, vp, vp, vp]),
             "bsq_gemm_nvfp4": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, vp]),
             "bsq_gemm_mxfp6": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, vp, i32, i64, i64, i64, vp]),
             "bsq_gemv_nvfp4": (i32, [vp, vp, vp, vp, vp, i32, i64, i64, i64, vp]),
@@ -101,6 +102,13 @@ def quantize_mxfp6_(x, fmt, codes, scales, s_global, workspace=None, stream=None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("bsq_quantize_mxfp6", load().bsq_quantize_mxfp6(
         _p(x), M, K, fmt, _p(codes), _p(scales), _p(s_global), _p(workspace), ws_bytes, _stream(stream)))
+
+
+def quantize_mxfp6_noalloc_(x, fmt, codes, scales, s_global, stream=None):
+    """The allocation-free quantizer entry point (no workspace argument)."""
+    M, K = x.shape
+    _check("bsq_quantize_mxfp6_noalloc", load().bsq_quantize_mxfp6_noalloc(
+        _p(x), M, K, fmt, _p(codes), _p(scales), _p(s_global), _stream(stream)))
 
 
 def quantize_nvfp4_(x, codes, scales, s_global, workspace=None, stream=None):

@@ -20,6 +20,7 @@
 // warp's load is 512 contiguous bytes.  A 32-value MX block is four lanes (a
 // quad), a 16-value nvfp4 block two lanes; the block amax is a shuffle.
 #include <cstdio>
+#include <mutex>
 
 #include "bsq_device.cuh"
 #include "bsq_internal.h"
@@ -362,3 +363,81 @@ bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32
 }
 
 }  // namespace bsq
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of bsq_quantize_mxfp6.
+//
+// Some callers cannot allocate device memory on this path: a plugin whose host
+// framework owns all device memory and forbids cudaMalloc while it executes, or
+// a latency-critical loop where an allocation (and the synchronization it
+// implies) is not acceptable.  This entry point keeps the large-tensor path's
+// scratch -- the per-CTA partial maxima of the amax pass -- in a file-scope
+// device array instead of a caller-provided workspace.
+//
+// The array (kMaxPartials words, 4 KiB) lives on every GPU that loads the
+// library until the process exits.  Its device address is looked up once per
+// device, with that device current, by the first call on that device (host
+// code cannot use the array's name as a device address).  Every call shares
+// the array: the amax pass rewrites each slot the encode pass reads, so nothing
+// needs clearing, but two calls whose kernels overlap on the GPU (for example
+// on two streams) race on it.
+// ---------------------------------------------------------------------------
+namespace bsq {
+namespace {
+
+static __device__ __align__(256) uint32_t g_noalloc_partials[kMaxPartials];
+
+constexpr int kNoallocMaxDevices = 64;
+std::once_flag g_noalloc_once[kNoallocMaxDevices];
+uint32_t* g_noalloc_ptr[kNoallocMaxDevices];
+
+// Device address of the scratch array on the current device (nullptr on error).
+uint32_t* noalloc_scratch() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) return nullptr;
+    std::call_once(g_noalloc_once[dev], [dev] {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_partials) == cudaSuccess) g_noalloc_ptr[dev] = static_cast<uint32_t*>(p);
+        else (void)cudaGetLastError();
+    });
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace bsq
+
+extern "C" BSQ_API bsq_status bsq_quantize_mxfp6_noalloc(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt fmt,
+                                                        uint8_t* codes, uint8_t* scales, float* s_global,
+                                                        cudaStream_t stream) {
+    using namespace bsq;
+    if (!x || !codes || !scales || !s_global || (fmt != BSQ_E3M2 && fmt != BSQ_E2M3 && fmt != BSQ_E4M3))
+        return BSQ_ERR_INVALID_ARG;
+    if (M < 1 || K < 32 || K % 32 || M >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return BSQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return BSQ_ERR_MISALIGNED;
+    if (M * K <= kFusedMaxElems)    // the single cluster launch needs no scratch
+        return quantize_mx_launch(x, M, K, fmt, codes, scales, s_global, nullptr, 0, stream);
+    bsq_status st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
+    uint32_t* scratch = noalloc_scratch();
+    if (!scratch) return BSQ_ERR_CUDA;
+    const int n_partial = amax_grid(info, M * K);
+    if (n_partial > kMaxPartials) return BSQ_ERR_UNSUPPORTED;   // more partial maxima than the array holds
+    amax_partial_kernel<<<n_partial, kThreads, 0, stream>>>(reinterpret_cast<const uint4*>(x), M * K / 8, scratch);
+    count_launch(BSQ_KERNEL_AMAX);
+    if (launch_status() != BSQ_OK) return BSQ_ERR_CUDA;
+    const int grid = encode_grid(info, M, K);
+    switch (fmt) {
+    case BSQ_E3M2:
+        quant_mx_kernel<kE3M2, false><<<grid, kThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        break;
+    case BSQ_E2M3:
+        quant_mx_kernel<kE2M3, false><<<grid, kThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        break;
+    default:
+        quant_mx_kernel<kE4M3, false><<<grid, kThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        break;
+    }
+    count_launch(BSQ_KERNEL_QUANT_MX);
+    return launch_status();
+}

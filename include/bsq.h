@@ -108,6 +108,23 @@ BSQ_API bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, b
                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * bsq_quantize_mxfp6_noalloc -- bsq_quantize_mxfp6 for callers that cannot
+ * allocate device memory on this path (no counterpart on the pages; this is a
+ * library convenience).  Same arguments, results and validation minus the
+ * workspace: the large-tensor path keeps its scratch (the amax pass's partial
+ * maxima) in a 4 KiB device array owned by the library, present on every GPU
+ * that loads it until the process exits.  The array holds 1024 partial maxima;
+ * the amax pass never launches more CTAs than that, so every size the checks
+ * above accept fits, and a call that would need more returns
+ * BSQ_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
+ * address (make it before any stream capture).  Calls share the array: two
+ * calls whose kernels overlap on the GPU race on it.  Calls no allocator.
+ */
+BSQ_API bsq_status bsq_quantize_mxfp6_noalloc(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt fmt,
+                                      uint8_t* codes, uint8_t* scales, float* s_global,
+                                      cudaStream_t stream);
+
+/*
  * bsq_quantize_nvfp4 -- bf16 [M, K] -> e2m1 words + ue4m3 block scales + s_global.
  * The pages give no nvfp4 recipe; this applies the MX recipe above with
  * e2m1's maximum 6 and a round-to-nearest e4m3 block scale:
