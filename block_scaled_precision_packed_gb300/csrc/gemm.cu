@@ -14,14 +14,16 @@
 //          (CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B), counting the 96 packed
 //          bytes of a 128-code row toward the stage's transaction.
 //
-// One persistent CTA per SM, warp-specialised (192 threads):
+// One persistent CTA per SM, warp-specialised (320 threads):
 //   warp 0      TMA producer: A / W tiles (128-byte swizzle) and the scale
 //               atoms (plain bulk copies) into an S-stage shared-memory ring.
 //   warp 1      owns the TMEM allocation; one lane issues tcgen05.cp (scale
 //               atoms -> TMEM) and tcgen05.mma, and commits each stage back to
 //               the producer and each finished tile to the epilogue.
-//   warps 2-5   epilogue: tcgen05.ld the 128 x BN fp32 accumulator, scale by
-//               gA*gW, convert, store.
+//   warps 2-9   epilogue (two warps per TMEM lane quarter, one per column
+//               half): tcgen05.ld the 128 x BN fp32 accumulator, scale by
+//               gA*gW, convert; for bf16 output the whole tile is held in
+//               registers so TMEM is released before the stores start.
 // Every wait is bounded (2 s); a timeout records its site in the device error
 // word, drains the copies in flight, frees TMEM and returns.
 //
@@ -38,7 +40,8 @@ namespace bsq {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;     // producer warp, MMA warp, 8 epilogue warps
+constexpr int kEpiThreads = 256;
 constexpr int kAtom = 512;          // bytes of one 128-row x 4-block scale atom
 constexpr uint32_t kTmemCols = 512;
 
@@ -77,7 +80,29 @@ struct GemmArgs {
     uint32_t* err;
 };
 
-template <bool NVF4, int BN>
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    float4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote));
+    return v;
+}
+
+// SPLIT == 1: persistent, one CTA per SM, tiles strided over the grid.
+// SPLIT  > 1: split-K; a cluster of SPLIT CTAs owns one output tile, CTA rank r
+//            runs K stages [r*S/SPLIT, (r+1)*S/SPLIT), and the fp32 partial
+//            tiles are summed (rank order, deterministic) through distributed
+//            shared memory -- no workspace, no atomics.
+template <bool NVF4, int BN, int SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const GemmArgs args) {
     using C = Cfg<NVF4, BN>;
@@ -100,8 +125,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int64_t M = args.M, N = args.N, K = args.K;
     const int64_t num_mb = (M + kBM - 1) / kBM, num_nb = (N + BN - 1) / BN;
     const int64_t num_tiles = num_mb * num_nb;
-    const int64_t nks = (K + C::kStageK - 1) / C::kStageK;
+    const int64_t nks_all = (K + C::kStageK - 1) / C::kStageK;
     const int64_t rt_total = pad_to(N, 128) / 128;   // 128-row scale tiles of W
+    const uint32_t krank = SPLIT > 1 ? cluster_rank() : 0u;
+    const int64_t ks_begin = nks_all * krank / SPLIT, ks_end = nks_all * (krank + 1) / SPLIT;
+    const int64_t tile_first = SPLIT > 1 ? (int64_t)(blockIdx.x / SPLIT) : (int64_t)blockIdx.x;
+    const int64_t tile_step = SPLIT > 1 ? num_tiles : (int64_t)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -109,7 +138,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(smem_u32(empty + s), 1);
         }
         mbar_init(smem_u32(acc_full), 1);
-        mbar_init(smem_u32(acc_empty), 4 * 32);
+        mbar_init(smem_u32(acc_empty), kEpiThreads);
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -133,9 +162,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             uint32_t issued_parity[8] = {0};
             bool issued_any[8] = {false};
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int64_t tile = tile_first; tile < num_tiles && ok; tile += tile_step) {
                 const int64_t mb = tile % num_mb, nb = tile / num_mb;
-                for (int64_t ks = 0; ks < nks; ++ks) {
+                for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
                     if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, args.err, abort_flag, kErrGemmProducer)) {
                         ok = false;
                         break;
@@ -178,10 +207,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int64_t tile = tile_first; tile < num_tiles && ok; tile += tile_step) {
                 if (!mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, args.err, abort_flag, kErrGemmMma)) break;
                 tc_fence_after();
-                for (int64_t ks = 0; ks < nks; ++ks) {
+                for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
                     if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
                         ok = false;
                         break;
@@ -206,7 +235,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     for (int kk = 0; kk < n_mma; ++kk) {
                         const uint64_t ad = smem_desc(a_base + 32 * kk, 16, 1024, 2);
                         const uint64_t bd = smem_desc(b_base + 32 * kk, 16, 1024, 2);
-                        const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t acc = (ks > ks_begin || kk > 0) ? 1u : 0u;
                         if constexpr (NVF4) {
                             tc_mma_mxf4nvf4(tmem, ad, bd, args.idesc, tmem + sf_col + 4 * kk,
                                             tmem + sf_col + C::kSfaCols + kk * C::kRowTilesB * 4, acc);
@@ -232,20 +261,87 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else {
         // ------------------------------------------------------- epilogue --
         const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const int half = (warp - 2) >> 2;             // which half of the tile's columns
+        constexpr int kHalf = BN / 2;
         const float f = __fmul_rn(args.gA ? __ldg(args.gA) : 1.0f, args.gW ? __ldg(args.gW) : 1.0f);
         uint32_t acc_phase = 0;
         const bool vec = args.out_bf16 ? (N % 8 == 0) : (N % 4 == 0);
-        for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        if constexpr (SPLIT > 1) {
+            // Partial tile -> this CTA's shared memory (the operand ring is idle:
+            // the single tile's last MMA has completed), then sum across the
+            // cluster, each CTA finishing kBM/SPLIT rows.
+            const int64_t tile = tile_first;
+            const int64_t mb = tile % num_mb, nb = tile / num_mb;
+            float* part = reinterpret_cast<float*>(smem);               // [kBM][BN + 4] fp32
+            constexpr int kPitch = BN + 4;
+            const bool have = mbar_wait(smem_u32(acc_full), 0, args.err, abort_flag, kErrGemmEpilogue);
+            if (have) {
+                tc_fence_after();
+                const int lrow = 32 * q + lane;
+#pragma unroll 1
+                for (int c = 0; c < kHalf / 32; ++c) {
+                    uint32_t r[32];
+                    tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kHalf * half + 32 * c), r);
+                    tc_wait_ld();
+                    float4* dst = reinterpret_cast<float4*>(part + lrow * kPitch + kHalf * half + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                             __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                }
+                tc_fence_before();
+            }
+        }
+        for (int64_t tile = tile_first; tile < num_tiles && SPLIT == 1; tile += tile_step) {
             const int64_t mb = tile % num_mb, nb = tile / num_mb;
             if (!mbar_wait(smem_u32(acc_full), acc_phase, args.err, abort_flag, kErrGemmEpilogue)) break;
             tc_fence_after();
             const int64_t row = mb * kBM + 32 * q + lane;
+            if (args.out_bf16) {
+                // Drain the whole accumulator row into registers as bf16 pairs,
+                // hand TMEM back to the MMA warp, then store: the next tile's
+                // MMAs overlap these stores.
+                uint32_t packed[kHalf / 2];
+#pragma unroll
+                for (int c = 0; c < kHalf / 32; ++c) {
+                    uint32_t r0[32];
+                    tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kHalf * half + 32 * c), r0);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        packed[16 * c + e] = (uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r0[2 * e]), f)) |
+                                             ((uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r0[2 * e + 1]), f)) << 16);
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(acc_empty));
+                acc_phase ^= 1;
+                if (row < M) {
+                    uint16_t* yr = static_cast<uint16_t*>(args.Y) + row * N + nb * BN + kHalf * half;
+#pragma unroll
+                    for (int c = 0; c < kHalf / 32; ++c) {
+                        const int64_t col0 = nb * BN + kHalf * half + 32 * c;
+                        if (vec && col0 + 32 <= N) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                *reinterpret_cast<uint4*>(yr + 32 * c + 8 * v) =
+                                    make_uint4(packed[16 * c + 4 * v], packed[16 * c + 4 * v + 1],
+                                               packed[16 * c + 4 * v + 2], packed[16 * c + 4 * v + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (col0 + e < N)
+                                    yr[32 * c + e] = (uint16_t)(packed[16 * c + e / 2] >> (16 * (e & 1)));
+                        }
+                    }
+                }
+                continue;
+            }
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < kHalf / 32; ++c) {
                 uint32_t r[32];
-                tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * c), r);
+                tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kHalf * half + 32 * c), r);
                 tc_wait_ld();
-                const int64_t col0 = nb * BN + 32 * c;
+                const int64_t col0 = nb * BN + kHalf * half + 32 * c;
                 if (row < M && col0 < N) {
                     if (args.out_bf16) {
                         uint16_t* yr = static_cast<uint16_t*>(args.Y) + row * N + col0;
@@ -287,6 +383,46 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
     }
 
+    if constexpr (SPLIT > 1) {
+        __syncwarp();                                     // reconverge the role warps first
+        cluster_sync();                                   // every rank's partial tile is in its smem
+        const int64_t tile = tile_first;
+        const int64_t mb = tile % num_mb, nb = tile / num_mb;
+        constexpr int kPitch = BN + 4;
+        constexpr int kRows = kBM / SPLIT;
+        const float f = __fmul_rn(args.gA ? __ldg(args.gA) : 1.0f, args.gW ? __ldg(args.gW) : 1.0f);
+        const uint32_t part = smem_u32(smem);
+        for (int it = threadIdx.x; it < kRows * (BN / 4); it += kThreads) {
+            const int lr = (int)krank * kRows + it / (BN / 4), cg = it % (BN / 4);
+            const uint32_t off = (uint32_t)((lr * kPitch + 4 * cg) * 4);
+            float4 v[SPLIT];
+#pragma unroll
+            for (int rk = 0; rk < SPLIT; ++rk) v[rk] = ld_dsmem_f4(part + off, rk);   // all in flight at once
+            float4 acc = v[0];
+#pragma unroll
+            for (int rk = 1; rk < SPLIT; ++rk) {
+                acc.x += v[rk].x; acc.y += v[rk].y; acc.z += v[rk].z; acc.w += v[rk].w;
+            }
+            const int64_t row = mb * kBM + lr, col = nb * BN + 4 * cg;
+            if (row >= M || col >= N) continue;
+            const float o[4] = {__fmul_rn(acc.x, f), __fmul_rn(acc.y, f), __fmul_rn(acc.z, f), __fmul_rn(acc.w, f)};
+            if (args.out_bf16) {
+                uint16_t* y = static_cast<uint16_t*>(args.Y) + row * N + col;
+                if (col + 4 <= N && (N % 4) == 0) {
+                    *reinterpret_cast<uint2*>(y) =
+                        make_uint2((uint32_t)f32_to_bf16_bits(o[0]) | ((uint32_t)f32_to_bf16_bits(o[1]) << 16),
+                                   (uint32_t)f32_to_bf16_bits(o[2]) | ((uint32_t)f32_to_bf16_bits(o[3]) << 16));
+                } else {
+                    for (int e = 0; e < 4 && col + e < N; ++e) y[e] = f32_to_bf16_bits(o[e]);
+                }
+            } else {
+                float* y = static_cast<float*>(args.Y) + row * N + col;
+                if (col + 4 <= N && (N % 4) == 0) *reinterpret_cast<float4*>(y) = make_float4(o[0], o[1], o[2], o[3]);
+                else for (int e = 0; e < 4 && col + e < N; ++e) y[e] = o[e];
+            }
+        }
+        cluster_sync();                                   // no rank leaves while others read its smem
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -338,7 +474,7 @@ bool operand_map(CUtensorMap* map, const void* p, int fmt, bool nvf4, int64_t ro
                       (uint64_t)(3 * K / 4), 128, box_rows);
 }
 
-template <bool NVF4, int BN>
+template <bool NVF4, int BN, int SPLIT>
 bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a,
                        cudaStream_t s) {
     using C = Cfg<NVF4, BN>;
@@ -348,14 +484,34 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     if (dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
     bool attr_ok = true;
     std::call_once(flags[dev], [&] {
-        attr_ok = cudaFuncSetAttribute(gemm_kernel<NVF4, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_ok = cudaFuncSetAttribute(gemm_kernel<NVF4, BN, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes) == cudaSuccess;
     });
     if (!attr_ok) return BSQ_ERR_CUDA;
     const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
-    const int grid = (int)imin64(tiles, info->num_sms);
-    gemm_kernel<NVF4, BN><<<grid, kThreads, C::kSmemBytes, s>>>(ta, tw, a);
-    return launch_status();
+    if constexpr (SPLIT == 1) {
+        const int grid = (int)imin64(tiles, info->num_sms);
+        gemm_kernel<NVF4, BN, 1><<<grid, kThreads, C::kSmemBytes, s>>>(ta, tw, a);
+        return launch_status();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(tiles * SPLIT), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = SPLIT;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, gemm_kernel<NVF4, BN, SPLIT>, ta, tw, a) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return BSQ_ERR_CUDA;
+        }
+        return BSQ_OK;
+    }
 }
 
 }  // namespace
@@ -366,9 +522,16 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
     bsq_status st;
     const DeviceInfo* info = device_info(&st);
     if (!info) return st;
-    // BN = 256 when that still gives every SM a tile, else 128.
+    // BN = 256 when that still gives every SM a tile, else 128; when even the
+    // 128-wide tiles leave most SMs idle, split K across a cluster.
     const int64_t tiles256 = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
+    const int64_t tiles128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
     const int bn = tiles256 >= info->num_sms ? 256 : 128;
+    const int64_t nks = (K + (nvf4 ? 255 : 127)) / (nvf4 ? 256 : 128);
+    int split = 1;
+    if (bn == 128)
+        for (int sp = 8; sp >= 2; sp /= 2)
+            if (tiles128 * sp <= info->num_sms && nks >= sp) { split = sp; break; }
     CUtensorMap ta, tw;
     if (!operand_map(&ta, A, fa, nvf4, M, K, kBM) || !operand_map(&tw, W, fw, nvf4, N, K, (uint32_t)bn))
         return BSQ_ERR_CUDA;
@@ -384,8 +547,19 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
     auto row_tx = [&](int f) { return (uint32_t)(nvf4 || f == kE4M3 ? 128 : 96); };
     a.tx_ab = kBM * row_tx(fa) + (uint32_t)bn * row_tx(fw);
     bsq_status r;
-    if (nvf4) r = bn == 256 ? launch_gemm<true, 256>(info, ta, tw, a, s) : launch_gemm<true, 128>(info, ta, tw, a, s);
-    else r = bn == 256 ? launch_gemm<false, 256>(info, ta, tw, a, s) : launch_gemm<false, 128>(info, ta, tw, a, s);
+    if (nvf4) {
+        if (bn == 256) r = launch_gemm<true, 256, 1>(info, ta, tw, a, s);
+        else if (split == 8) r = launch_gemm<true, 128, 8>(info, ta, tw, a, s);
+        else if (split == 4) r = launch_gemm<true, 128, 4>(info, ta, tw, a, s);
+        else if (split == 2) r = launch_gemm<true, 128, 2>(info, ta, tw, a, s);
+        else r = launch_gemm<true, 128, 1>(info, ta, tw, a, s);
+    } else {
+        if (bn == 256) r = launch_gemm<false, 256, 1>(info, ta, tw, a, s);
+        else if (split == 8) r = launch_gemm<false, 128, 8>(info, ta, tw, a, s);
+        else if (split == 4) r = launch_gemm<false, 128, 4>(info, ta, tw, a, s);
+        else if (split == 2) r = launch_gemm<false, 128, 2>(info, ta, tw, a, s);
+        else r = launch_gemm<false, 128, 1>(info, ta, tw, a, s);
+    }
     count_launch(nvf4 ? BSQ_KERNEL_GEMM_NVFP4 : BSQ_KERNEL_GEMM_MX);
     return r;
 }
