@@ -17,8 +17,12 @@ bf16 out) -- every row of the hot path this workload exercises.
   cpu_baseline  the CPU oracle on a bounded sample of the same step, extrapolated.
 
 Other workloads (--workload) measure the decode GEMV, the nvfp4 prefill GEMM
-and the W6A8 GEMM the same way.  L2 is flushed (a 256 MiB write) before every
-timed step; each step is timed with CUDA events on the launching stream.
+and the W6A8 GEMM the same way.  L2 is flushed before every timed step (a
+256 MiB write, then a 256 MiB read of another buffer so no dirty lines remain).
+The step is captured once as a CUDA graph with event nodes at its two ends and
+replayed (device time).  A second capture with an event node after every op,
+replayed after the timed steps, gives the per-op split and the dominant op's
+duration for the roofline.
 """
 from __future__ import annotations
 
@@ -254,39 +258,81 @@ def run_bsq(args, rank, world, dev_index):
     wl = Workload(args.workload, dev, gemv_m=args.gemv_m)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    # after the write, a read of a second buffer of the same size leaves L2
+    # holding clean lines, so the step does not pay for the flush's write-backs
+    flush_b = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
     dist = None
     if world > 1:
         import torch.distributed as dist
     ops = wl.ops()
 
+    # The step is captured once as a CUDA graph and replayed: the timed region
+    # measures device time, not the host's launch rate.  The timed graph has
+    # event nodes only at its two ends; a second capture with an event node
+    # after every op, replayed for the same number of steps after the timed
+    # region, gives the per-op split (its event nodes add a little time per op,
+    # so the split slightly overstates each op).  The L2 flush runs outside the
+    # graphs, before every step.
+    n_ops = len(ops)
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            flush.fill_(i)
-            wl.step(stream)
+        for i in range(2):
+            wl.step(stream)                     # loads kernels before capture
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, L2 flushed before each, per-op events ----
-    n_ops = len(ops)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ops)]
-          for _ in range(args.steps)]
+    def capture(per_op):
+        # external events become event-record nodes inside the captured graph
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ops + 1)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            evs[0].record(stream)
+            for j, (_, fn, *_r) in enumerate(ops):
+                fn(stream)
+                if per_op or j == n_ops - 1:
+                    evs[j + 1].record(stream)
+        return graph, evs
+
     bsq.reset_launch_counts()
+    graph, evs = capture(False)
+    launches_per_step = sum(bsq.launch_count(k) for k in bsq.KERNEL_IDS)
+    graph_ops, evs_ops = capture(True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            for g in (graph, graph_ops):
+                flush.fill_(i)
+                g.replay()
+    torch.cuda.synchronize()
+
+    def flushed_replay(g, i):
+        with torch.cuda.stream(stream):
+            flush.fill_(i + 1000)
+            torch.sum(flush_b, dim=0, dtype=torch.int64, out=flush_sink)
+            g.replay()
+        stream.synchronize()
+
+    # ---- timed region: K steps, L2 flushed before each ----
+    step_ms_all = np.zeros(args.steps)
+    op_ms = np.zeros((args.steps, n_ops))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev_index) as clk:
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                flush.fill_(i + 1000)
-                for j, (_, fn, *_r) in enumerate(ops):
-                    ev[i][j][0].record(stream)
-                    fn(stream)
-                    ev[i][j][1].record(stream)
+        for i in range(args.steps):
+            flushed_replay(graph, i)
+            step_ms_all[i] = evs[0].elapsed_time(evs[n_ops])
         torch.cuda.synchronize()
-    launches = sum(bsq.launch_count(k) for k in bsq.KERNEL_IDS)
+        if dist:
+            dist.barrier()
+        # per-op split (same flush, the instrumented capture)
+        for i in range(args.steps):
+            flushed_replay(graph_ops, i)
+            for j in range(n_ops):
+                op_ms[i, j] = evs_ops[j].elapsed_time(evs_ops[j + 1])
+        torch.cuda.synchronize()
+    launches = launches_per_step * args.steps
     if dist:
         dist.barrier()
-    op_ms = np.array([[ev[i][j][0].elapsed_time(ev[i][j][1]) for j in range(n_ops)] for i in range(args.steps)])
-    step_ms = float(op_ms.sum(axis=1).mean())
+    step_ms = float(step_ms_all.mean())
     if dist:
         t = torch.tensor([step_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -466,7 +512,9 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["step_ms"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(args.workload),
             "data": "synthetic (seeded; shapes and distributions of the workload)",
-            "config": dict(wl_cfg, l2="flushed (256 MiB write) before every timed step",
+            "config": dict(wl_cfg, l2="flushed before every timed step (256 MiB write, then a read pass)",
+                           timing="step captured as a CUDA graph (event nodes at its ends only) and replayed; "
+                                  "per-op split from a second capture with an event node after each op",
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "roofline": r["roofline"], "per_op_us": r["per_op_us"], "e2e": r["e2e"],
             "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "cpu_baseline": cpu}

@@ -42,6 +42,8 @@ enum ErrorSite : uint32_t {
     kErrGemmDrain = 0x104,
     kErrGemvProducer = 0x201,
     kErrGemvConsumer = 0x202,
+    kErrQuantLoad = 0x301,
+    kErrQuantBarrier = 0x302,
 };
 
 // Wall-clock bound of every spin-wait in these kernels (ns).

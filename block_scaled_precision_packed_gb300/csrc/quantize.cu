@@ -7,18 +7,19 @@
 // with e2m1's maximum and a round-to-nearest e4m3 block scale).
 //
 // Two launch shapes:
-//  * small tensors (M*K <= kFusedMaxElems): ONE launch of a thread-block
+//  * small tensors (M*K <= kFusedMaxElems): ONE launch of a 16-CTA thread-block
 //    cluster.  Each CTA reduces the amax of its slice, the cluster exchanges
 //    the partial maxima through distributed shared memory, and every CTA then
 //    encodes its share of the blocks.  No workspace, no grid-wide wait.
 //  * large tensors: an amax pass writes per-CTA partial maxima to the caller's
 //    workspace; the encode pass reduces them (a few hundred words) in every
-//    CTA and encodes.  The second read of x is normally an L2 hit.
+//    CTA and encodes.  The second read of x is normally an L2 hit.  The encode
+//    pass is a programmatic dependent launch: it is scheduled while the amax
+//    pass runs and waits for it (griddepcontrol) before reading the partials.
 //
-// Encode mapping: one warp per (row, 1024-element chunk).  Lane l loads 16
-// contiguous bytes (8 values) per step j (0..3) at element 256*j + 8*l, so a
-// warp's load is 512 contiguous bytes.  A 32-value MX block is four lanes (a
-// quad), a 16-value nvfp4 block two lanes; the block amax is a shuffle.
+// Encode mapping: one warp per (row, 1024-element chunk); each lane owns 32
+// consecutive values (one MX block, or two nvfp4 blocks) = 64 contiguous bytes,
+// so the block amax and scale math run once per 32 values without shuffles.
 #include <cstdio>
 #include <mutex>
 
@@ -28,11 +29,11 @@
 namespace bsq {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kMaxPartials = 1024;
-constexpr int64_t kFusedMaxElems = 262144;   // 512 KB of bf16
-constexpr int kFusedCluster = 8;
+constexpr int kThreads = 256;                // amax pass and the fused cluster launch
+constexpr int kEncThreads = 1024;            // encode pass: one CTA per SM
+constexpr int kMaxPartials = 2048;
+constexpr int64_t kFusedMaxElems = 1 << 16;    // 128 KiB of bf16
+constexpr int kFusedCluster = 16;   // non-portable size; 8 where 16 is refused
 
 // Largest |bf16| magnitude bits among the 8 values of a 16-byte load.
 // For non-NaN bf16, (bits & 0x7FFF) orders like |value|.
@@ -56,16 +57,29 @@ __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
     __syncthreads();
     if (lane == 0) red[warp] = v;
     __syncthreads();
-    v = lane < kWarps ? red[lane] : 0u;
+    v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
     return warp_max(v);
 }
+
+// Lets the dependent encode pass (launched with programmatic stream
+// serialization) start its launch now; it waits for this grid's completion
+// before reading the partials.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisite_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads) amax_partial_kernel(const uint4* __restrict__ x, int64_t n8,
                                                                 uint32_t* __restrict__ partial) {
     __shared__ uint32_t red[32];
+    launch_dependents();
     uint32_t m = 0;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n8; i += (int64_t)gridDim.x * kThreads)
-        m = max(m, absmax8_bits(__ldg(x + i)));
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n8; i += 8 * stride) {
+        uint4 v[8];                                   // eight 16-byte loads in flight per thread
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = i + u * stride < n8 ? __ldg(x + i + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m = max(m, absmax8_bits(v[u]));
+    }
     m = block_max(m, red);
     if (threadIdx.x == 0) partial[blockIdx.x] = m;
 }
@@ -103,7 +117,13 @@ __device__ __forceinline__ uint32_t tensor_amax_bits(const uint16_t* __restrict_
         const int64_t lo = n8 * rank / csize, hi = n8 * (rank + 1) / csize;
         const uint4* x4 = reinterpret_cast<const uint4*>(x);
         uint32_t m = 0;
-        for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) m = max(m, absmax8_bits(__ldg(x4 + i)));
+        const int64_t bd = blockDim.x;
+        int64_t i = lo + threadIdx.x;
+        for (; i + 3 * bd < hi; i += 4 * bd) {
+            const uint4 a = __ldg(x4 + i), b = __ldg(x4 + i + bd), c = __ldg(x4 + i + 2 * bd), d = __ldg(x4 + i + 3 * bd);
+            m = max(m, max(max(absmax8_bits(a), absmax8_bits(b)), max(absmax8_bits(c), absmax8_bits(d))));
+        }
+        for (; i < hi; i += bd) m = max(m, absmax8_bits(__ldg(x4 + i)));
         m = block_max(m, red);
         if (threadIdx.x == 0) *xchg = m;
         cluster_sync();                              // every CTA's partial is visible
@@ -113,8 +133,9 @@ __device__ __forceinline__ uint32_t tensor_amax_bits(const uint16_t* __restrict_
         cluster_sync();                              // no CTA leaves while others read it
         return all;
     } else {
+        wait_prerequisite_grid();
         uint32_t m = 0;
-        for (int i = threadIdx.x; i < n_partial; i += kThreads) m = max(m, __ldg(partial + i));
+        for (int i = threadIdx.x; i < n_partial; i += blockDim.x) m = max(m, partial[i]);
         return block_max(m, red);
     }
 }
@@ -122,9 +143,110 @@ __device__ __forceinline__ uint32_t tensor_amax_bits(const uint16_t* __restrict_
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// ------------------------------------------------------- per-block encode ----
+// Largest |bf16| magnitude bits among the 32 values of one 64-byte unit.
+__device__ __forceinline__ uint32_t absmax32_bits(const uint4 (&v)[4]) {
+    const uint32_t m = 0x7FFF7FFFu;
+    const uint32_t a = __vmaxu2(__vmaxu2(v[0].x & m, v[0].y & m), __vmaxu2(v[0].z & m, v[0].w & m));
+    const uint32_t b = __vmaxu2(__vmaxu2(v[1].x & m, v[1].y & m), __vmaxu2(v[1].z & m, v[1].w & m));
+    const uint32_t c = __vmaxu2(__vmaxu2(v[2].x & m, v[2].y & m), __vmaxu2(v[2].z & m, v[2].w & m));
+    const uint32_t d = __vmaxu2(__vmaxu2(v[3].x & m, v[3].y & m), __vmaxu2(v[3].z & m, v[3].w & m));
+    const uint32_t e = __vmaxu2(__vmaxu2(a, b), __vmaxu2(c, d));
+    return max(e & 0xFFFFu, e >> 16);
+}
+
+// MX block scale from the block's amax (bf16 magnitude bits): the UE8M0 byte by
+// the exact ceil rule and the encode multiplier inv = gs * 2^(127-ue).
+template <int FMT>
+__device__ __forceinline__ void mx_block_scale(uint32_t amax_bits, float gs, uint32_t& ue, float& inv) {
+    ue = 0;
+    inv = 0.0f;
+    if (gs != 0.0f) {
+        ue = ue8m0_from_block_max(bf16_bits_to_f32(amax_bits), gs, fmt_max(FMT));
+        inv = ue8m0_output_scale(ue, gs);
+    }
+}
+
+// The 32 codes of one MX block as output words: 6 (fp6, four codes in three
+// bytes, c0 | c1<<6 | c2<<12 | c3<<18 little-endian) or 8 (e4m3, a byte each).
+// All zero when inv == 0.  The conversion leaves each 6-bit code in its own
+// byte with the top two bits clear, so a pair p = c0 | c1<<8 compacts to
+// c0 | c1<<6 as p - (p>>8)*192, and disjoint fields combine by multiply-add.
+template <int FMT>
+__device__ __forceinline__ void mx_encode_words(const uint4 (&v)[4], float inv, uint32_t (&w)[8]) {
+    if (inv == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0;
+        return;
+    }
+    uint32_t p[16];   // p[i]: codes 2i (low byte) and 2i+1
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t x2 = (&v[i >> 2].x)[i & 3];
+        p[i] = cvt_x2<FMT>(__fmul_rn(bf16_lo(x2), inv), __fmul_rn(bf16_hi(x2), inv));
+    }
+    if constexpr (FMT == kE4M3) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = p[2 * k] + (p[2 * k + 1] << 16);
+    } else {
+        uint32_t g[8];    // g[j]: codes 4j..4j+3 -> 24 bits
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t a = p[2 * j] - (p[2 * j] >> 8) * 192u;
+            const uint32_t b = p[2 * j + 1] - (p[2 * j + 1] >> 8) * 192u;
+            g[j] = a + b * 4096u;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            w[3 * h + 0] = g[4 * h + 0] + (g[4 * h + 1] << 24);
+            w[3 * h + 1] = (g[4 * h + 1] >> 8) + (g[4 * h + 2] << 16);
+            w[3 * h + 2] = (g[4 * h + 2] >> 16) + (g[4 * h + 3] << 8);
+        }
+    }
+}
+
+// Store one MX block's words at codes + row offset + block offset (24 or 32 bytes).
+template <int FMT>
+__device__ __forceinline__ void mx_store_words(uint8_t* __restrict__ dst, const uint32_t (&w)[8]) {
+    if constexpr (FMT == kE4M3) {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+        reinterpret_cast<uint2*>(dst)[0] = make_uint2(w[0], w[1]);
+        reinterpret_cast<uint2*>(dst)[1] = make_uint2(w[2], w[3]);
+        reinterpret_cast<uint2*>(dst)[2] = make_uint2(w[4], w[5]);
+    }
+}
+
+// One nvfp4 block (16 values: two uint4) from its amax bits: the ue4m3 scale
+// (round to nearest of fl(fl(amax*gs)/6)) and two words of eight e2m1 codes.
+__device__ __forceinline__ void nvfp4_encode_block(uint4 v0, uint4 v1, uint32_t amax_bits, float gs, uint32_t& sc,
+                                                   uint32_t& w0, uint32_t& w1) {
+    sc = 0;
+    w0 = w1 = 0;
+    if (gs == 0.0f) return;
+    const float t = __fmul_rn(bf16_bits_to_f32(amax_bits), gs);
+    sc = cvt_x2<kE4M3>(__fdiv_rn(t, kMaxE2M1), 0.0f) & 0xFFu;
+    if (sc == 0) return;
+    const float inv = __fdiv_rn(gs, e4m3_to_f32(sc));
+    w0 = cvt_e2m1x2(__fmul_rn(bf16_lo(v0.x), inv), __fmul_rn(bf16_hi(v0.x), inv)) |
+         (cvt_e2m1x2(__fmul_rn(bf16_lo(v0.y), inv), __fmul_rn(bf16_hi(v0.y), inv)) << 8) |
+         (cvt_e2m1x2(__fmul_rn(bf16_lo(v0.z), inv), __fmul_rn(bf16_hi(v0.z), inv)) << 16) |
+         (cvt_e2m1x2(__fmul_rn(bf16_lo(v0.w), inv), __fmul_rn(bf16_hi(v0.w), inv)) << 24);
+    w1 = cvt_e2m1x2(__fmul_rn(bf16_lo(v1.x), inv), __fmul_rn(bf16_hi(v1.x), inv)) |
+         (cvt_e2m1x2(__fmul_rn(bf16_lo(v1.y), inv), __fmul_rn(bf16_hi(v1.y), inv)) << 8) |
+         (cvt_e2m1x2(__fmul_rn(bf16_lo(v1.z), inv), __fmul_rn(bf16_hi(v1.z), inv)) << 16) |
+         (cvt_e2m1x2(__fmul_rn(bf16_lo(v1.w), inv), __fmul_rn(bf16_hi(v1.w), inv)) << 24);
+}
+
 // ------------------------------------------------------------------ MX ----
+// Each lane owns whole blocks: block slot gb = (row, b) of a row-major grid of
+// pad128(M) x pad4(K/32) slots, walked with a grid-wide stride so every lane
+// gets the same work (+-1 block).  A block is 32 values = 64 contiguous bytes
+// (four 16-byte loads whose sectors the neighbouring lanes' loads share); the
+// block amax needs no shuffle and the scale math is done once per 32 values.
 template <int FMT, bool FUSED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kEncThreads)
 quant_mx_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint32_t* __restrict__ partial,
                 int n_partial, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                 float* __restrict__ s_global) {
@@ -135,76 +257,46 @@ quant_mx_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint
     const float gs = amax > 0.0f ? __fdiv_rn(gs_numerator(FMT), amax) : 0.0f;
     if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = gs != 0.0f ? __fdiv_rn(1.0f, gs) : 0.0f;
 
-    constexpr float fmax = fmt_max(FMT);
-    const int lane = threadIdx.x & 31, q = lane & 3;
-    const int64_t nb = K / 32, cpd4 = pad_to(nb, 4) / 4;
-    const int64_t chunks = (K + 1023) / 1024, rows_pad = pad_to(M, 128);
-    const int64_t n_tasks = rows_pad * chunks;
+    const int lane = threadIdx.x & 31;
+    const uint32_t nb = (uint32_t)(K / 32);
+    const int64_t cpd4 = pad_to(nb, 4) / 4;
+    const uint32_t nbp = (uint32_t)pad_to(nb, 4);                 // block slots per row
+    const uint32_t total = (uint32_t)pad_to(M, 128) * nbp;        // a multiple of 128
     const int64_t row_bytes = FMT == kE4M3 ? K : 3 * K / 4;
-    const int64_t warp0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+    const uint32_t stride = gridDim.x * blockDim.x;
 
-    for (int64_t task = warp0; task < n_tasks; task += nwarps) {
-        const int64_t r = task / chunks, c = task % chunks;
+    for (uint32_t gb = blockIdx.x * blockDim.x + threadIdx.x; gb < total; gb += stride) {
+        const uint32_t r = gb / nbp, b = gb - r * nbp;
+        const bool valid = r < M && b < nb;
+        uint4 v[4];
+        if (valid) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * K + 32 * (int64_t)b);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t e = c * 1024 + j * 256 + lane * 8;
-            const bool valid = r < M && e < K;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) v = __ldg(reinterpret_cast<const uint4*>(x + r * K + e));
-            uint32_t mb = absmax8_bits(v);
-            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
-            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
-            const float amax_b = bf16_bits_to_f32(mb);
-            uint32_t ue = 0;
-            float inv = 0.0f;
-            if (gs != 0.0f) {
-                ue = ue8m0_from_block_max(amax_b, gs, fmax);
-                inv = ue8m0_output_scale(ue, gs);
-            }
-            // eight codes, one byte each (zero when inv == 0)
-            uint32_t p0 = 0, p1 = 0, p2 = 0, p3 = 0;
-            if (inv != 0.0f) {
-                p0 = cvt_x2<FMT>(__fmul_rn(bf16_lo(v.x), inv), __fmul_rn(bf16_hi(v.x), inv));
-                p1 = cvt_x2<FMT>(__fmul_rn(bf16_lo(v.y), inv), __fmul_rn(bf16_hi(v.y), inv));
-                p2 = cvt_x2<FMT>(__fmul_rn(bf16_lo(v.z), inv), __fmul_rn(bf16_hi(v.z), inv));
-                p3 = cvt_x2<FMT>(__fmul_rn(bf16_lo(v.w), inv), __fmul_rn(bf16_hi(v.w), inv));
-            }
-            if constexpr (FMT == kE4M3) {
-                if (valid) {
-                    const uint64_t w = (uint64_t)(p0 | (p1 << 16)) | ((uint64_t)(p2 | (p3 << 16)) << 32);
-                    *reinterpret_cast<uint64_t*>(codes + r * row_bytes + e) = w;
-                }
-            } else {
-                // 8 codes -> 48 bits, c_i at bit 6i (four-in-three rule, twice)
-                const uint64_t v48 = (uint64_t)(p0 & 0x3F) | ((uint64_t)((p0 >> 8) & 0x3F) << 6) |
-                                     ((uint64_t)(p1 & 0x3F) << 12) | ((uint64_t)((p1 >> 8) & 0x3F) << 18) |
-                                     ((uint64_t)(p2 & 0x3F) << 24) | ((uint64_t)((p2 >> 8) & 0x3F) << 30) |
-                                     ((uint64_t)(p3 & 0x3F) << 36) | ((uint64_t)((p3 >> 8) & 0x3F) << 42);
-                const uint64_t nxt = __shfl_down_sync(0xFFFFFFFFu, v48, 1);
-                // the quad's 24 bytes as three 8-byte words
-                const uint64_t out = q == 0 ? (v48 | (nxt << 48))
-                                   : q == 1 ? ((v48 >> 16) | (nxt << 32))
-                                            : ((v48 >> 32) | (nxt << 16));
-                if (valid && q < 3) {
-                    const int64_t b = e / 32;
-                    *reinterpret_cast<uint64_t*>(codes + r * row_bytes + b * 24 + q * 8) = out;
-                }
-            }
-            // four consecutive blocks' scale bytes -> one 32-bit store
-            const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 4) << 8) |
-                                (__shfl_down_sync(0xFFFFFFFFu, ue, 8) << 16) |
-                                (__shfl_down_sync(0xFFFFFFFFu, ue, 12) << 24);
-            const int64_t b0 = c * 32 + j * 8 + (lane >> 2);
-            if ((lane & 15) == 0 && b0 < nb)
-                *reinterpret_cast<uint32_t*>(scales + swz_offset(r, b0, cpd4)) = s4;
+            for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
         }
+        uint32_t ue;
+        float inv;
+        mx_block_scale<FMT>(absmax32_bits(v), gs, ue, inv);
+        uint32_t w[8];
+        mx_encode_words<FMT>(v, inv, w);
+        if (valid) mx_store_words<FMT>(codes + (int64_t)r * row_bytes + (FMT == kE4M3 ? 32 : 24) * (int64_t)b, w);
+        // four consecutive blocks' scale bytes (four consecutive lanes, the same
+        // row: nbp % 4 == 0) -> one 32-bit store
+        const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
+                            (__shfl_down_sync(0xFFFFFFFFu, ue, 2) << 16) | (__shfl_down_sync(0xFFFFFFFFu, ue, 3) << 24);
+        if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(scales + swz_offset(r, b, cpd4)) = s4;
     }
 }
 
 // --------------------------------------------------------------- nvfp4 ----
+// Each lane owns two consecutive blocks of 16 (32 values, 64 contiguous bytes,
+// four output words), pair slots walked with a grid-wide stride as above.
 template <bool FUSED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kEncThreads)
 quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint32_t* __restrict__ partial,
                    int n_partial, uint32_t* __restrict__ codes, uint8_t* __restrict__ scales,
                    float* __restrict__ s_global) {
@@ -216,82 +308,393 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const u
     if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = gs != 0.0f ? __fdiv_rn(1.0f, gs) : 0.0f;
 
     const int lane = threadIdx.x & 31;
-    const int64_t nb = K / 16, cpd4 = pad_to(nb, 4) / 4;
-    const int64_t chunks = (K + 1023) / 1024, rows_pad = pad_to(M, 128);
-    const int64_t n_tasks = rows_pad * chunks;
-    const int64_t warp0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+    const uint32_t nb = (uint32_t)(K / 16);
+    const int64_t cpd4 = pad_to(nb, 4) / 4;
+    const uint32_t npp = (uint32_t)pad_to(nb, 4) / 2;             // block-pair slots per row
+    const uint32_t total = (uint32_t)pad_to(M, 128) * npp;        // a multiple of 256
+    const uint32_t stride = gridDim.x * blockDim.x;
 
-    for (int64_t task = warp0; task < n_tasks; task += nwarps) {
-        const int64_t r = task / chunks, c = task % chunks;
+    for (uint32_t gp = blockIdx.x * blockDim.x + threadIdx.x; gp < total; gp += stride) {
+        const uint32_t r = gp / npp;
+        const uint32_t b0 = 2 * (gp - r * npp);                    // this lane's first block
+        uint32_t sb[2];
+        uint32_t word[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t e = c * 1024 + j * 256 + lane * 8;
-            const bool valid = r < M && e < K;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) v = __ldg(reinterpret_cast<const uint4*>(x + r * K + e));
-            uint32_t mb = absmax8_bits(v);
-            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
-            const float amax_b = bf16_bits_to_f32(mb);
-            uint32_t sb = 0;
-            float inv = 0.0f;
-            if (gs != 0.0f) {
-                const float t = __fmul_rn(amax_b, gs);
-                const float ratio = __fdiv_rn(t, kMaxE2M1);
-                sb = cvt_x2<kE4M3>(ratio, 0.0f) & 0xFFu;
-                if (sb != 0) inv = __fdiv_rn(gs, e4m3_to_f32(sb));
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t b = b0 + h;
+            const bool valid = r < M && b < nb;
+            uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+            if (valid) {
+                const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * K + 16 * (int64_t)b);
+                v0 = __ldg(src);
+                v1 = __ldg(src + 1);
             }
-            uint32_t word = 0;
-            if (inv != 0.0f) {
-                word = cvt_e2m1x2(__fmul_rn(bf16_lo(v.x), inv), __fmul_rn(bf16_hi(v.x), inv)) |
-                       (cvt_e2m1x2(__fmul_rn(bf16_lo(v.y), inv), __fmul_rn(bf16_hi(v.y), inv)) << 8) |
-                       (cvt_e2m1x2(__fmul_rn(bf16_lo(v.z), inv), __fmul_rn(bf16_hi(v.z), inv)) << 16) |
-                       (cvt_e2m1x2(__fmul_rn(bf16_lo(v.w), inv), __fmul_rn(bf16_hi(v.w), inv)) << 24);
-            }
-            if (valid) codes[r * (K / 8) + e / 8] = word;
-            const uint32_t s4 = sb | (__shfl_down_sync(0xFFFFFFFFu, sb, 2) << 8) |
-                                (__shfl_down_sync(0xFFFFFFFFu, sb, 4) << 16) |
-                                (__shfl_down_sync(0xFFFFFFFFu, sb, 6) << 24);
-            const int64_t b0 = c * 64 + j * 16 + (lane >> 1);
-            if ((lane & 7) == 0 && b0 < nb)
-                *reinterpret_cast<uint32_t*>(scales + swz_offset(r, b0, cpd4)) = s4;
+            uint32_t w0, w1;
+            nvfp4_encode_block(v0, v1, max(absmax8_bits(v0), absmax8_bits(v1)), gs, sb[h], w0, w1);
+            word[2 * h] = w0;
+            word[2 * h + 1] = w1;
         }
+        if (r < M && b0 < nb) {
+            uint32_t* dst = codes + (int64_t)r * (K / 8) + 2 * (int64_t)b0;   // 8-byte aligned rows (K % 16 == 0)
+            *reinterpret_cast<uint2*>(dst) = make_uint2(word[0], word[1]);
+            if (b0 + 1 < nb) *reinterpret_cast<uint2*>(dst + 2) = make_uint2(word[2], word[3]);
+        }
+        // blocks b0, b0+1 from this lane and b0+2, b0+3 from the next -> one 32-bit store
+        const uint32_t s2 = sb[0] | (sb[1] << 8);
+        const uint32_t s4 = s2 | (__shfl_down_sync(0xFFFFFFFFu, s2, 1) << 16);
+        if ((lane & 1) == 0)
+            *reinterpret_cast<uint32_t*>(scales + swz_offset(r, b0, cpd4)) = s4;
+    }
+}
+
+// -------------------------------------------------------------- one pass ----
+// The whole quantizer in ONE cooperative launch, one CTA per SM: each CTA
+// bulk-copies its contiguous slice of x into shared memory in 32 KiB chunks
+// (one mbarrier each) and reduces the amax of every chunk as it lands,
+// publishes its partial maximum, waits at a bounded grid barrier for every
+// CTA's partial, then encodes its slice from shared memory.  x is read from
+// HBM once.  Used when every slice fits in one SM's shared memory; larger
+// tensors take the two-pass path above.
+//
+// Work unit ("slot") = 32 consecutive values of a row = 64 bytes of x: one MX
+// block, or two nvfp4 blocks.  Slots run over a padded grid of pad128(M) rows x
+// `slots_per_row` (pad4(K/32) for MX, pad4(K/16)/2 for nvfp4), so the padding of
+// the scale buffer is written too; CTA ranges are multiples of four slots, so
+// a group of four scale bytes never straddles two CTAs.
+//
+// Grid barrier: workspace word 0 counts arrivals (zeroed before the launch);
+// CTA c stores its partial in word 1 + c, then adds to the counter with
+// release semantics; after the counter reads G (acquire) every partial is
+// visible.  One polling thread per CTA keeps the counter's line uncontended.
+constexpr int kOneThreads = 1024;
+constexpr int kOneIters = 4;           // slots per thread: a slice holds <= 4 * kOneThreads slots
+constexpr uint32_t kChunkBytes = 32768;
+constexpr int kMaxChunks = 8;
+
+struct OnePassArgs {
+    const uint16_t* x;
+    int64_t M, K;
+    uint32_t* ws;           // [0] arrival counter (zeroed before the launch), [1..G] partial maxima
+    void* codes;
+    uint8_t* scales;
+    float* s_global;
+    uint32_t* err;
+    uint32_t slots_per_row; // padded
+    uint32_t slots_per_cta; // a multiple of 4
+};
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// swz_offset in 32-bit arithmetic (scale buffers of the one-pass path are < 4 GiB).
+__device__ __forceinline__ uint32_t swz_offset32(uint32_t row, uint32_t block, uint32_t cpd4) {
+    return ((((row >> 7) * cpd4 + (block >> 2)) * 32 + (row & 31)) * 4 + ((row >> 5) & 3)) * 4 + (block & 3);
+}
+
+// Flat index (in 64-byte units of x) of slot s: rows have K/32 units of data.
+__device__ __forceinline__ int64_t slot_data_index(uint32_t s, uint32_t spr, int64_t units_row, int64_t M) {
+    const int64_t r = s / spr, b = s - r * spr;
+    if (r >= M) return M * units_row;
+    return r * units_row + (b < units_row ? b : units_row);
+}
+
+// The 64-byte unit at shared address `addr` (unit index u within the slice).
+// The four 16-byte pieces are read starting at piece (u >> 1) & 3, so the eight
+// lanes of a quarter-warp reading consecutive units hit eight different bank
+// groups, then put back in order with two select stages.
+__device__ __forceinline__ void load_unit(uint32_t addr, uint32_t u, uint4 (&v)[4]) {
+    const uint32_t rot = (u >> 1) & 3;
+    uint4 w[4], t[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = lds128(addr + 16 * ((j + rot) & 3));   // w[j] = piece (j + rot) & 3
+    const bool r1 = rot & 1, r2 = rot & 2;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) t[k] = r1 ? w[(k + 3) & 3] : w[k];              // t[k] = piece (k + (rot & 2)) & 3
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = r2 ? t[(k + 2) & 3] : t[k];              // v[k] = piece k
+}
+
+template <int FMT>   // kE3M2 / kE2M3 / kE4M3, or kNvfp4
+__global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const OnePassArgs a) {
+    extern __shared__ __align__(128) uint8_t slice[];
+    __shared__ uint64_t bar[kMaxChunks];
+    __shared__ uint32_t red[32];
+    __shared__ int abort_flag;
+    const uint32_t G = gridDim.x, c = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t units_row = a.K / 32;
+    const uint32_t spr = a.slots_per_row;
+    const uint32_t total = (uint32_t)pad_to(a.M, 128) * spr;
+    const uint32_t s0 = min(total, c * a.slots_per_cta), s1 = min(total, s0 + a.slots_per_cta);
+    const int64_t f0 = slot_data_index(s0, spr, units_row, a.M), f1 = slot_data_index(s1, spr, units_row, a.M);
+    const uint32_t bytes = (uint32_t)((f1 - f0) * 64);
+    const uint32_t n_chunks = (bytes + kChunkBytes - 1) / kChunkBytes;
+    const uint32_t slice_addr = smem_u32(slice);
+
+    // 1. the slice -> shared memory, one bulk copy and one barrier per chunk
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (uint32_t k = 0; k < n_chunks; ++k) mbar_init(smem_u32(bar + k), 1);
+        fence_mbar_init();
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x) + f0 * 64;
+        for (uint32_t k = 0; k < n_chunks; ++k) {
+            const uint32_t off = k * kChunkBytes, n = min(kChunkBytes, bytes - off);
+            mbar_arrive_expect_tx(smem_u32(bar + k), n);
+            bulk_load(slice_addr + off, src + off, n, smem_u32(bar + k));
+        }
+    }
+    __syncthreads();
+
+    // 2. block maxima of this thread's slots as their chunks land, kept in
+    //    registers for step 3 (the slot -> thread map is the same there), and the
+    //    slice amax.  Iteration it covers units < (it + 1) * kOneThreads.
+    //    Thread t's slot in iteration it: s = s0 + it * kOneThreads + t, at
+    //    (row, slot-in-row) stepped without a division per iteration.
+    const uint32_t s_t = s0 + threadIdx.x;
+    const uint32_t r_t = s_t / spr, b_t = s_t - r_t * spr;
+    const uint32_t dr = kOneThreads / spr, db = kOneThreads - dr * spr;
+    uint32_t bm[kOneIters];   // MX: the block's amax bits; nvfp4: block 2b | block 2b+1 << 16
+    uint32_t m = 0;
+    {
+        uint32_t r = r_t, b = b_t, waited = 0;
+#pragma unroll
+        for (int it = 0; it < kOneIters; ++it) {
+            const uint32_t need = min(n_chunks, ((uint32_t)(it + 1) * kOneThreads * 64 + kChunkBytes - 1) / kChunkBytes);
+            while (waited < need) {
+                if (!mbar_wait(smem_u32(bar + waited), 0, a.err, &abort_flag, kErrQuantLoad)) {
+                    waited = n_chunks;                           // aborted: results are void
+                    break;
+                }
+                ++waited;
+            }
+            bm[it] = 0;
+            const uint32_t s = s_t + it * kOneThreads;
+            if (s < s1 && r < a.M && b < units_row) {
+                const uint32_t u = (uint32_t)(r * units_row + b - f0);
+                const uint32_t addr = slice_addr + 64 * u, rot = (u >> 1) & 3;
+                uint32_t mb[2] = {0, 0};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {          // rotated piece order: conflict-free
+                    const uint32_t pc = (j + rot) & 3;
+                    const uint32_t x8 = absmax8_bits(lds128(addr + 16 * pc));
+                    if (pc < 2) mb[0] = max(mb[0], x8); else mb[1] = max(mb[1], x8);
+                }
+                bm[it] = FMT == kNvfp4 ? (mb[0] | (mb[1] << 16)) : max(mb[0], mb[1]);
+                m = max(m, max(mb[0], mb[1]));
+            }
+            b += db;
+            r += dr;
+            if (b >= spr) { b -= spr; ++r; }
+        }
+    }
+    m = block_max(m, red);
+
+    // publish, then the bounded grid barrier: thread 0 stores the partial and
+    // counts itself in with a release add, then polls the counter
+    if (threadIdx.x == 0) {
+        a.ws[1 + c] = m;
+        red_release_add_u32(a.ws, 1u);
+        if (ld_acquire_u32(a.ws) < G) {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_u32(a.ws) < G) {
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    atomicCAS(a.err, 0u, (uint32_t)kErrQuantBarrier);
+                    abort_flag = 1;
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    uint32_t am = 0;
+    if (threadIdx.x < G) am = ld_relaxed_u32(a.ws + 1 + threadIdx.x);
+    am = block_max(am, red);   // (its barriers also publish abort_flag)
+    if (abort_flag) {
+        // leave no bulk copy in flight into this CTA's shared memory
+        if (threadIdx.x == 0)
+            for (uint32_t k = 0; k < n_chunks; ++k) {
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(smem_u32(bar + k), 0) && globaltimer() - t0 < kWaitLimitNs) {
+                }
+            }
+        return;
+    }
+    const float amax = bf16_bits_to_f32(am);
+    constexpr float kNum = FMT == kNvfp4 ? kMaxE4M3 * kMaxE2M1 : gs_numerator(FMT == kNvfp4 ? 0 : FMT);
+    const float gs = amax > 0.0f ? __fdiv_rn(kNum, amax) : 0.0f;
+    if (c == 0 && threadIdx.x == 0) *a.s_global = gs != 0.0f ? __fdiv_rn(1.0f, gs) : 0.0f;
+
+    // 3. encode from shared memory, one slot per lane
+    const int64_t row_bytes = FMT == kNvfp4 ? a.K / 2 : FMT == kE4M3 ? a.K : 3 * a.K / 4;
+    const uint32_t nb = FMT == kNvfp4 ? (uint32_t)(a.K / 16) : (uint32_t)units_row;
+    const uint32_t cpd4 = (nb + 3) / 4;
+    uint32_t r = r_t, b = b_t;
+#pragma unroll
+    for (int it = 0; it < kOneIters; ++it) {
+        const uint32_t s = s_t + it * kOneThreads;
+        if (s0 + it * kOneThreads >= s1) break;                     // uniform across the CTA
+        const bool in_range = s < s1;
+        const bool valid = in_range && r < a.M && b < units_row;
+        uint4 v[4];
+        if (valid) {
+            const uint32_t u = (uint32_t)(r * units_row + b - f0);
+            load_unit(slice_addr + 64 * u, u, v);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = make_uint4(0, 0, 0, 0);
+        }
+        uint8_t* const row_codes = static_cast<uint8_t*>(a.codes) + (int64_t)r * row_bytes;
+        if constexpr (FMT == kNvfp4) {
+            uint32_t sb0, sb1, w[4];
+            nvfp4_encode_block(v[0], v[1], bm[it] & 0xFFFFu, gs, sb0, w[0], w[1]);
+            nvfp4_encode_block(v[2], v[3], bm[it] >> 16, gs, sb1, w[2], w[3]);
+            if (valid) *reinterpret_cast<uint4*>(row_codes + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+            const uint32_t s2 = sb0 | (sb1 << 8);
+            const uint32_t s4 = s2 | (__shfl_down_sync(0xFFFFFFFFu, s2, 1) << 16);
+            if (in_range && (lane & 1) == 0) *reinterpret_cast<uint32_t*>(a.scales + swz_offset32(r, 2 * b, cpd4)) = s4;
+        } else {
+            uint32_t ue, w[8];
+            float inv;
+            mx_block_scale<FMT>(bm[it], gs, ue, inv);
+            mx_encode_words<FMT>(v, inv, w);
+            if (valid) mx_store_words<FMT>(row_codes + (FMT == kE4M3 ? 32 : 24) * b, w);
+            const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
+                                (__shfl_down_sync(0xFFFFFFFFu, ue, 2) << 16) | (__shfl_down_sync(0xFFFFFFFFu, ue, 3) << 24);
+            if (in_range && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.scales + swz_offset32(r, b, cpd4)) = s4;
+        }
+        b += db;
+        r += dr;
+        if (b >= spr) { b -= spr; ++r; }
     }
 }
 
 // ------------------------------------------------------------ launching ----
+// One cluster of kFusedCluster CTAs (16 needs the non-portable opt-in; a
+// device that refuses it gets 8).
 template <typename KernelT, typename... Args>
 cudaError_t launch_cluster(KernelT kernel, cudaStream_t s, Args... args) {
+    int csize = kFusedCluster;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        csize = 8;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kFusedCluster, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kFusedCluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    for (;; csize = 8) {
+        cfg.gridDim = dim3(csize, 1, 1);
+        attr[0].val.clusterDim.x = csize;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+        if (e == cudaSuccess || csize == 8) return e;
+        (void)cudaGetLastError();
+    }
+}
+
+// The encode pass, launched so that it may start while the amax pass runs; it
+// waits (griddepcontrol.wait) for the amax pass before reading the partials.
+template <typename KernelT, typename... Args>
+cudaError_t launch_dependent(KernelT kernel, int grid, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kEncThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The amax pass runs at full occupancy (8 x 256 threads per SM, <= 32
+// registers) with eight loads in flight per thread; the encode pass runs one
+// 1024-thread CTA per SM (a short launch ramp) walking whole blocks.
+constexpr int kAmaxPerSm = 8;
+
 int encode_grid(const DeviceInfo* info, int64_t M, int64_t K) {
-    const int64_t tasks = pad_to(M, 128) * ((K + 1023) / 1024);
-    int64_t g = (tasks + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)info->num_sms * 8;
+    const int64_t slots = pad_to(M, 128) * pad_to(K / 32, 4);      // lanes needed (MX; nvfp4 pairs: the same)
+    int64_t g = (slots + kEncThreads - 1) / kEncThreads;
+    const int64_t cap = (int64_t)info->num_sms;
     return (int)(g < cap ? g : cap);
 }
 
 int amax_grid(const DeviceInfo* info, int64_t n) {
-    int64_t g = (n / 8 + kThreads - 1) / kThreads;
-    int64_t cap = (int64_t)info->num_sms * 4;
+    int64_t g = (n / 8 + 8 * kThreads - 1) / (8 * kThreads);       // up to eight loads per thread
+    int64_t cap = (int64_t)info->num_sms * kAmaxPerSm;
     if (cap > kMaxPartials) cap = kMaxPartials;
     if (g > cap) g = cap;
     return (int)(g < 1 ? 1 : g);
 }
 
+
+// The one-pass launch, when every CTA's slice fits its SM's shared memory.
+template <int FMT>
+bool onepass_try(const DeviceInfo* info, const uint16_t* x, int64_t M, int64_t K, void* codes, uint8_t* scales,
+                 float* s_global, uint32_t* ws, size_t ws_bytes, cudaStream_t s, bsq_status* st) {
+    if (K % 32 != 0 || !ws) return false;
+    const int G = info->num_sms;
+    if (G > kOneThreads || (size_t)(G + 1) * sizeof(uint32_t) > ws_bytes) return false;
+    const int64_t spr = FMT == kNvfp4 ? pad_to(K / 16, 4) / 2 : pad_to(K / 32, 4);
+    const int64_t total = pad_to(M, 128) * spr;
+    const int64_t per_cta = pad_to((total + G - 1) / G, 4);
+    int64_t slice_max = (int64_t)info->max_smem_optin - 1024;
+    if (slice_max > (int64_t)kMaxChunks * kChunkBytes) slice_max = (int64_t)kMaxChunks * kChunkBytes;
+    if (per_cta * 64 > slice_max || per_cta > (int64_t)kOneIters * kOneThreads || total >= (int64_t(1) << 31))
+        return false;
+    const size_t smem = (size_t)(per_cta * 64);
+    static std::once_flag once[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    bool ok = dev >= 0 && dev < 64;
+    if (ok) std::call_once(once[dev], [&] {
+        ok = cudaFuncSetAttribute(quant_onepass_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  info->max_smem_optin - 1024) == cudaSuccess;
+    });
+    if (!ok) { (void)cudaGetLastError(); return false; }
+    OnePassArgs a;
+    a.x = x; a.M = M; a.K = K; a.ws = ws; a.codes = codes; a.scales = scales; a.s_global = s_global;
+    a.err = info->err; a.slots_per_row = (uint32_t)spr; a.slots_per_cta = (uint32_t)per_cta;
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) { *st = BSQ_ERR_CUDA; return true; }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G, 1, 1);
+    cfg.blockDim = dim3(kOneThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident at once: the grid barrier can complete
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, quant_onepass_kernel<FMT>, a);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); *st = BSQ_ERR_CUDA; return true; }
+    count_launch(FMT == kNvfp4 ? BSQ_KERNEL_QUANT_NVFP4 : BSQ_KERNEL_QUANT_MX);
+    *st = BSQ_OK;
+    return true;
+}
 }  // namespace
 
 size_t quantize_workspace_bytes(int64_t M, int64_t K) {
@@ -310,6 +713,13 @@ bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, 
     if (!fused) {
         if (!ws || ws_bytes < quantize_workspace_bytes(M, K)) return BSQ_ERR_WORKSPACE;
         if (!aligned16(ws)) return BSQ_ERR_MISALIGNED;
+        bool done = false;
+        switch (fmt) {
+        case kE3M2: done = onepass_try<kE3M2>(info, x, M, K, codes, scales, s_global, partial, ws_bytes, s, &st); break;
+        case kE2M3: done = onepass_try<kE2M3>(info, x, M, K, codes, scales, s_global, partial, ws_bytes, s, &st); break;
+        default: done = onepass_try<kE4M3>(info, x, M, K, codes, scales, s_global, partial, ws_bytes, s, &st); break;
+        }
+        if (done) return st;
         n_partial = amax_grid(info, M * K);
         amax_partial_kernel<<<n_partial, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), M * K / 8, partial);
         count_launch(BSQ_KERNEL_AMAX);
@@ -322,7 +732,8 @@ bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, 
         e = launch_cluster(quant_mx_kernel<F, true>, s, x, M, K, (const uint32_t*)nullptr, 0, codes, scales, \
                            s_global);                                                                       \
     else                                                                                                    \
-        quant_mx_kernel<F, false><<<grid, kThreads, 0, s>>>(x, M, K, partial, n_partial, codes, scales, s_global);
+        e = launch_dependent(quant_mx_kernel<F, false>, grid, s, x, M, K, (const uint32_t*)partial, n_partial,   \
+                             codes, scales, s_global);
     switch (fmt) {
     case kE3M2: BSQ_QMX(kE3M2); break;
     case kE2M3: BSQ_QMX(kE2M3); break;
@@ -345,6 +756,7 @@ bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32
     if (!fused) {
         if (!ws || ws_bytes < quantize_workspace_bytes(M, K)) return BSQ_ERR_WORKSPACE;
         if (!aligned16(ws)) return BSQ_ERR_MISALIGNED;
+        if (onepass_try<kNvfp4>(info, x, M, K, codes, scales, s_global, partial, ws_bytes, s, &st)) return st;
         n_partial = amax_grid(info, M * K);
         amax_partial_kernel<<<n_partial, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), M * K / 8, partial);
         count_launch(BSQ_KERNEL_AMAX);
@@ -355,8 +767,8 @@ bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32
         e = launch_cluster(quant_nvfp4_kernel<true>, s, x, M, K, (const uint32_t*)nullptr, 0, codes, scales,
                            s_global);
     else
-        quant_nvfp4_kernel<false><<<encode_grid(info, M, K), kThreads, 0, s>>>(x, M, K, partial, n_partial, codes,
-                                                                              scales, s_global);
+        e = launch_dependent(quant_nvfp4_kernel<false>, encode_grid(info, M, K), s, x, M, K,
+                             (const uint32_t*)partial, n_partial, codes, scales, s_global);
     count_launch(fused ? BSQ_KERNEL_QUANT_SMALL : BSQ_KERNEL_QUANT_NVFP4);
     if (e != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
     return launch_status();
@@ -374,7 +786,7 @@ bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32
 // scratch -- the per-CTA partial maxima of the amax pass -- in a file-scope
 // device array instead of a caller-provided workspace.
 //
-// The array (kMaxPartials words, 4 KiB) lives on every GPU that loads the
+// The array (kMaxPartials words, 8 KiB) lives on every GPU that loads the
 // library until the process exits.  Its device address is looked up once per
 // device, with that device current, by the first call on that device (host
 // code cannot use the array's name as a device address).  Every call shares
@@ -429,13 +841,13 @@ extern "C" BSQ_API bsq_status bsq_quantize_mxfp6_noalloc(const uint16_t* x, int6
     const int grid = encode_grid(info, M, K);
     switch (fmt) {
     case BSQ_E3M2:
-        quant_mx_kernel<kE3M2, false><<<grid, kThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        quant_mx_kernel<kE3M2, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
         break;
     case BSQ_E2M3:
-        quant_mx_kernel<kE2M3, false><<<grid, kThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        quant_mx_kernel<kE2M3, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
         break;
     default:
-        quant_mx_kernel<kE4M3, false><<<grid, kThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        quant_mx_kernel<kE4M3, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
         break;
     }
     count_launch(BSQ_KERNEL_QUANT_MX);

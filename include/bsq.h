@@ -79,9 +79,12 @@ BSQ_API int bsq_abi_version(void);
 /* Bytes of a block-scale buffer: pad128(rows) * pad4(n_blocks). */
 BSQ_API size_t bsq_scale_bytes(int64_t rows, int64_t n_blocks);
 
-/* Workspace the quantizers need for an [M, K] input (the per-CTA partial
- * maxima of the tensor amax pass); 0 when M*K is small enough for the
- * single-launch path.  Always 256-byte aligned sizes. */
+/* Workspace the quantizers need for an [M, K] input; 0 when M*K is small
+ * enough for the single-cluster path.  It holds the per-CTA partial maxima of
+ * the tensor amax (and, on the one-pass cooperative path, an arrival counter
+ * that the call zeroes on its stream before the kernel).  A call owns its
+ * workspace until its kernels finish: two calls whose kernels may overlap on
+ * the GPU need two workspaces.  Always 256-byte aligned sizes. */
 BSQ_API size_t bsq_quantize_workspace_bytes(int64_t M, int64_t K);
 
 /*
@@ -112,8 +115,8 @@ BSQ_API bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, b
  * allocate device memory on this path (no counterpart on the pages; this is a
  * library convenience).  Same arguments, results and validation minus the
  * workspace: the large-tensor path keeps its scratch (the amax pass's partial
- * maxima) in a 4 KiB device array owned by the library, present on every GPU
- * that loads it until the process exits.  The array holds 1024 partial maxima;
+ * maxima) in an 8 KiB device array owned by the library, present on every GPU
+ * that loads it until the process exits.  The array holds 2048 partial maxima;
  * the amax pass never launches more CTAs than that, so every size the checks
  * above accept fits, and a call that would need more returns
  * BSQ_ERR_UNSUPPORTED.  The first call on a device looks up the array's device

@@ -1,7 +1,10 @@
 """GPU quantizers against the oracle: codes, block scales (whole swizzled
-buffer, padding included) and s_global bit for bit, on both launch shapes
-(the single cluster launch for small tensors, amax pass + encode pass for
-large ones), ragged shapes and the degenerate inputs."""
+buffer, padding included) and s_global bit for bit, on all three launch
+shapes -- the single cluster launch for small tensors, the one-pass
+cooperative launch for tensors that fit the GPU's shared memory (including a
+grid with idle CTAs, (600, 128)), and amax pass + encode pass beyond that
+((4480, 4096), and nvfp4 rows that are not a whole number of 32-value slots)
+-- on ragged shapes and on the degenerate inputs."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +16,8 @@ from tests.parity import dev_tensor, host_bytes
 pytestmark = pytest.mark.gpu
 
 MX = [("e3m2", O.E3M2), ("e2m3", O.E2M3), ("e4m3", O.E4M3)]
-SHAPES = [(1, 32), (3, 96), (16, 4096), (130, 1056), (200, 2048), (257, 4128)]
+SHAPES = [(1, 32), (3, 96), (16, 4096), (130, 1056), (200, 2048), (257, 4128), (1100, 1024), (600, 128),
+          (4480, 4096)]
 
 
 def fixture(M, K, seed, std=0.02):
@@ -39,7 +43,7 @@ def test_quantize_mx_bit_exact(bsq, name, fmt, M, K):
     assert np.float32(g.item()) == np.float32(og)
 
 
-@pytest.mark.parametrize("M,K", SHAPES + [(5, 16), (7, 48)])
+@pytest.mark.parametrize("M,K", SHAPES + [(5, 16), (7, 48), (5000, 48)])
 def test_quantize_nvfp4_bit_exact(bsq, M, K):
     x = fixture(M, K, 300 + M + K, std=1.0)
     codes, scales, g = bsq.quantize_nvfp4(dev_tensor(x))

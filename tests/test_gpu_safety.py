@@ -43,7 +43,9 @@ def test_quantize_writes_only_its_outputs_and_keeps_inputs(bsq):
         cw, c = guarded(cb)
         sw, s = guarded(sb)
         gw, g = guarded(4)
-        bsq.quantize_mxfp6_(xd, f, c, s, g.view(torch.float32))
+        wsb = bsq.quantize_workspace_bytes(M, K)
+        ww, ws = guarded(wsb)
+        bsq.quantize_mxfp6_(xd, f, c, s, g.view(torch.float32), ws if wsb else None)
         torch.cuda.synchronize()
         assert guards_intact(cw, cb) and guards_intact(sw, sb) and guards_intact(gw, 4), name
         oc, os_, _ = O.quantize_mx(x, O.MX_FMTS[name])
@@ -75,8 +77,10 @@ def test_products_write_only_their_outputs(bsq):
 
 def test_graph_capture_replays_on_the_callers_stream(bsq):
     """Capture quantize + GEMM + a following scale in a graph on a side stream and
-    replay twice: identical bits both times, equal to the eager result doubled."""
-    M, N, K = 128, 256, 256
+    replay twice: identical bits both times, equal to the eager result doubled.
+    The activation quantizer is the single cluster launch, the weight quantizer
+    the cooperative one-pass launch (memset of its counter + the kernel)."""
+    M, N, K = 128, 1024, 256
     a = dev_tensor(S.normal_bf16((M, K), 0.02, 1))
     w = dev_tensor(S.normal_bf16((N, K), 0.02, 2))
     # eager (also loads the kernels before capture)
@@ -85,12 +89,14 @@ def test_graph_capture_replays_on_the_callers_stream(bsq):
     y_eager = bsq.gemm_mxfp6(ca, "e3m2", sa, ga, cw, "e3m2", sw, gw, K, out_dtype=torch.float32)
     torch.cuda.synchronize()
     y = torch.empty_like(y_eager)
+    ws = torch.empty(bsq.quantize_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
             bsq.quantize_mxfp6_(a, 0, ca, sa, ga, stream=s)
-            bsq.quantize_mxfp6_(w, 0, cw, sw, gw, stream=s)
+            bsq.quantize_mxfp6_(w, 0, cw, sw, gw, ws, stream=s)
             bsq.gemm_mxfp6_(ca, 0, sa, ga, cw, 0, sw, gw, y, M, N, K, stream=s)
             y.mul_(2.0)
     outs = []
@@ -132,7 +138,10 @@ def test_launch_counters_show_the_dispatch(bsq):
     x = dev_tensor(S.normal_bf16((16, 4096), 1.0, 4))
     bsq.quantize_mxfp6(x, "e2m3")                   # small: one cluster launch
     assert bsq.launch_count("quant_small") == 1 and bsq.launch_count("amax") == 0
-    xb = dev_tensor(S.normal_bf16((512, 1024), 1.0, 5))
-    bsq.quantize_nvfp4(xb)                          # large: amax pass + encode pass
-    assert bsq.launch_count("amax") == 1 and bsq.launch_count("quant_nvfp4") == 1
+    xb = dev_tensor(S.normal_bf16((1024, 2048), 1.0, 5))
+    bsq.quantize_nvfp4(xb)                          # fits shared memory: one cooperative launch
+    assert bsq.launch_count("amax") == 0 and bsq.launch_count("quant_nvfp4") == 1
+    xc = dev_tensor(S.normal_bf16((4480, 4096), 1.0, 6))
+    bsq.quantize_nvfp4(xc)                          # beyond it: amax pass + encode pass
+    assert bsq.launch_count("amax") == 1 and bsq.launch_count("quant_nvfp4") == 2
     torch.cuda.synchronize()

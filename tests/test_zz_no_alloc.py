@@ -33,7 +33,7 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(bsq):
     dev = torch.device("cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     p = lambda t: ctypes.c_void_p(t.data_ptr())
-    cases = [(512, 1024, "e3m2", 21), (300, 2048, "e2m3", 22)]     # both above the single-launch size
+    cases = [(1024, 1280, "e3m2", 21), (600, 2048, "e2m3", 22)]    # both above the single-launch size
     for M, K, name, seed in cases:
         fmt = bsq.FMT_IDS[name]
         x = dev_tensor(S.normal_bf16((M, K), 0.02, seed, outlier_frac=0.01))
