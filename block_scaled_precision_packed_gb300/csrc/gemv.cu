@@ -22,6 +22,10 @@
 //    operands (pairs (j, j+4) of each 8-code group share a bf16x2 register);
 //    the activation chunk is staged in shared memory in that order with a
 //    bank-conflict-free layout.
+#include <climits>
+#include <mutex>
+#include <type_traits>
+
 #include "bsq_device.cuh"
 #include "bsq_internal.h"
 
@@ -268,6 +272,440 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
     }
 }
 
+// ------------------------------------------------------------- nvfp4 ----
+// The nvfp4 decode GEMV.  Weight bytes stream HBM -> shared memory through a
+// TMA ring (the bytes in flight per SM, not the instruction count, bound a
+// decode GEMV), so the SM's load window is the ring, not registers.
+//
+//  * CTA = CW consumer warps x 16 weight rows + one producer warp.  R = 16 CW
+//    rows per CTA, chosen on the host so the CTAs fill the SMs in whole waves.
+//  * Stage = 256 codes of every row: a 2-D TMA box {128 B, R rows} with the
+//    128-byte swizzle, plus the block-scale atoms of those 16 blocks (one bulk
+//    copy of up to 4 atoms per 128-row block the tile touches).
+//  * Consumers read their 16 rows with ldmatrix (eight rows x 16 B per matrix;
+//    the swizzle puts the eight rows' chunks in eight bank groups), so thread
+//    (g, t) holds codes 8t..8t+7 of a 32-code chunk for rows g and g+8.
+//  * x is staged per stage by the consumer threads (loaded two stages ahead
+//    into registers), natural K order, row pitch 36 x 16 B.
+//
+// Exact decode, two ways, chosen per stage (uniform in the CTA):
+//  * f16: when every activation of the stage is zero or an f16 normal, x is
+//    staged as f16 and each code pair (one byte, two e2m1 codes) goes through
+//    the hardware e2m1x2 -> f16x2 conversion and one f16x2 multiply by the
+//    block scale (ue4m3 -> f16, exact).  value * scale lies in [2^-10, 2688]
+//    with at most 5 significant bits: exact, an f16 normal; x * w is then exact
+//    in the f32 MMA accumulate.
+//  * bf16 (any other stage): x is staged as raw bf16 and the codes are
+//    "placed" into bf16 (value * 2^-126) and multiplied by scale * 2^119 in
+//    bf16x2, exact; those products carry 2^-7, so they accumulate separately
+//    and are lifted by 2^7 at the end.
+namespace nvf4 {
+
+constexpr int kPitch = 36;          // 16-byte units per staged x row (32 used; == 4 mod 8)
+constexpr int kMaxRowBlocks = 3;    // 128-row scale blocks one tile can touch (R <= 256)
+constexpr int kSmemLimit = 232448;  // opt-in shared memory per CTA
+
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t r;
+    asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
+    return r;
+}
+// the four code pairs (bytes) of a word -> four f16x2
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+    asm("{ .reg .b8 b0, b1, b2, b3;\n"
+        "  mov.b32 {b0, b1, b2, b3}, %4;\n"
+        "  cvt.rn.f16x2.e2m1x2 %0, b0;\n  cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        "  cvt.rn.f16x2.e2m1x2 %2, b2;\n  cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two));
+    return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// codes (2j, 2j+1) of one byte placed into a bf16x2: value * 2^-126 each
+__device__ __forceinline__ uint32_t place_byte_bf16x2(uint32_t b) {
+    return ((b & 7u) << 6) | ((b & 8u) << 12) | ((b & 0x70u) << 18) | ((b & 0x80u) << 24);
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+// AND of `ok` over the consumer threads (named barrier 1).
+__device__ __forceinline__ bool consumers_and(bool ok, int nthreads) {
+    uint32_t r;
+    asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; barrier.red.and.pred p, 1, %2, q; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(r) : "r"((uint32_t)ok), "r"(nthreads) : "memory");
+    return r != 0;
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (F16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// bf16x2 word of x -> f16x2, and whether both halves are zero or f16 normals
+// (bf16 exponent field 113..142; every such bf16 value is an f16 normal).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& ok) {
+    const uint32_t lo_e = (w >> 7) & 0xFFu, hi_e = (w >> 23) & 0xFFu;
+    const bool lo_ok = (w & 0x7FFFu) == 0 || (lo_e >= 113 && lo_e <= 142);
+    const bool hi_ok = (w & 0x7FFF0000u) == 0 || (hi_e >= 113 && hi_e <= 142);
+    ok = lo_ok && hi_ok;
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
+    return r;
+}
+
+struct Args {
+    const uint16_t* x;
+    const uint8_t* sW;
+    const float* gW;
+    void* y;
+    uint32_t* err;
+    int64_t M, N, K;
+    int64_t cpd4;        // scale atoms per 128-row block
+    int out_bf16;
+};
+
+// Shared memory plan: ring stages (codes + scale atoms), two x buffers in
+// two copies (f16, bf16), barriers; as many stages as fit, at most 8.
+template <int NT, int CW>
+struct Plan {
+    static constexpr int kXBuf = 8 * NT * kPitch * 16;             // bytes of one staged x copy
+    static constexpr int kStageBytes = 16 * CW * 128 + kMaxRowBlocks * 2048;
+    static constexpr int kFixed = 1024 + 4 * kXBuf + 256;
+    static constexpr int kFit = (kSmemLimit - kFixed) / kStageBytes;
+    static constexpr int kStages = kFit < 8 ? kFit : 8;
+    static constexpr int kBytes = kFixed + kStages * kStageBytes;
+    static_assert(kStages >= 3, "too little shared memory for the ring");
+};
+
+template <int NT, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, 1)
+gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
+    constexpr int R = 16 * CW;
+    constexpr int kCons = CW * 32;
+    constexpr int kWBytes = R * 128;                        // one stage of codes
+    constexpr int kSBytes = kMaxRowBlocks * 2048;           // one stage of scale atoms (room)
+    constexpr int kRowsX = 8 * NT;
+    constexpr int kUnits = kRowsX * 32;                     // 16-byte x units per stage
+    constexpr int kPer = (kUnits + kCons - 1) / kCons;
+    constexpr int kXBuf = Plan<NT, CW>::kXBuf;
+    constexpr int kStages = Plan<NT, CW>::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sWst = smem;                                   // kStages x kWBytes (1024-aligned stages)
+    uint8_t* sSst = sWst + kStages * kWBytes;               // kStages x kSBytes
+    uint8_t* sXh = sSst + kStages * kSBytes;                // 2 x kXBuf (f16)
+    uint8_t* sXb = sXh + 2 * kXBuf;                         // 2 x kXBuf (bf16)
+    uint64_t* full = reinterpret_cast<uint64_t*>(sXb + 2 * kXBuf);
+    uint64_t* empty = full + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t M = args.M, N = args.N, K = args.K;
+    const int64_t row_base = (int64_t)blockIdx.x * R;
+    const int nst = (int)((K + 255) / 256);
+    const int rb0 = (int)(row_base >> 7);
+    const int rb1 = (int)((row_base + R - 1) >> 7);
+    const int64_t n_rb_total = (N + 127) / 128;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(full + s), 1);
+            mbar_init(smem_u32(empty + s), CW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages &&
+                    !mbar_wait(smem_u32(empty + s), ((i / kStages) - 1) & 1, args.err, abort_flag, kErrGemvProducer))
+                    break;
+                const int64_t atoms_left = args.cpd4 - 4LL * i;
+                const uint32_t n_atoms = (uint32_t)(atoms_left < 4 ? atoms_left : 4);
+                uint32_t n_rb = 0;
+                for (int rb = rb0; rb <= rb1 && rb < n_rb_total; ++rb) ++n_rb;
+                mbar_arrive_expect_tx(smem_u32(full + s), kWBytes + n_rb * n_atoms * 512);
+                tma_load_2d(smem_u32(sWst + s * kWBytes), &tmW, smem_u32(full + s), i * 128, (int32_t)row_base);
+                for (uint32_t j = 0; j < n_rb; ++j) {
+                    const uint8_t* src = args.sW + ((int64_t)(rb0 + j) * args.cpd4 + 4LL * i) * 512;
+                    bulk_load(smem_u32(sSst + s * kSBytes + j * 2048), src, n_atoms * 512, smem_u32(full + s));
+                }
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                // leave no copy in flight into this CTA's shared memory
+                for (int i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i) {
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(full + i % kStages), (i / kStages) & 1) &&
+                           globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t row0 = row_base + warp * 16 + g, row1 = row0 + 8;
+    const int nblocks32 = (int)(K / 16);     // K < 2^31: the entry point bounds every dimension
+
+    auto x_load = [&](int64_t st, uint4 (&v)[kPer]) {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int idx = threadIdx.x + i * kCons;
+            const int r = idx >> 5, u = idx & 31;
+            const int64_t k = st * 256 + 8 * u;
+            v[i] = make_uint4(0, 0, 0, 0);
+            if (idx < kUnits && r < M && k < K) v[i] = __ldg(reinterpret_cast<const uint4*>(args.x + r * K + k));
+        }
+    };
+    auto x_store = [&](int buf, const uint4 (&v)[kPer]) -> bool {
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int idx = threadIdx.x + i * kCons;
+            if (idx < kUnits) {
+                const int r = idx >> 5, u = idx & 31;
+                const int off = (r * kPitch + u) * 16;
+                uint4 hv = make_uint4(0, 0, 0, 0);          // rows >= M are zero in both copies
+                if (r < M) {
+                    bool a, b, c, d;
+                    hv = make_uint4(bf16x2_to_f16x2(v[i].x, a), bf16x2_to_f16x2(v[i].y, b),
+                                    bf16x2_to_f16x2(v[i].z, c), bf16x2_to_f16x2(v[i].w, d));
+                    ok = ok && a && b && c && d;
+                }
+                *reinterpret_cast<uint4*>(sXh + buf * kXBuf + off) = hv;
+                *reinterpret_cast<uint4*>(sXb + buf * kXBuf + off) = v[i];
+            }
+        }
+        return ok;
+    };
+
+    float acc_h[NT][4], acc_b[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc_h[i][j] = acc_b[i][j] = 0.0f;
+
+    // ldmatrix addresses: lane L supplies row (L & 7) of matrix L >> 3:
+    // matrices {rows 0-7, chunk c}, {rows 8-15, c}, {rows 0-7, c+1}, {rows 8-15, c+1}
+    const int mrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);   // row within the tile
+    const int mcol = lane >> 4;                                        // 0: chunk c, 1: chunk c+1
+    // scale word of rows g, g+8 (chunk pair c, c+1 share one 4-byte group)
+    int srb[2], soff[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int64_t row = r ? row1 : row0;
+        srb[r] = (int)((row >> 7) - rb0);
+        soff[r] = srb[r] * 2048 + (int)(row & 31) * 16 + (int)((row >> 5) & 3) * 4;
+    }
+    const uint32_t ssel = (t >> 1) ? 0x31u : 0x20u;   // bytes (t>>1) and 2 + (t>>1) of the group
+
+    // one stage of MMAs: chunk pairs (c, c+1) = (2cp, 2cp+1), each one
+    // ldmatrix.x4 of codes (rows g, g+8 x chunks c, c+1) and one 4-byte scale
+    // group per row.  F16 selects the decode (and the accumulator set).
+    auto consume = [&](auto f16_tag, uint32_t wst, uint32_t sst, uint32_t xs, int i, float (&acc)[NT][4]) {
+        constexpr bool F16 = decltype(f16_tag)::value;
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp) {
+            uint32_t wr[4];
+            ldmatrix_x4(wst + mrow * 128 + (((2 * cp + mcol) ^ (mrow & 7)) << 4), wr);
+            const int blk0 = 16 * i + 4 * cp + (t >> 1);                // chunk 2cp; chunk 2cp+1 is blk0 + 2
+            const bool v0 = blk0 < nblocks32, v1 = blk0 + 2 < nblocks32;
+            uint32_t S[2][2];   // [row][chunk] pair multipliers; zero for blocks past K
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t two = __byte_perm(lds32(sst + soff[r] + cp * 512), 0, ssel);
+                if constexpr (F16) {
+                    const uint32_t sf = e4m3x2_to_f16x2(two);
+                    S[r][0] = v0 ? __byte_perm(sf, sf, 0x1010) : 0u;
+                    S[r][1] = v1 ? __byte_perm(sf, sf, 0x3232) : 0u;
+                } else {
+                    const uint32_t b0 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32(two & 0xFF), 0x1p119f));
+                    const uint32_t b1 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32((two >> 8) & 0xFF), 0x1p119f));
+                    S[r][0] = v0 ? (b0 | (b0 << 16)) : 0u;
+                    S[r][1] = v1 ? (b1 | (b1 << 16)) : 0u;
+                }
+            }
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {               // chunk 2cp + ch
+                uint32_t P[2][4];   // pairs j = 0..3 of rows g (wr[2ch]) and g+8 (wr[2ch+1])
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if constexpr (F16) {
+                        e2m1x8_to_f16x2(wr[2 * ch + r], P[r]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) P[r][j] = hmul2(P[r][j], S[r][ch]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            P[r][j] = bmul2(place_byte_bf16x2((wr[2 * ch + r] >> (8 * j)) & 0xFFu), S[r][ch]);
+                    }
+                }
+                uint4 xv[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) xv[nt] = lds128(xs + ((8 * nt + g) * kPitch + 4 * (2 * cp + ch) + t) * 16);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t a[4] = {P[0][2 * e], P[1][2 * e], P[0][2 * e + 1], P[1][2 * e + 1]};
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816<F16>(acc[nt], a, e ? xv[nt].z : xv[nt].x, e ? xv[nt].w : xv[nt].y);
+                }
+            }
+        }
+    };
+
+    uint4 xa[kPer], xn[kPer];
+    x_load(0, xa);
+    bool f16_cur;
+    {
+        const bool ok = x_store(0, xa);
+        if (1 < nst) x_load(1, xa);
+        f16_cur = consumers_and(ok, kCons);
+    }
+
+    for (int i = 0; i < nst; ++i) {
+        const int s = i % kStages, buf = i & 1;
+        if (i + 2 < nst) x_load(i + 2, xn);
+        // a failed wait (abort) skips the stage's math but keeps the named
+        // barriers below balanced across the consumer warps
+        const bool have = mbar_wait(smem_u32(full + s), (i / kStages) & 1, args.err, abort_flag, kErrGemvConsumer);
+        if (have) {
+            const uint32_t wst = smem_u32(sWst + s * kWBytes);
+            const uint32_t sst = smem_u32(sSst + s * kSBytes);
+            if (f16_cur) consume(std::true_type{}, wst, sst, smem_u32(sXh + buf * kXBuf), i, acc_h);
+            else consume(std::false_type{}, wst, sst, smem_u32(sXb + buf * kXBuf), i, acc_b);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        bool ok = true;
+        if (i + 1 < nst) ok = x_store(buf ^ 1, xa);
+        f16_cur = consumers_and(ok, kCons);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) xa[u] = xn[u];
+    }
+
+    // ---- epilogue: acc_h + 2^7 acc_b, times gW ----
+    if (*abort_flag) return;
+    const float gw = args.gW ? __ldg(args.gW) : 1.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t m = 8 * nt + 2 * t + (i & 1);
+            const int64_t n = (i < 2) ? row0 : row1;
+            if (m < M && n < N) {
+                const float v = __fmul_rn(__fmaf_rn(acc_b[nt][i], 0x1p7f, acc_h[nt][i]), gw);
+                if (args.out_bf16) reinterpret_cast<uint16_t*>(args.y)[m * N + n] = f32_to_bf16_bits(v);
+                else reinterpret_cast<float*>(args.y)[m * N + n] = v;
+            }
+        }
+    }
+}
+
+}  // namespace nvf4
+
+// Consumer warps per CTA (16 rows each) for the nvfp4 GEMV: the choice in
+// {4, 6, 8, 12} with the least rows per SM over whole waves (one CTA per SM).
+int nvf4_warps(int64_t N, int sms) {
+    const int cand[4] = {12, 8, 6, 4};
+    int best = 8;
+    int64_t best_cost = INT64_MAX;
+    for (int w : cand) {
+        const int64_t tiles = (N + 16 * w - 1) / (16 * w);
+        const int64_t cost = (tiles + sms - 1) / sms * w;
+        if (cost < best_cost) { best_cost = cost; best = w; }
+    }
+    return best;
+}
+
+template <int NT, int CW>
+bsq_status launch_nvf4_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+    constexpr int R = 16 * CW;
+    constexpr size_t smem = nvf4::Plan<NT, CW>::kBytes;
+    auto kern = nvf4::gemv_nvf4_kernel<NT, CW>;
+    static std::once_flag once[64];
+    static bool ok_dev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
+    std::call_once(once[dev], [&] {
+        ok_dev[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess;
+    });
+    if (!ok_dev[dev]) { (void)cudaGetLastError(); return BSQ_ERR_UNSUPPORTED; }
+    const dim3 grid((unsigned)((a.N + R - 1) / R));
+    kern<<<grid, (CW + 1) * 32, smem, s>>>(tm, a);
+    return launch_status();
+}
+
+template <int NT>
+bsq_status launch_nvf4_nt(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+    switch (cw) {
+    case 12: return launch_nvf4_cfg<NT, 12>(tm, a, s);
+    case 8: return launch_nvf4_cfg<NT, 8>(tm, a, s);
+    case 6: return launch_nvf4_cfg<NT, 6>(tm, a, s);
+    default: return launch_nvf4_cfg<NT, 4>(tm, a, s);
+    }
+}
+
+bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t* W, const uint8_t* sW,
+                       const float* gW, void* y, int out, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+    const int cw = nvf4_warps(N, info->num_sms);
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return BSQ_ERR_UNSUPPORTED;
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    const cuuint32_t box[2] = {128, (cuuint32_t)(16 * cw)};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return BSQ_ERR_UNSUPPORTED;
+    nvf4::Args a;
+    a.x = x; a.sW = sW; a.gW = gW; a.y = y; a.err = info->err; a.M = M; a.N = N; a.K = K;
+    a.cpd4 = pad_to(K / 16, 4) / 4;
+    a.out_bf16 = out;
+    if (M <= 8) return launch_nvf4_nt<1>(cw, tm, a, s);
+    if (M <= 16) return launch_nvf4_nt<2>(cw, tm, a, s);
+    return launch_nvf4_nt<4>(cw, tm, a, s);
+}
+
 template <int WFMT>
 bsq_status launch_fmt(const uint16_t* x, const uint8_t* W, const uint8_t* sW, const float* gW, void* y, int out,
                       int64_t M, int64_t N, int64_t K, cudaStream_t s) {
@@ -283,11 +721,12 @@ bsq_status launch_fmt(const uint16_t* x, const uint8_t* W, const uint8_t* sW, co
 bsq_status gemv_launch(const uint16_t* x, const void* W, int fw, const uint8_t* sW, const float* gW, void* y,
                        int out, int64_t M, int64_t N, int64_t K, bool nvfp4, cudaStream_t s) {
     bsq_status st;
-    if (!device_info(&st)) return st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
     const uint8_t* Wb = static_cast<const uint8_t*>(W);
     bsq_status r;
     if (nvfp4) {
-        r = launch_fmt<kNvfp4>(x, Wb, sW, gW, y, out, M, N, K, s);
+        r = launch_nvf4(info, x, Wb, sW, gW, y, out, M, N, K, s);
         count_launch(BSQ_KERNEL_GEMV_NVFP4);
     } else {
         if (fw == kE3M2) r = launch_fmt<kE3M2>(x, Wb, sW, gW, y, out, M, N, K, s);

@@ -55,6 +55,24 @@ def test_gemv_nvfp4_every_code_and_subnormal_scales(bsq):
     check_products(y, want, s, "gemv_nvfp4 all codes")
 
 
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_gemv_nvfp4_activations_outside_f16(bsq, M):
+    """Activations that f16 cannot hold exactly (huge, tiny, bf16 subnormal) in
+    some 256-wide K chunks and not in others: those chunks take the bf16 decode,
+    the rest the f16 one, in the same call and the same outputs."""
+    N, K = 300, 1536
+    x = S.normal_bf16((M, K), 1.0, 40 + M)
+    x[:, 300] = 0x4B80          # 1.68e7  (> f16 max)
+    x[:, 777] = 0x3380          # 5.96e-8 (below the f16 normal range)
+    x[0, 1300] = 0x0005         # bf16 subnormal
+    x[-1, 1301] = 0xC780        # -65536 (just beyond f16)
+    W, sc = nvfp4_operand(N, K, 44)
+    for out in (torch.float32, torch.bfloat16):
+        y = bsq.gemv_nvfp4(dev_tensor(x), dev_tensor(W), dev_tensor(sc), None, K, out_dtype=out)
+        want, s = O.gemv_nvfp4(x, W, sc, 1.0, M, N, K)
+        check_products(y, want, s, f"gemv_nvfp4 mixed chunks M{M}")
+
+
 @pytest.mark.parametrize("fmt", ["e3m2", "e2m3", "e4m3"])
 @pytest.mark.parametrize("M,N,K", [(1, 256, 256), (8, 300, 512), (32, 129, 384)])
 def test_gemv_mx(bsq, fmt, M, N, K):
