@@ -539,27 +539,32 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
     // one stage of MMAs: chunk pairs (c, c+1) = (2cp, 2cp+1), each one
     // ldmatrix.x4 of codes (rows g, g+8 x chunks c, c+1) and one 4-byte scale
     // group per row.  F16 selects the decode (and the accumulator set).
-    auto consume = [&](auto f16_tag, uint32_t wst, uint32_t sst, uint32_t xs, int i, float (&acc)[NT][4]) {
+    auto consume = [&](auto f16_tag, auto tail_tag, uint32_t wst, uint32_t sst, uint32_t xs, int i,
+                       float (&acc)[NT][4]) {
         constexpr bool F16 = decltype(f16_tag)::value;
+        constexpr bool TAIL = decltype(tail_tag)::value;   // zero the multipliers of blocks past K
 #pragma unroll
         for (int cp = 0; cp < 4; ++cp) {
             uint32_t wr[4];
             ldmatrix_x4(wst + mrow * 128 + (((2 * cp + mcol) ^ (mrow & 7)) << 4), wr);
-            const int blk0 = 16 * i + 4 * cp + (t >> 1);                // chunk 2cp; chunk 2cp+1 is blk0 + 2
-            const bool v0 = blk0 < nblocks32, v1 = blk0 + 2 < nblocks32;
-            uint32_t S[2][2];   // [row][chunk] pair multipliers; zero for blocks past K
+            uint32_t S[2][2];   // [row][chunk] pair multipliers
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const uint32_t two = __byte_perm(lds32(sst + soff[r] + cp * 512), 0, ssel);
                 if constexpr (F16) {
                     const uint32_t sf = e4m3x2_to_f16x2(two);
-                    S[r][0] = v0 ? __byte_perm(sf, sf, 0x1010) : 0u;
-                    S[r][1] = v1 ? __byte_perm(sf, sf, 0x3232) : 0u;
+                    S[r][0] = __byte_perm(sf, sf, 0x1010);
+                    S[r][1] = __byte_perm(sf, sf, 0x3232);
                 } else {
                     const uint32_t b0 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32(two & 0xFF), 0x1p119f));
                     const uint32_t b1 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32((two >> 8) & 0xFF), 0x1p119f));
-                    S[r][0] = v0 ? (b0 | (b0 << 16)) : 0u;
-                    S[r][1] = v1 ? (b1 | (b1 << 16)) : 0u;
+                    S[r][0] = b0 | (b0 << 16);
+                    S[r][1] = b1 | (b1 << 16);
+                }
+                if constexpr (TAIL) {
+                    const int blk0 = 16 * i + 4 * cp + (t >> 1);        // chunk 2cp; chunk 2cp+1 is blk0 + 2
+                    if (blk0 >= nblocks32) S[r][0] = 0;
+                    if (blk0 + 2 >= nblocks32) S[r][1] = 0;
                 }
             }
 #pragma unroll
@@ -609,8 +614,15 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
         if (have) {
             const uint32_t wst = smem_u32(sWst + s * kWBytes);
             const uint32_t sst = smem_u32(sSst + s * kSBytes);
-            if (f16_cur) consume(std::true_type{}, wst, sst, smem_u32(sXh + buf * kXBuf), i, acc_h);
-            else consume(std::false_type{}, wst, sst, smem_u32(sXb + buf * kXBuf), i, acc_b);
+            const bool tail = 16 * (i + 1) > nblocks32;
+            const uint32_t xh = smem_u32(sXh + buf * kXBuf), xb = smem_u32(sXb + buf * kXBuf);
+            if (f16_cur) {
+                if (tail) consume(std::true_type{}, std::true_type{}, wst, sst, xh, i, acc_h);
+                else consume(std::true_type{}, std::false_type{}, wst, sst, xh, i, acc_h);
+            } else {
+                if (tail) consume(std::false_type{}, std::true_type{}, wst, sst, xb, i, acc_b);
+                else consume(std::false_type{}, std::false_type{}, wst, sst, xb, i, acc_b);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(empty + s));
