@@ -23,8 +23,16 @@ FMT_IDS = {"e3m2": E3M2, "e2m3": E2M3, "e4m3": E4M3}
 KERNEL_IDS = {"amax": 0, "quant_mx": 1, "quant_nvfp4": 2, "quant_small": 3, "gemm_nvfp4": 4,
               "gemm_mx": 5, "gemv_nvfp4": 6, "gemv_mx": 7, "dequant": 8}
 
+MAX_BATCH = 8
+
 _lib = None
 _lock = threading.Lock()
+
+
+class QTensor(ctypes.Structure):
+    """bsq_qtensor: one tensor of a batched quantizer call."""
+    _fields_ = [("x", ctypes.c_void_p), ("M", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("s_global", ctypes.c_void_p)]
 
 
 class BsqError(RuntimeError):
@@ -52,6 +60,9 @@ def load(path: str | None = None):
             "bsq_quantize_mxfp6": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_nvfp4": (i32, [vp, i64, i64, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_mxfp6_noalloc": (i32, [vp, i64, i64, i32, vp, vp, vp, vp]),
+            "bsq_quantize_batch_workspace_bytes": (sz, []),
+            "bsq_quantize_mxfp6_batch": (i32, [vp, i32, i32, vp, sz, vp]),
+            "bsq_quantize_nvfp4_batch": (i32, [vp, i32, vp, sz, vp]),
             "bsq_gemm_nvfp4": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, vp]),
             "bsq_gemm_mxfp6": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, vp, i32, i64, i64, i64, vp]),
             "bsq_gemv_nvfp4": (i32, [vp, vp, vp, vp, vp, i32, i64, i64, i64, vp]),
@@ -116,6 +127,33 @@ def quantize_nvfp4_(x, codes, scales, s_global, workspace=None, stream=None):
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("bsq_quantize_nvfp4", load().bsq_quantize_nvfp4(
         _p(x), M, K, _p(codes), _p(scales), _p(s_global), _p(workspace), ws_bytes, _stream(stream)))
+
+
+def quantize_batch_workspace_bytes() -> int:
+    return load().bsq_quantize_batch_workspace_bytes()
+
+
+def _qtensors(items):
+    arr = (QTensor * len(items))()
+    for i, (x, codes, scales, g) in enumerate(items):
+        M, K = x.shape
+        arr[i] = QTensor(x.data_ptr(), M, K, codes.data_ptr(), scales.data_ptr(), g.data_ptr())
+    return arr
+
+
+def quantize_mxfp6_batch_(items, fmt, workspace, stream=None):
+    """items: [(x, codes, scales, s_global), ...] -- one launch for the batch."""
+    arr = _qtensors(items)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("bsq_quantize_mxfp6_batch", load().bsq_quantize_mxfp6_batch(
+        ctypes.cast(arr, ctypes.c_void_p), len(items), fmt, _p(workspace), ws_bytes, _stream(stream)))
+
+
+def quantize_nvfp4_batch_(items, workspace, stream=None):
+    arr = _qtensors(items)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("bsq_quantize_nvfp4_batch", load().bsq_quantize_nvfp4_batch(
+        ctypes.cast(arr, ctypes.c_void_p), len(items), _p(workspace), ws_bytes, _stream(stream)))
 
 
 def gemm_nvfp4_(A, sA, gA, W, sW, gW, Y, M, N, K, stream=None):

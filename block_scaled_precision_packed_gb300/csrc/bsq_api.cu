@@ -125,6 +125,33 @@ bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt
     return quantize_mx_launch(x, M, K, fmt, codes, scales, s_global, workspace, workspace_bytes, stream);
 }
 
+size_t bsq_quantize_batch_workspace_bytes(void) { return quantize_batch_workspace_bytes(); }
+
+static bsq_status quantize_batch(const bsq_qtensor* t, int n, int fmt, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (!t || n < 1 || n > BSQ_MAX_BATCH) return BSQ_ERR_INVALID_ARG;
+    QTensor q[BSQ_MAX_BATCH];
+    const int64_t kmod = fmt == kNvfp4 ? 16 : 32;
+    for (int i = 0; i < n; ++i) {
+        if (!t[i].x || !t[i].codes || !t[i].scales || !t[i].s_global) return BSQ_ERR_INVALID_ARG;
+        if (t[i].M < 1 || t[i].K < kmod || t[i].K % kmod || t[i].M >= kMaxDim || t[i].K >= kMaxDim)
+            return BSQ_ERR_INVALID_ARG;
+        if (!aligned16(t[i].x) || !aligned16(t[i].codes) || !aligned16(t[i].scales)) return BSQ_ERR_MISALIGNED;
+        q[i] = QTensor{t[i].x, t[i].M, t[i].K, t[i].codes, t[i].scales, t[i].s_global};
+    }
+    return quantize_batch_launch(q, n, fmt, ws, ws_bytes, s);
+}
+
+bsq_status bsq_quantize_mxfp6_batch(const bsq_qtensor* tensors, int n, bsq_mxfmt fmt, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream) {
+    if (!valid_mx(fmt)) return BSQ_ERR_INVALID_ARG;
+    return quantize_batch(tensors, n, fmt, workspace, workspace_bytes, stream);
+}
+
+bsq_status bsq_quantize_nvfp4_batch(const bsq_qtensor* tensors, int n, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+    return quantize_batch(tensors, n, kNvfp4, workspace, workspace_bytes, stream);
+}
+
 bsq_status bsq_quantize_nvfp4(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,
                               float* s_global, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     if (!x || !codes || !scales || !s_global) return BSQ_ERR_INVALID_ARG;

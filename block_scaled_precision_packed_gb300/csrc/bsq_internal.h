@@ -36,12 +36,24 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 
+// One tensor of a quantizer batch.
+struct QTensor {
+    const uint16_t* x;
+    int64_t M, K;
+    void* codes;
+    uint8_t* scales;
+    float* s_global;
+};
+
 // Entry points implemented per translation unit.
 bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, uint8_t* codes,
                               uint8_t* scales, float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
 bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,
                                  float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t quantize_workspace_bytes(int64_t M, int64_t K);
+size_t quantize_batch_workspace_bytes();
+// fmt: a bsq_mxfmt, or kNvfp4
+bsq_status quantize_batch_launch(const QTensor* ts, int n, int fmt, void* ws, size_t ws_bytes, cudaStream_t s);
 
 bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA, const void* W, int fw,
                        const uint8_t* sW, const float* gW, void* Y, int out, int64_t M, int64_t N,

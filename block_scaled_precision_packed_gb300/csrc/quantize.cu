@@ -366,21 +366,34 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const u
 // CTA c stores its partial in word 1 + c, then adds to the counter with
 // release semantics; after the counter reads G (acquire) every partial is
 // visible.  One polling thread per CTA keeps the counter's line uncontended.
+//
+// Several tensors can share one launch (and one barrier): each owns a range of
+// CTAs sized to its share of the slots, and reduces only its own partials, so
+// every tensor gets its own amax and s_global exactly as in a launch of its own.
 constexpr int kOneThreads = 1024;
 constexpr int kOneIters = 4;           // slots per thread: a slice holds <= 4 * kOneThreads slots
 constexpr uint32_t kChunkBytes = 32768;
 constexpr int kMaxChunks = 8;
 
-struct OnePassArgs {
+constexpr int kMaxBatch = 8;          // tensors per one-pass launch
+
+struct OneTensor {
     const uint16_t* x;
     int64_t M, K;
-    uint32_t* ws;           // [0] arrival counter (zeroed before the launch), [1..G] partial maxima
     void* codes;
     uint8_t* scales;
     float* s_global;
-    uint32_t* err;
     uint32_t slots_per_row; // padded
     uint32_t slots_per_cta; // a multiple of 4
+};
+
+// A batch of tensors in one launch: tensor i owns CTAs [first_cta[i], first_cta[i+1]).
+struct OnePassArgs {
+    OneTensor t[kMaxBatch];
+    uint32_t first_cta[kMaxBatch + 1];
+    int n;
+    uint32_t* ws;           // [0] arrival counter (zeroed before the launch), [1 + cta] partial maxima
+    uint32_t* err;
 };
 
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
@@ -431,12 +444,17 @@ __device__ __forceinline__ void load_unit(uint32_t addr, uint32_t u, uint4 (&v)[
 }
 
 template <int FMT>   // kE3M2 / kE2M3 / kE4M3, or kNvfp4
-__global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const OnePassArgs a) {
+__global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __grid_constant__ OnePassArgs args) {
     extern __shared__ __align__(128) uint8_t slice[];
     __shared__ uint64_t bar[kMaxChunks];
     __shared__ uint32_t red[32];
     __shared__ int abort_flag;
-    const uint32_t G = gridDim.x, c = blockIdx.x;
+    int ti = 0;
+    while (ti + 1 < args.n && blockIdx.x >= args.first_cta[ti + 1]) ++ti;
+    const OneTensor a = args.t[ti];                          // this CTA's tensor
+    const uint32_t G = gridDim.x;                            // the grid barrier counts every CTA
+    const uint32_t p0 = args.first_cta[ti], Gt = args.first_cta[ti + 1] - p0;
+    const uint32_t c = blockIdx.x - p0;                      // CTA index within the tensor
     const int lane = threadIdx.x & 31;
     const int64_t units_row = a.K / 32;
     const uint32_t spr = a.slots_per_row;
@@ -477,7 +495,7 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const One
         for (int it = 0; it < kOneIters; ++it) {
             const uint32_t need = min(n_chunks, ((uint32_t)(it + 1) * kOneThreads * 64 + kChunkBytes - 1) / kChunkBytes);
             while (waited < need) {
-                if (!mbar_wait(smem_u32(bar + waited), 0, a.err, &abort_flag, kErrQuantLoad)) {
+                if (!mbar_wait(smem_u32(bar + waited), 0, args.err, &abort_flag, kErrQuantLoad)) {
                     waited = n_chunks;                           // aborted: results are void
                     break;
                 }
@@ -508,13 +526,13 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const One
     // publish, then the bounded grid barrier: thread 0 stores the partial and
     // counts itself in with a release add, then polls the counter
     if (threadIdx.x == 0) {
-        a.ws[1 + c] = m;
-        red_release_add_u32(a.ws, 1u);
-        if (ld_acquire_u32(a.ws) < G) {
+        args.ws[1 + blockIdx.x] = m;
+        red_release_add_u32(args.ws, 1u);
+        if (ld_acquire_u32(args.ws) < G) {
             const uint64_t t0 = globaltimer();
-            while (ld_acquire_u32(a.ws) < G) {
+            while (ld_acquire_u32(args.ws) < G) {
                 if (globaltimer() - t0 > kWaitLimitNs) {
-                    atomicCAS(a.err, 0u, (uint32_t)kErrQuantBarrier);
+                    atomicCAS(args.err, 0u, (uint32_t)kErrQuantBarrier);
                     abort_flag = 1;
                     break;
                 }
@@ -523,7 +541,7 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const One
     }
     __syncthreads();
     uint32_t am = 0;
-    if (threadIdx.x < G) am = ld_relaxed_u32(a.ws + 1 + threadIdx.x);
+    if (threadIdx.x < Gt) am = ld_relaxed_u32(args.ws + 1 + p0 + threadIdx.x);   // this tensor's CTAs
     am = block_max(am, red);   // (its barriers also publish abort_flag)
     if (abort_flag) {
         // leave no bulk copy in flight into this CTA's shared memory
@@ -651,36 +669,62 @@ int amax_grid(const DeviceInfo* info, int64_t n) {
 }
 
 
-// The one-pass launch, when every CTA's slice fits its SM's shared memory.
+// The one-pass launch for a batch of tensors, when every CTA's slice fits its
+// SM's shared memory.  CTAs are dealt to the tensors one at a time, each to the
+// tensor whose CTAs currently carry the most slots.  Returns false (nothing
+// launched) when the batch does not fit one launch.
 template <int FMT>
-bool onepass_try(const DeviceInfo* info, const uint16_t* x, int64_t M, int64_t K, void* codes, uint8_t* scales,
-                 float* s_global, uint32_t* ws, size_t ws_bytes, cudaStream_t s, bsq_status* st) {
-    if (K % 32 != 0 || !ws) return false;
+bool onepass_batch(const DeviceInfo* info, const QTensor* ts, int n, uint32_t* ws, size_t ws_bytes, cudaStream_t s,
+                   bsq_status* st) {
     const int G = info->num_sms;
-    if (G > kOneThreads || (size_t)(G + 1) * sizeof(uint32_t) > ws_bytes) return false;
-    const int64_t spr = FMT == kNvfp4 ? pad_to(K / 16, 4) / 2 : pad_to(K / 32, 4);
-    const int64_t total = pad_to(M, 128) * spr;
-    const int64_t per_cta = pad_to((total + G - 1) / G, 4);
+    if (n < 1 || n > kMaxBatch || n > G || !ws || G > kOneThreads) return false;
+    if ((size_t)(G + 1) * sizeof(uint32_t) > ws_bytes) return false;
+    int64_t slots[kMaxBatch], spr[kMaxBatch];
+    int cnt[kMaxBatch];
+    for (int i = 0; i < n; ++i) {
+        if (ts[i].K % 32 != 0) return false;
+        spr[i] = FMT == kNvfp4 ? pad_to(ts[i].K / 16, 4) / 2 : pad_to(ts[i].K / 32, 4);
+        slots[i] = pad_to(ts[i].M, 128) * spr[i];
+        if (slots[i] >= (int64_t(1) << 31)) return false;
+        cnt[i] = 1;
+    }
+    for (int extra = G - n; extra > 0; --extra) {
+        int best = 0;
+        for (int i = 1; i < n; ++i)
+            if (slots[i] * cnt[best] > slots[best] * cnt[i]) best = i;   // slots/cnt, compared exactly
+        ++cnt[best];
+    }
     int64_t slice_max = (int64_t)info->max_smem_optin - 1024;
     if (slice_max > (int64_t)kMaxChunks * kChunkBytes) slice_max = (int64_t)kMaxChunks * kChunkBytes;
-    if (per_cta * 64 > slice_max || per_cta > (int64_t)kOneIters * kOneThreads || total >= (int64_t(1) << 31))
-        return false;
-    const size_t smem = (size_t)(per_cta * 64);
-    static std::once_flag once[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    bool ok = dev >= 0 && dev < 64;
-    if (ok) std::call_once(once[dev], [&] {
-        ok = cudaFuncSetAttribute(quant_onepass_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  info->max_smem_optin - 1024) == cudaSuccess;
-    });
-    if (!ok) { (void)cudaGetLastError(); return false; }
     OnePassArgs a;
-    a.x = x; a.M = M; a.K = K; a.ws = ws; a.codes = codes; a.scales = scales; a.s_global = s_global;
-    a.err = info->err; a.slots_per_row = (uint32_t)spr; a.slots_per_cta = (uint32_t)per_cta;
+    int64_t per_max = 0;
+    uint32_t first = 0;
+    for (int i = 0; i < n; ++i) {
+        const int64_t per = pad_to((slots[i] + cnt[i] - 1) / cnt[i], 4);
+        if (per * 64 > slice_max || per > (int64_t)kOneIters * kOneThreads) return false;
+        per_max = per > per_max ? per : per_max;
+        OneTensor& t = a.t[i];
+        t.x = ts[i].x; t.M = ts[i].M; t.K = ts[i].K; t.codes = ts[i].codes; t.scales = ts[i].scales;
+        t.s_global = ts[i].s_global; t.slots_per_row = (uint32_t)spr[i]; t.slots_per_cta = (uint32_t)per;
+        a.first_cta[i] = first;
+        first += (uint32_t)cnt[i];
+    }
+    for (int i = n; i <= kMaxBatch; ++i) a.first_cta[i] = first;
+    for (int i = n; i < kMaxBatch; ++i) a.t[i] = a.t[0];
+    a.n = n; a.ws = ws; a.err = info->err;
+    const size_t smem = (size_t)(per_max * 64);
+    static std::once_flag once[64];
+    static bool ok_dev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::call_once(once[dev], [&] {
+        ok_dev[dev] = cudaFuncSetAttribute(quant_onepass_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           info->max_smem_optin - 1024) == cudaSuccess;
+    });
+    if (!ok_dev[dev]) { (void)cudaGetLastError(); return false; }
     if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) { *st = BSQ_ERR_CUDA; return true; }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(G, 1, 1);
+    cfg.gridDim = dim3(first, 1, 1);
     cfg.blockDim = dim3(kOneThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -695,7 +739,43 @@ bool onepass_try(const DeviceInfo* info, const uint16_t* x, int64_t M, int64_t K
     *st = BSQ_OK;
     return true;
 }
+
+template <int FMT>
+bool onepass_try(const DeviceInfo* info, const uint16_t* x, int64_t M, int64_t K, void* codes, uint8_t* scales,
+                 float* s_global, uint32_t* ws, size_t ws_bytes, cudaStream_t s, bsq_status* st) {
+    const QTensor t = {x, M, K, codes, scales, s_global};
+    return onepass_batch<FMT>(info, &t, 1, ws, ws_bytes, s, st);
+}
 }  // namespace
+
+size_t quantize_batch_workspace_bytes() { return (size_t)kMaxPartials * sizeof(uint32_t); }
+
+bsq_status quantize_batch_launch(const QTensor* ts, int n, int fmt, void* ws, size_t ws_bytes, cudaStream_t s) {
+    bsq_status st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
+    if (!ws || ws_bytes < quantize_batch_workspace_bytes()) return BSQ_ERR_WORKSPACE;
+    if (!aligned16(ws)) return BSQ_ERR_MISALIGNED;
+    uint32_t* partial = static_cast<uint32_t*>(ws);
+    bool done = false;
+    switch (fmt) {
+    case kE3M2: done = onepass_batch<kE3M2>(info, ts, n, partial, ws_bytes, s, &st); break;
+    case kE2M3: done = onepass_batch<kE2M3>(info, ts, n, partial, ws_bytes, s, &st); break;
+    case kE4M3: done = onepass_batch<kE4M3>(info, ts, n, partial, ws_bytes, s, &st); break;
+    default: done = onepass_batch<kNvfp4>(info, ts, n, partial, ws_bytes, s, &st); break;
+    }
+    if (done) return st;
+    // too large for one launch: the tensors one after another on the stream
+    for (int i = 0; i < n; ++i) {
+        const QTensor& t = ts[i];
+        st = fmt == kNvfp4 ? quantize_nvfp4_launch(t.x, t.M, t.K, static_cast<uint32_t*>(t.codes), t.scales,
+                                                   t.s_global, ws, ws_bytes, s)
+                           : quantize_mx_launch(t.x, t.M, t.K, fmt, static_cast<uint8_t*>(t.codes), t.scales,
+                                                t.s_global, ws, ws_bytes, s);
+        if (st != BSQ_OK) return st;
+    }
+    return BSQ_OK;
+}
 
 size_t quantize_workspace_bytes(int64_t M, int64_t K) {
     if (M * K <= kFusedMaxElems) return 0;

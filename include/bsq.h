@@ -141,6 +141,43 @@ BSQ_API bsq_status bsq_quantize_nvfp4(const uint16_t* x, int64_t M, int64_t K,
                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Batched quantizers -- up to BSQ_MAX_BATCH independent tensors (for example
+ * a layer's activation and its weight) in one launch.  Each tensor is
+ * quantized exactly as the single-tensor entry point above would (its own
+ * amax, block scales and s_global; bit-identical results); the batch shares
+ * one launch and one grid-wide wait instead of paying them per tensor.  The
+ * b12x pages quantize "grouped" tensors (several experts' rows with
+ * per-group global scales, _lib/fp6.py quantize_grouped_mxfp6_torch); this is
+ * that idea for tensors of different shapes, not the pages' interleaved
+ * grouped code layout.
+ *   tensors[i]  as the single-tensor arguments: x [M, K] bf16 bits; codes as
+ *               bsq_quantize_mxfp6 / bsq_quantize_nvfp4 lay them out; scales
+ *               bsq_scale_bytes(M, K/32) (MX) or bsq_scale_bytes(M, K/16)
+ *               (nvfp4); s_global one device float.  The tensors' outputs must
+ *               not overlap one another or any input.
+ *   n           1 .. BSQ_MAX_BATCH.
+ *   workspace   >= bsq_quantize_batch_workspace_bytes() bytes of device
+ *               memory, 16-byte aligned, owned by the call until its kernels
+ *               finish.
+ * A batch too large for one launch (more shared memory than the GPU has) runs
+ * its tensors one after another on the stream, with the same results.
+ */
+#define BSQ_MAX_BATCH 8
+typedef struct {
+    const uint16_t* x;
+    int64_t M, K;
+    void* codes;
+    uint8_t* scales;
+    float* s_global;
+} bsq_qtensor;
+
+BSQ_API size_t bsq_quantize_batch_workspace_bytes(void);
+BSQ_API bsq_status bsq_quantize_mxfp6_batch(const bsq_qtensor* tensors, int n, bsq_mxfmt fmt,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+BSQ_API bsq_status bsq_quantize_nvfp4_batch(const bsq_qtensor* tensors, int n,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * bsq_gemm_nvfp4 -- Y = gA*gW * A W^T with both operands nvfp4, on the 5th-gen
  * tensor cores (tcgen05.mma kind::mxf4nvf4, ue4m3 scale per 16).
  *   A [M, K/8] words + sA (bsq_scale_bytes(M, K/16)); W [N, K/8] + sW.

@@ -44,6 +44,7 @@ def test_host_helpers(lib):
         assert bsq.scale_bytes(rows, blocks) == O.scale_bytes(rows, blocks)
     assert bsq.quantize_workspace_bytes(16, 4096) == 0
     assert bsq.quantize_workspace_bytes(4096, 4096) >= 1024
+    assert bsq.quantize_batch_workspace_bytes() >= 4 * (1 + 1024)   # counter + a partial per CTA
 
 
 def test_oracle_and_library_share_nothing():

@@ -111,3 +111,84 @@ def test_dequant_matches_oracle(bsq, name, fmt):
     bsq.dequant_nvfp4_(w, sw, gw, out2, M, K)
     want2 = O.dequant_nvfp4(w.cpu().numpy().view(np.uint32), host_bytes(sw), float(gw.item()), M, K)
     assert np.array_equal(out2.cpu().numpy(), want2.astype(np.float32))
+
+
+# ---- batched quantizers: each tensor exactly as its own call would be ----
+BATCH = [(128, 4096), (3, 96), (1100, 1024), (257, 4128), (16, 64)]
+
+
+def _mx_outputs(M, K, name):
+    codes = torch.empty((M, K if name == "e4m3" else 3 * K // 4), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(O.scale_bytes(M, K // 32), dtype=torch.uint8, device="cuda")
+    return codes, scales, torch.empty(1, dtype=torch.float32, device="cuda")
+
+
+@pytest.mark.parametrize("name,fmt", MX)
+def test_quantize_mx_batch_bit_exact(bsq, name, fmt):
+    xs = [fixture(M, K, 500 + i) for i, (M, K) in enumerate(BATCH)]
+    xs[1][:] = 0                                   # an all-zero tensor in the batch: gs = 0
+    outs = [_mx_outputs(M, K, name) for M, K in BATCH]
+    ws = torch.empty(bsq.quantize_batch_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    bsq.reset_launch_counts()
+    bsq.quantize_mxfp6_batch_([(dev_tensor(x),) + o for x, o in zip(xs, outs)], bsq.FMT_IDS[name], ws)
+    torch.cuda.synchronize()
+    assert bsq.launch_count("quant_mx") == 1 and bsq.launch_count("amax") == 0   # one launch for all
+    for x, (codes, scales, g) in zip(xs, outs):
+        oc, os_, og = O.quantize_mx(x, fmt)
+        assert np.array_equal(host_bytes(codes).reshape(oc.shape), oc)
+        assert np.array_equal(host_bytes(scales), os_)
+        assert np.float32(g.item()) == np.float32(og)
+
+
+def test_quantize_nvfp4_batch_bit_exact(bsq):
+    shapes = BATCH + [(7, 4096)]
+    xs = [fixture(M, K, 600 + i, std=1.0) for i, (M, K) in enumerate(shapes)]
+    outs = [(torch.empty((M, K // 8), dtype=torch.int32, device="cuda"),
+             torch.empty(O.scale_bytes(M, K // 16), dtype=torch.uint8, device="cuda"),
+             torch.empty(1, dtype=torch.float32, device="cuda")) for M, K in shapes]
+    ws = torch.empty(bsq.quantize_batch_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    bsq.quantize_nvfp4_batch_([(dev_tensor(x),) + o for x, o in zip(xs, outs)], ws)
+    torch.cuda.synchronize()
+    for x, (codes, scales, g) in zip(xs, outs):
+        oc, os_, og = O.quantize_nvfp4(x)
+        assert np.array_equal(codes.cpu().numpy().view(np.uint32), oc)
+        assert np.array_equal(host_bytes(scales), os_)
+        assert np.float32(g.item()) == np.float32(og)
+
+
+def test_quantize_batch_beyond_one_launch_runs_one_by_one(bsq):
+    """Two tensors whose slices do not fit the GPU's shared memory together: the
+    call falls back to one quantizer per tensor, with the same results."""
+    shapes = [(4096, 4096), (1024, 4096)]
+    xs = [fixture(M, K, 700 + i) for i, (M, K) in enumerate(shapes)]
+    outs = [_mx_outputs(M, K, "e2m3") for M, K in shapes]
+    ws = torch.empty(bsq.quantize_batch_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    bsq.reset_launch_counts()
+    bsq.quantize_mxfp6_batch_([(dev_tensor(x),) + o for x, o in zip(xs, outs)], bsq.FMT_IDS["e2m3"], ws)
+    torch.cuda.synchronize()
+    assert bsq.launch_count("quant_mx") == 2
+    for x, (codes, scales, g) in zip(xs, outs):
+        oc, os_, og = O.quantize_mx(x, O.E2M3)
+        assert np.array_equal(host_bytes(codes).reshape(oc.shape), oc)
+        assert np.array_equal(host_bytes(scales), os_)
+        assert np.float32(g.item()) == np.float32(og)
+
+
+def test_quantize_batch_bad_arguments(bsq):
+    import ctypes
+    L = bsq.load()
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    c, s, g = _mx_outputs(4, 64, "e3m2")
+    ws = torch.empty(bsq.quantize_batch_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    wsp, wsb = ctypes.c_void_p(ws.data_ptr()), ws.numel()
+    bsq.reset_launch_counts()
+    one = bsq._qtensors([(x, c, s, g)])
+    assert L.bsq_quantize_mxfp6_batch(ctypes.cast(one, ctypes.c_void_p), 0, 0, wsp, wsb, st) == 1       # n = 0
+    nine = bsq._qtensors([(x, c, s, g)] * 9)
+    assert L.bsq_quantize_mxfp6_batch(ctypes.cast(nine, ctypes.c_void_p), 9, 0, wsp, wsb, st) == 1      # n > 8
+    bad = bsq._qtensors([(x, c, s, g)])
+    bad[0].K = 48
+    assert L.bsq_quantize_mxfp6_batch(ctypes.cast(bad, ctypes.c_void_p), 1, 0, wsp, wsb, st) == 1       # K % 32
+    assert L.bsq_quantize_mxfp6_batch(ctypes.cast(one, ctypes.c_void_p), 1, 0, wsp, 64, st) == 4        # workspace
+    assert sum(bsq.launch_count(k) for k in bsq.KERNEL_IDS) == 0
