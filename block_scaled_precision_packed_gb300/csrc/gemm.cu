@@ -88,6 +88,10 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Programmatic dependent launch: the next kernel on the stream may start its
+// prologue; this kernel waits for the previous one's results before reading them.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t local_addr, uint32_t rank) {
     uint32_t remote;
     float4 v;
@@ -153,6 +157,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_s;
+    // the setup above overlaps the previous kernel; its outputs (A, W, their
+    // scales and global factors) are read only after this
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -423,6 +430,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         cluster_sync();                                   // no rank leaves while others read its smem
     }
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -479,39 +487,42 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
                        cudaStream_t s) {
     using C = Cfg<NVF4, BN>;
     static std::once_flag flags[64];
+    static bool ok_dev[64];
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
-    bool attr_ok = true;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
     std::call_once(flags[dev], [&] {
-        attr_ok = cudaFuncSetAttribute(gemm_kernel<NVF4, BN, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes) == cudaSuccess;
+        ok_dev[dev] = cudaFuncSetAttribute(gemm_kernel<NVF4, BN, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           C::kSmemBytes) == cudaSuccess;
     });
-    if (!attr_ok) return BSQ_ERR_CUDA;
+    if (!ok_dev[dev]) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
     const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    // programmatic dependent launch: the prologue may overlap the previous kernel
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     if constexpr (SPLIT == 1) {
-        const int grid = (int)imin64(tiles, info->num_sms);
-        gemm_kernel<NVF4, BN, 1><<<grid, kThreads, C::kSmemBytes, s>>>(ta, tw, a);
-        return launch_status();
+        cfg.gridDim = dim3((unsigned)imin64(tiles, info->num_sms), 1, 1);
     } else {
-        cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(tiles * SPLIT), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = C::kSmemBytes;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = SPLIT;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gemm_kernel<NVF4, BN, SPLIT>, ta, tw, a) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return BSQ_ERR_CUDA;
-        }
-        return BSQ_OK;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = SPLIT;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    if (cudaLaunchKernelEx(&cfg, gemm_kernel<NVF4, BN, SPLIT>, ta, tw, a) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return BSQ_ERR_CUDA;
+    }
+    return BSQ_OK;
 }
 
 }  // namespace

@@ -540,6 +540,7 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
         }
     }
     __syncthreads();
+    launch_dependents();       // the next kernel (a GEMM) may launch; it waits for this grid's results
     uint32_t am = 0;
     if (threadIdx.x < Gt) am = ld_relaxed_u32(args.ws + 1 + p0 + threadIdx.x);   // this tensor's CTAs
     am = block_max(am, red);   // (its barriers also publish abort_flag)
