@@ -211,6 +211,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else if (warp == 1) {
         if (lane == 0) {
             // --------------------------------------------------- MMA issue --
+            // Descriptors of stage 0's tiles and scale atoms; a stage, atom or
+            // K step is an offset in the 16-byte-unit address field (smem < 256 KB),
+            // so the single issuing thread spends one add per tcgen05 instruction.
+            const uint64_t dA0 = smem_desc(smem_u32(sA_st), 16, 1024, 2);
+            const uint64_t dB0 = smem_desc(smem_u32(sB_st), 16, 1024, 2);
+            const uint64_t dSA0 = smem_desc(smem_u32(sSfa), 0, 128, 0);
+            const uint64_t dSB0 = smem_desc(smem_u32(sSfb), 0, 128, 0);
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -226,22 +233,30 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t sf_col = (uint32_t)(BN + stage * C::kSfColsPerStage);
                     const int64_t kg = ks * C::kAtomsPerStage;
                     const int natoms = (int)imin64(C::kAtomsPerStage, args.cpd4 - kg);
+                    const uint64_t sa = dSA0 + (uint64_t)(stage * (C::kSfaBytes >> 4));
+                    const uint64_t sb = dSB0 + (uint64_t)(stage * (C::kSfbBytes >> 4));
                     // scale atoms -> TMEM (4 columns each, replicated to all lane quarters)
-                    for (int a = 0; a < natoms; ++a) {
-                        tc_cp_scales(tmem + sf_col + 4 * a,
-                                     smem_desc(smem_u32(sSfa + stage * C::kSfaBytes + a * kAtom), 0, 128, 0));
+                    auto copy_atom = [&](int a) {
+                        tc_cp_scales(tmem + sf_col + 4 * a, sa + (uint64_t)(a * (kAtom >> 4)));
 #pragma unroll
                         for (int rt = 0; rt < C::kRowTilesB; ++rt)
                             tc_cp_scales(tmem + sf_col + C::kSfaCols + (a * C::kRowTilesB + rt) * 4,
-                                         smem_desc(smem_u32(sSfb + stage * C::kSfbBytes +
-                                                            (rt * C::kAtomsPerStage + a) * kAtom), 0, 128, 0));
+                                         sb + (uint64_t)((rt * C::kAtomsPerStage + a) * (kAtom >> 4)));
+                    };
+                    if (natoms == C::kAtomsPerStage) {
+#pragma unroll
+                        for (int a = 0; a < C::kAtomsPerStage; ++a) copy_atom(a);
+                    } else {
+                        for (int a = 0; a < natoms; ++a) copy_atom(a);
                     }
-                    const uint32_t a_base = smem_u32(sA_st + stage * C::kABytes);
-                    const uint32_t b_base = smem_u32(sB_st + stage * C::kBBytes);
+                    const uint64_t a_st = dA0 + (uint64_t)(stage * (C::kABytes >> 4));
+                    const uint64_t b_st = dB0 + (uint64_t)(stage * (C::kBBytes >> 4));
                     const int n_mma = NVF4 ? (int)imin64(4, (K - ks * C::kStageK) / 64) : 4;
-                    for (int kk = 0; kk < n_mma; ++kk) {
-                        const uint64_t ad = smem_desc(a_base + 32 * kk, 16, 1024, 2);
-                        const uint64_t bd = smem_desc(b_base + 32 * kk, 16, 1024, 2);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (kk >= n_mma) break;
+                        const uint64_t ad = a_st + (uint64_t)(2 * kk);          // +32 bytes per K step
+                        const uint64_t bd = b_st + (uint64_t)(2 * kk);
                         const uint32_t acc = (ks > ks_begin || kk > 0) ? 1u : 0u;
                         if constexpr (NVF4) {
                             tc_mma_mxf4nvf4(tmem, ad, bd, args.idesc, tmem + sf_col + 4 * kk,
