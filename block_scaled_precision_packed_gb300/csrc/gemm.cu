@@ -231,8 +231,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     }
                     tc_fence_after();
                     const uint32_t sf_col = (uint32_t)(BN + stage * C::kSfColsPerStage);
-                    const int64_t kg = ks * C::kAtomsPerStage;
-                    const int natoms = (int)imin64(C::kAtomsPerStage, args.cpd4 - kg);
                     const uint64_t sa = dSA0 + (uint64_t)(stage * (C::kSfaBytes >> 4));
                     const uint64_t sb = dSB0 + (uint64_t)(stage * (C::kSfbBytes >> 4));
                     // scale atoms -> TMEM (4 columns each, replicated to all lane quarters)
@@ -243,18 +241,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             tc_cp_scales(tmem + sf_col + C::kSfaCols + (a * C::kRowTilesB + rt) * 4,
                                          sb + (uint64_t)((rt * C::kAtomsPerStage + a) * (kAtom >> 4)));
                     };
-                    if (natoms == C::kAtomsPerStage) {
-#pragma unroll
-                        for (int a = 0; a < C::kAtomsPerStage; ++a) copy_atom(a);
-                    } else {
-                        for (int a = 0; a < natoms; ++a) copy_atom(a);
-                    }
                     const uint64_t a_st = dA0 + (uint64_t)(stage * (C::kABytes >> 4));
                     const uint64_t b_st = dB0 + (uint64_t)(stage * (C::kBBytes >> 4));
                     const int n_mma = NVF4 ? (int)imin64(4, (K - ks * C::kStageK) / 64) : 4;
+                    // MX: the stage's one atom per operand serves all 4 K steps
+                    if constexpr (!NVF4) copy_atom(0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         if (kk >= n_mma) break;
+                        // nvfp4: each K step's own atoms right before its MMA, so the
+                        // next step's copies run while this MMA executes
+                        if constexpr (NVF4) copy_atom(kk);
                         const uint64_t ad = a_st + (uint64_t)(2 * kk);          // +32 bytes per K step
                         const uint64_t bd = b_st + (uint64_t)(2 * kk);
                         const uint32_t acc = (ks > ks_begin || kk > 0) ? 1u : 0u;
