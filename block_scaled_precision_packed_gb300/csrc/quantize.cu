@@ -362,10 +362,11 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const u
 // the scale buffer is written too; CTA ranges are multiples of four slots, so
 // a group of four scale bytes never straddles two CTAs.
 //
-// Grid barrier: workspace word 0 counts arrivals (zeroed before the launch);
-// CTA c stores its partial in word 1 + c, then adds to the counter with
-// release semantics; after the counter reads G (acquire) every partial is
-// visible.  One polling thread per CTA keeps the counter's line uncontended.
+// Grid barrier: CTA c stores its partial in workspace word 1 + c, then adds to
+// the control block's arrival counter with release semantics; after the counter
+// reads G (acquire) every partial is visible.  One polling thread per CTA keeps
+// the counter's line uncontended.  Each CTA then counts itself out; the last
+// one out zeroes both counters for the next call.
 //
 // Several tensors can share one launch (and one barrier): each owns a range of
 // CTAs sized to its share of the slots, and reduces only its own partials, so
@@ -376,6 +377,15 @@ constexpr uint32_t kChunkBytes = 32768;
 constexpr int kMaxChunks = 8;
 
 constexpr int kMaxBatch = 8;          // tensors per one-pass launch
+// One-pass control block, after the partials in the caller's workspace:
+// [0..1] a 64-bit magic (valid: the counters below are consistent), [2] arrivals,
+// [3] departures.  Every call leaves it valid with both counters zero, so no
+// launch needs a memset; a workspace that does not hold the magic (a fresh
+// allocation, or one left by a call that timed out) is initialized by CTA 0
+// while the other CTAs wait for the magic.
+constexpr int kCtlWord = kMaxPartials;
+constexpr int kCtlWords = 64;
+constexpr uint64_t kCtlMagic = 0x7F4A7C159E3779B9ull;
 
 struct OneTensor {
     const uint16_t* x;
@@ -392,7 +402,7 @@ struct OnePassArgs {
     OneTensor t[kMaxBatch];
     uint32_t first_cta[kMaxBatch + 1];
     int n;
-    uint32_t* ws;           // [0] arrival counter (zeroed before the launch), [1 + cta] partial maxima
+    uint32_t* ws;           // [1 + cta] partial maxima; [kCtlWord ..] the control block
     uint32_t* err;
 };
 
@@ -405,6 +415,14 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint32_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(uint32_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
@@ -476,6 +494,24 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
             mbar_arrive_expect_tx(smem_u32(bar + k), n);
             bulk_load(slice_addr + off, src + off, n, smem_u32(bar + k));
         }
+        // control block: initialize it (CTA 0) or wait for it if it is not valid
+        uint32_t* ctl = args.ws + kCtlWord;
+        if (ld_acquire_u64(ctl) != kCtlMagic) {
+            if (blockIdx.x == 0) {
+                ctl[2] = 0;
+                ctl[3] = 0;
+                st_release_u64(ctl, kCtlMagic);          // the zeroed counters before the magic
+            } else {
+                const uint64_t t0 = globaltimer();
+                while (ld_acquire_u64(ctl) != kCtlMagic) {
+                    if (globaltimer() - t0 > kWaitLimitNs) {
+                        atomicCAS(args.err, 0u, (uint32_t)kErrQuantBarrier);
+                        abort_flag = 1;
+                        break;
+                    }
+                }
+            }
+        }
     }
     __syncthreads();
 
@@ -526,17 +562,24 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
     // publish, then the bounded grid barrier: thread 0 stores the partial and
     // counts itself in with a release add, then polls the counter
     if (threadIdx.x == 0) {
+        uint32_t* ctl = args.ws + kCtlWord;
         args.ws[1 + blockIdx.x] = m;
-        red_release_add_u32(args.ws, 1u);
-        if (ld_acquire_u32(args.ws) < G) {
+        red_release_add_u32(ctl + 2, 1u);
+        if (ld_acquire_u32(ctl + 2) < G) {
             const uint64_t t0 = globaltimer();
-            while (ld_acquire_u32(args.ws) < G) {
-                if (globaltimer() - t0 > kWaitLimitNs) {
+            while (ld_acquire_u32(ctl + 2) < G) {
+                if (abort_flag || globaltimer() - t0 > kWaitLimitNs) {
                     atomicCAS(args.err, 0u, (uint32_t)kErrQuantBarrier);
                     abort_flag = 1;
                     break;
                 }
             }
+        }
+        if (abort_flag) {
+            st_release_u64(ctl, 0ull);                   // the next call re-initializes the block
+        } else if (atomicAdd(ctl + 3, 1u) == G - 1) {    // last one out: zero the counters
+            ctl[2] = 0;
+            ctl[3] = 0;
         }
     }
     __syncthreads();
@@ -679,7 +722,7 @@ bool onepass_batch(const DeviceInfo* info, const QTensor* ts, int n, uint32_t* w
                    bsq_status* st) {
     const int G = info->num_sms;
     if (n < 1 || n > kMaxBatch || n > G || !ws || G > kOneThreads) return false;
-    if ((size_t)(G + 1) * sizeof(uint32_t) > ws_bytes) return false;
+    if ((size_t)(kCtlWord + 4) * sizeof(uint32_t) > ws_bytes || G + 1 > kCtlWord) return false;
     int64_t slots[kMaxBatch], spr[kMaxBatch];
     int cnt[kMaxBatch];
     for (int i = 0; i < n; ++i) {
@@ -723,7 +766,6 @@ bool onepass_batch(const DeviceInfo* info, const QTensor* ts, int n, uint32_t* w
                                            info->max_smem_optin - 1024) == cudaSuccess;
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return false; }
-    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) { *st = BSQ_ERR_CUDA; return true; }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(first, 1, 1);
     cfg.blockDim = dim3(kOneThreads, 1, 1);
@@ -749,7 +791,7 @@ bool onepass_try(const DeviceInfo* info, const uint16_t* x, int64_t M, int64_t K
 }
 }  // namespace
 
-size_t quantize_batch_workspace_bytes() { return (size_t)kMaxPartials * sizeof(uint32_t); }
+size_t quantize_batch_workspace_bytes() { return (size_t)(kMaxPartials + kCtlWords) * sizeof(uint32_t); }
 
 bsq_status quantize_batch_launch(const QTensor* ts, int n, int fmt, void* ws, size_t ws_bytes, cudaStream_t s) {
     bsq_status st;
@@ -780,7 +822,7 @@ bsq_status quantize_batch_launch(const QTensor* ts, int n, int fmt, void* ws, si
 
 size_t quantize_workspace_bytes(int64_t M, int64_t K) {
     if (M * K <= kFusedMaxElems) return 0;
-    return (size_t)kMaxPartials * sizeof(uint32_t);
+    return (size_t)(kMaxPartials + kCtlWords) * sizeof(uint32_t);
 }
 
 bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, uint8_t* codes,

@@ -81,10 +81,15 @@ BSQ_API size_t bsq_scale_bytes(int64_t rows, int64_t n_blocks);
 
 /* Workspace the quantizers need for an [M, K] input; 0 when M*K is small
  * enough for the single-cluster path.  It holds the per-CTA partial maxima of
- * the tensor amax (and, on the one-pass cooperative path, an arrival counter
- * that the call zeroes on its stream before the kernel).  A call owns its
- * workspace until its kernels finish: two calls whose kernels may overlap on
- * the GPU need two workspaces.  Always 256-byte aligned sizes. */
+ * the tensor amax and, at its end, a small control block for the grid-wide
+ * wait of the one-pass path.  Any initial contents are accepted: a call that
+ * does not find the block's 64-bit marker initializes it, every call leaves it
+ * ready for the next, and a call that reports a device error clears the marker
+ * so the next call starts afresh.  (Contents that happen to hold the exact
+ * marker with inconsistent counters -- odds 2^-64 for random bytes -- are not
+ * detected.)  A call owns its workspace until its kernels finish: two calls
+ * whose kernels may overlap on the GPU need two workspaces.  Always 256-byte
+ * aligned sizes. */
 BSQ_API size_t bsq_quantize_workspace_bytes(int64_t M, int64_t K);
 
 /*

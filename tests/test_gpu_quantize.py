@@ -192,3 +192,29 @@ def test_quantize_batch_bad_arguments(bsq):
     assert L.bsq_quantize_mxfp6_batch(ctypes.cast(bad, ctypes.c_void_p), 1, 0, wsp, wsb, st) == 1       # K % 32
     assert L.bsq_quantize_mxfp6_batch(ctypes.cast(one, ctypes.c_void_p), 1, 0, wsp, 64, st) == 4        # workspace
     assert sum(bsq.launch_count(k) for k in bsq.KERNEL_IDS) == 0
+
+
+@pytest.mark.parametrize("fill", ["zeros", "ones", "random"])
+def test_one_pass_accepts_any_workspace_contents(bsq, fill):
+    """The one-pass path keeps its grid-wait control block in the workspace with
+    no memset per call: a fresh workspace of any contents is initialized by the
+    first call, and the next calls on the same workspace see it ready."""
+    M, K = 512, 2048
+    wsb = bsq.quantize_workspace_bytes(M, K)
+    if fill == "zeros":
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    elif fill == "ones":
+        ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device="cuda")
+    else:
+        ws = torch.from_numpy(np.random.default_rng(5).integers(0, 256, wsb, dtype=np.uint8)).cuda()
+    for call in range(3):
+        x = fixture(M, K, 800 + call)
+        codes, scales, g = _mx_outputs(M, K, "e3m2")
+        bsq.reset_launch_counts()
+        bsq.quantize_mxfp6_(dev_tensor(x), O.E3M2, codes, scales, g, ws)
+        torch.cuda.synchronize()
+        assert bsq.launch_count("quant_mx") == 1 and bsq.launch_count("amax") == 0   # the one-pass path
+        oc, os_, og = O.quantize_mx(x, O.E3M2)
+        assert np.array_equal(host_bytes(codes).reshape(oc.shape), oc)
+        assert np.array_equal(host_bytes(scales), os_)
+        assert np.float32(g.item()) == np.float32(og)
