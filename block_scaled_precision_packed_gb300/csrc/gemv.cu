@@ -651,6 +651,224 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
     }
 }
 
+// Resident-x variant (small M, when M x K fits next to a 6-stage ring): x is
+// checked once, staged once (f16 when every value is zero or an f16 normal,
+// else raw bf16) and stays in shared memory for the whole K walk, so the
+// stage loop has no x staging and no consumer-wide barrier.  The ring depth is
+// whatever the rest of shared memory holds (6..8 stages).
+constexpr int kResMaxStages = 8;
+
+// both halves of a bf16x2 word zero or f16 normals (bf16 exponent field 113..142)
+__device__ __forceinline__ bool f16_exact2(uint32_t w) {
+    const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
+    return (lo == 0 || lo - (113u << 7) < (30u << 7)) && (hi == 0 || hi - (113u << 7) < (30u << 7));
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_rn(uint32_t w) {
+    bool unused;
+    return bf16x2_to_f16x2(w, unused);
+}
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool ok) {
+    uint32_t r;
+    asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; barrier.red.and.pred p, %2, %3, q; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(r) : "r"((uint32_t)ok), "r"(id), "r"(nthreads) : "memory");
+    return r != 0;
+}
+
+template <int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, 1)
+gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, int n_stages, uint32_t x_pitch) {
+    constexpr int R = 16 * CW;
+    constexpr int kCons = CW * 32;
+    constexpr int kWBytes = R * 128;
+    constexpr int kSBytes = kMaxRowBlocks * 2048;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int64_t M = args.M, N = args.N, K = args.K;
+    uint8_t* sWst = smem;
+    uint8_t* sSst = sWst + n_stages * kWBytes;
+    uint8_t* sX = sSst + n_stages * kSBytes;                            // M rows x x_pitch bytes
+    uint64_t* full = reinterpret_cast<uint64_t*>(sX + M * x_pitch);      // x_pitch % 16 == 0
+    uint64_t* empty = full + kResMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kResMaxStages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row_base = (int64_t)blockIdx.x * R;
+    const int nst = (int)((K + 255) / 256);
+    const int rb0 = (int)(row_base >> 7);
+    const int rb1 = (int)((row_base + R - 1) >> 7);
+    const int64_t n_rb_total = (N + 127) / 128;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int st = 0; st < n_stages; ++st) {
+            mbar_init(smem_u32(full + st), 1);
+            mbar_init(smem_u32(empty + st), CW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer (as in gemv_nvf4_kernel) ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int st = i % n_stages;
+                if (i >= n_stages &&
+                    !mbar_wait(smem_u32(empty + st), ((i / n_stages) - 1) & 1, args.err, abort_flag, kErrGemvProducer))
+                    break;
+                const int64_t atoms_left = args.cpd4 - 4LL * i;
+                const uint32_t n_atoms = (uint32_t)(atoms_left < 4 ? atoms_left : 4);
+                uint32_t n_rb = 0;
+                for (int rb = rb0; rb <= rb1 && rb < n_rb_total; ++rb) ++n_rb;
+                mbar_arrive_expect_tx(smem_u32(full + st), kWBytes + n_rb * n_atoms * 512);
+                tma_load_2d(smem_u32(sWst + st * kWBytes), &tmW, smem_u32(full + st), i * 128, (int32_t)row_base);
+                for (uint32_t j = 0; j < n_rb; ++j) {
+                    const uint8_t* src = args.sW + ((int64_t)(rb0 + j) * args.cpd4 + 4LL * i) * 512;
+                    bulk_load(smem_u32(sSst + st * kSBytes + j * 2048), src, n_atoms * 512, smem_u32(full + st));
+                }
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                for (int i = issued - n_stages < 0 ? 0 : issued - n_stages; i < issued; ++i) {
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(full + i % n_stages), (i / n_stages) & 1) &&
+                           globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    // 1. x -> shared memory once: check every value (one AND over the consumer
+    //    threads), then store it as f16 or as raw bf16; x is re-read from L2.
+    //    A row holds nst * 256 values (the K tail zero, as the weight's TMA
+    //    fill there is zero) plus 64 bytes of padding.
+    const int64_t units = M * (K / 8);                                  // 16-byte units of x
+    bool ok = true;
+    for (int64_t u = threadIdx.x; u < units; u += kCons) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(args.x) + u);
+        ok = ok && f16_exact2(v.x) && f16_exact2(v.y) && f16_exact2(v.z) && f16_exact2(v.w);
+    }
+    const bool use_f16 = bar_and(1, kCons, ok);
+    const int64_t row_units = (int64_t)nst * 32;                        // 16-byte units per staged row
+    for (int64_t u = threadIdx.x; u < M * row_units; u += kCons) {
+        const int64_t r = u / row_units, c = u - r * row_units;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (c < K / 8) {
+            v = __ldg(reinterpret_cast<const uint4*>(args.x + r * K) + c);
+            if (use_f16)
+                v = make_uint4(bf16x2_to_f16x2_rn(v.x), bf16x2_to_f16x2_rn(v.y), bf16x2_to_f16x2_rn(v.z),
+                               bf16x2_to_f16x2_rn(v.w));
+        }
+        *reinterpret_cast<uint4*>(sX + r * x_pitch + 16 * c) = v;
+    }
+    bar_and(1, kCons, true);                                            // x staged for every warp
+
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t row0 = row_base + warp * 16 + g, row1 = row0 + 8;
+    const int nblocks32 = (int)(K / 16);     // K < 2^31: the entry point bounds every dimension
+    const int mrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int mcol = lane >> 4;
+    int soff[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int64_t row = r ? row1 : row0;
+        soff[r] = (int)((row >> 7) - rb0) * 2048 + (int)(row & 31) * 16 + (int)((row >> 5) & 3) * 4;
+    }
+    const uint32_t ssel = (t >> 1) ? 0x31u : 0x20u;
+    const bool x_row = g < M;                                           // B rows past M are zero
+    const uint32_t xrow = smem_u32(sX) + (uint32_t)(x_row ? g : 0) * x_pitch + 16 * t;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+
+    auto consume = [&](auto f16_tag, auto tail_tag, uint32_t wst, uint32_t sst, int i) {
+        constexpr bool F16 = decltype(f16_tag)::value;
+        constexpr bool TAIL = decltype(tail_tag)::value;
+        const uint32_t xs = xrow + (uint32_t)i * 512;                   // 256 values of this stage
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp) {
+            uint32_t wr[4];
+            ldmatrix_x4(wst + mrow * 128 + (((2 * cp + mcol) ^ (mrow & 7)) << 4), wr);
+            uint32_t S[2][2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t two = __byte_perm(lds32(sst + soff[r] + cp * 512), 0, ssel);
+                if constexpr (F16) {
+                    const uint32_t sf = e4m3x2_to_f16x2(two);
+                    S[r][0] = __byte_perm(sf, sf, 0x1010);
+                    S[r][1] = __byte_perm(sf, sf, 0x3232);
+                } else {
+                    const uint32_t b0 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32(two & 0xFF), 0x1p119f));
+                    const uint32_t b1 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32((two >> 8) & 0xFF), 0x1p119f));
+                    S[r][0] = b0 | (b0 << 16);
+                    S[r][1] = b1 | (b1 << 16);
+                }
+                if constexpr (TAIL) {
+                    const int blk0 = 16 * i + 4 * cp + (t >> 1);
+                    if (blk0 >= nblocks32) S[r][0] = 0;
+                    if (blk0 + 2 >= nblocks32) S[r][1] = 0;
+                }
+            }
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t Pp[2][4];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if constexpr (F16) {
+                        e2m1x8_to_f16x2(wr[2 * ch + r], Pp[r]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) Pp[r][j] = hmul2(Pp[r][j], S[r][ch]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            Pp[r][j] = bmul2(place_byte_bf16x2((wr[2 * ch + r] >> (8 * j)) & 0xFFu), S[r][ch]);
+                    }
+                }
+                const uint4 xv = x_row ? lds128(xs + 64 * (2 * cp + ch)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t a[4] = {Pp[0][2 * e], Pp[1][2 * e], Pp[0][2 * e + 1], Pp[1][2 * e + 1]};
+                    mma16816<F16>(acc, a, e ? xv.z : xv.x, e ? xv.w : xv.y);
+                }
+            }
+        }
+    };
+
+    for (int i = 0; i < nst; ++i) {
+        const int st = i % n_stages;
+        if (mbar_wait(smem_u32(full + st), (i / n_stages) & 1, args.err, abort_flag, kErrGemvConsumer)) {
+            const uint32_t wst = smem_u32(sWst + st * kWBytes), sst = smem_u32(sSst + st * kSBytes);
+            const bool tail = 16 * (i + 1) > nblocks32;
+            if (use_f16) {
+                if (tail) consume(std::true_type{}, std::true_type{}, wst, sst, i);
+                else consume(std::true_type{}, std::false_type{}, wst, sst, i);
+            } else {
+                if (tail) consume(std::false_type{}, std::true_type{}, wst, sst, i);
+                else consume(std::false_type{}, std::false_type{}, wst, sst, i);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(empty + st));
+    }
+
+    // ---- epilogue: the bf16 path's products carry 2^-7 ----
+    if (*abort_flag) return;
+    const float gw = __fmul_rn(args.gW ? __ldg(args.gW) : 1.0f, use_f16 ? 1.0f : 0x1p7f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t m = 2 * t + (i & 1);
+        const int64_t n = (i < 2) ? row0 : row1;
+        if (m < M && n < N) {
+            const float v = __fmul_rn(acc[i], gw);
+            if (args.out_bf16) reinterpret_cast<uint16_t*>(args.y)[m * N + n] = f32_to_bf16_bits(v);
+            else reinterpret_cast<float*>(args.y)[m * N + n] = v;
+        }
+    }
+}
+
 }  // namespace nvf4
 
 // Consumer warps per CTA (16 rows each) for the nvfp4 GEMV: the choice in
@@ -695,6 +913,43 @@ bsq_status launch_nvf4_nt(int cw, const CUtensorMap& tm, const nvf4::Args& a, cu
     }
 }
 
+// The resident-x kernel when x and a ring of >= 6 stages fit (M <= 2 at K = 8192);
+// returns -1 (nothing launched) when they do not.
+template <int CW>
+int launch_nvf4_res_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+    constexpr int R = 16 * CW;
+    constexpr int64_t kStage = R * 128 + nvf4::kMaxRowBlocks * 2048;
+    // nst * 256 values per row (the K tail zero) + 64 bytes: == 64 mod 128, conflict-free B reads
+    const int64_t pitch = (a.K + 255) / 256 * 512 + 64;
+    const int64_t fixed = 1024 + a.M * pitch + 2 * nvf4::kResMaxStages * 8 + 16;
+    int64_t stages = (nvf4::kSmemLimit - fixed) / kStage;
+    if (stages > nvf4::kResMaxStages) stages = nvf4::kResMaxStages;
+    if (stages < 6) return -1;                               // a shallower ring starves the consumers
+    const size_t smem = (size_t)(fixed + stages * kStage);
+    auto kern = nvf4::gemv_nvf4_res_kernel<CW>;
+    static std::once_flag once[64];
+    static bool ok_dev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
+    std::call_once(once[dev], [&] {
+        ok_dev[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, nvf4::kSmemLimit) ==
+                      cudaSuccess;
+    });
+    if (!ok_dev[dev]) { (void)cudaGetLastError(); return -1; }
+    const dim3 grid((unsigned)((a.N + R - 1) / R));
+    kern<<<grid, (CW + 1) * 32, smem, s>>>(tm, a, (int)stages, (uint32_t)pitch);
+    return (int)launch_status();
+}
+
+int launch_nvf4_res(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+    switch (cw) {
+    case 12: return launch_nvf4_res_cfg<12>(tm, a, s);
+    case 8: return launch_nvf4_res_cfg<8>(tm, a, s);
+    case 6: return launch_nvf4_res_cfg<6>(tm, a, s);
+    default: return launch_nvf4_res_cfg<4>(tm, a, s);
+    }
+}
+
 bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t* W, const uint8_t* sW,
                        const float* gW, void* y, int out, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
     const int cw = nvf4_warps(N, info->num_sms);
@@ -713,7 +968,11 @@ bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t*
     a.x = x; a.sW = sW; a.gW = gW; a.y = y; a.err = info->err; a.M = M; a.N = N; a.K = K;
     a.cpd4 = pad_to(K / 16, 4) / 4;
     a.out_bf16 = out;
-    if (M <= 8) return launch_nvf4_nt<1>(cw, tm, a, s);
+    if (M <= 8) {
+        const int st = launch_nvf4_res(cw, tm, a, s);
+        if (st >= 0) return (bsq_status)st;
+        return launch_nvf4_nt<1>(cw, tm, a, s);
+    }
     if (M <= 16) return launch_nvf4_nt<2>(cw, tm, a, s);
     return launch_nvf4_nt<4>(cw, tm, a, s);
 }

@@ -28,8 +28,8 @@ def mx_operand(R, K, fmt_name, seed):
     return O.quantize_mx(x, MX[fmt_name])
 
 
-@pytest.mark.parametrize("M", [1, 5, 8, 13, 32])
-@pytest.mark.parametrize("N,K", [(256, 256), (300, 320), (129, 1024), (1, 64)])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 13, 32])
+@pytest.mark.parametrize("N,K", [(256, 256), (300, 320), (129, 1024), (1, 64), (200, 4160)])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 def test_gemv_nvfp4(bsq, M, N, K, out):
     x = S.normal_bf16((M, K), 1.0, 7 + M)
@@ -55,7 +55,7 @@ def test_gemv_nvfp4_every_code_and_subnormal_scales(bsq):
     check_products(y, want, s, "gemv_nvfp4 all codes")
 
 
-@pytest.mark.parametrize("M", [1, 8, 32])
+@pytest.mark.parametrize("M", [1, 2, 8, 32])
 def test_gemv_nvfp4_activations_outside_f16(bsq, M):
     """Activations that f16 cannot hold exactly (huge, tiny, bf16 subnormal) in
     some 256-wide K chunks and not in others: those chunks take the bf16 decode,
