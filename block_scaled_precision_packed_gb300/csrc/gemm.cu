@@ -289,8 +289,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             // Partial tile -> this CTA's shared memory (the operand ring is idle:
             // the single tile's last MMA has completed), then sum across the
             // cluster, each CTA finishing kBM/SPLIT rows.
-            const int64_t tile = tile_first;
-            const int64_t mb = tile % num_mb, nb = tile / num_mb;
             float* part = reinterpret_cast<float*>(smem);               // [kBM][BN + 4] fp32
             constexpr int kPitch = BN + 4;
             const bool have = mbar_wait(smem_u32(acc_full), 0, args.err, abort_flag, kErrGemmEpilogue);

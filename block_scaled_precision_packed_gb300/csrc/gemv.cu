@@ -4,24 +4,28 @@
 // one-row product, N spread across CTAs, the accumulator held in registers
 // for the whole K walk and drained once).
 //
-// Design (sm_103a):
-//  * A CTA owns 128 weight rows (8 warps x 16 rows) and walks all of K.
-//  * The weight is dequantized in registers, never staged: each thread loads
-//    its rows' packed bytes straight from global memory (16-byte loads,
-//    prefetched a 256-element chunk ahead) and turns them into bf16 pairs.
-//  * Products run on the tensor cores as mma.sync m16n8k16 bf16 -> f32, weight
-//    rows as the A operand (16 rows), activation rows as B (8 per n-tile).
-//  * Exact decode: a code's bits are "placed" into a bf16 (its exponent and
-//    mantissa fields dropped into the low bf16 fields and its sign into the
-//    sign bit), which is the code's value times a fixed power of two (bf16
-//    subnormals included).  One bf16x2 multiply by (block scale * 2^c) then
-//    yields value*scale*2^c' exactly: every e2m1*ue4m3 and fp6*2^k product
-//    fits bf16's 8-bit significand.  The fixed power is undone in fp32 at the
-//    end.  No rounding happens before the tensor-core accumulate.
-//  * K inside a 32-element thread range is permuted consistently for both
-//    operands (pairs (j, j+4) of each 8-code group share a bf16x2 register);
-//    the activation chunk is staged in shared memory in that order with a
-//    bank-conflict-free layout.
+// Two kernels (sm_103a):
+//  * nvfp4 (gemv_nvf4_kernel, gemv_nvf4_res_kernel, below): the weight
+//    streams through a TMA ring in shared memory and is decoded with the
+//    hardware e2m1 -> f16 conversion; see the comment at its namespace.
+//  * MX formats (gemv_kernel, here): a CTA owns 128 weight rows (8 warps x 16
+//    rows) and walks all of K; the weight is dequantized in registers, never
+//    staged: each thread loads its rows' packed bytes straight from global
+//    memory (16-byte loads, prefetched a 256-element chunk ahead) and turns
+//    them into bf16 pairs.  Products run on the tensor cores as mma.sync
+//    m16n8k16 bf16 -> f32, weight rows as the A operand (16 rows), activation
+//    rows as B (8 per n-tile).
+//  * Exact decode ("placed" bf16): a code's bits are dropped into the low
+//    bf16 exponent/mantissa fields and its sign into the sign bit, which is
+//    the code's value times a fixed power of two (bf16 subnormals included).
+//    One bf16x2 multiply by (block scale * 2^c) then yields value*scale*2^c'
+//    exactly: every fp6*2^k and e2m1*ue4m3 product fits bf16's 8-bit
+//    significand.  The fixed power is undone in fp32 at the end.  No rounding
+//    happens before the tensor-core accumulate.
+//  * In the MX kernel K inside a 32-element thread range is permuted
+//    consistently for both operands (pairs (j, j+4) of each 8-code group share
+//    a bf16x2 register); the activation chunk is staged in shared memory in
+//    that order with a bank-conflict-free layout.
 #include <climits>
 #include <mutex>
 #include <type_traits>
@@ -39,9 +43,6 @@ constexpr int kPitch = kChunk / 8 + 4;   // 16-byte units per staged x row (== 4
 
 template <int WFMT>
 struct WTraits;
-// nvfp4: 4-bit codes, 16 per block, 32 codes of a thread = 16 bytes.
-template <>
-struct WTraits<kNvfp4> { static constexpr int kRegs = 4; static constexpr int kBlock = 16; };
 template <>
 struct WTraits<kE3M2> { static constexpr int kRegs = 6; static constexpr int kBlock = 32; };
 template <>
@@ -65,11 +66,7 @@ __device__ __forceinline__ void load_row(RowRaw<WFMT>& rr, const uint8_t* __rest
         rr.s = 0;
         return;
     }
-    if constexpr (WFMT == kNvfp4) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(W + row * (K / 2) + k / 2));
-        rr.w[0] = v.x; rr.w[1] = v.y; rr.w[2] = v.z; rr.w[3] = v.w;
-        rr.s = __ldg(reinterpret_cast<const uint16_t*>(sW + swz_offset(row, k / 16, cpd4)));
-    } else if constexpr (WFMT == kE4M3) {
+    if constexpr (WFMT == kE4M3) {
         const uint4* p = reinterpret_cast<const uint4*>(W + row * K + k);
         const uint4 a = __ldg(p), b = __ldg(p + 1);
         rr.w[0] = a.x; rr.w[1] = a.y; rr.w[2] = a.z; rr.w[3] = a.w;
@@ -89,11 +86,10 @@ __device__ __forceinline__ uint32_t fp6_to_containers(uint32_t bits24) {
 }
 
 // Place two codes (code A in bits 0..7 of u, code B in bits 16..23) into a
-// bf16x2: value(code) * 2^-P with P = 126 (e2m1, e2m3), 124 (e3m2), 120 (e4m3).
+// bf16x2: value(code) * 2^-P with P = 126 (e2m3), 124 (e3m2), 120 (e4m3).
 template <int WFMT>
 __device__ __forceinline__ uint32_t place_pair(uint32_t u) {
-    if constexpr (WFMT == kNvfp4) return ((u << 6) & 0x01C001C0u) | ((u << 12) & 0x80008000u);
-    else if constexpr (WFMT == kE3M2) return ((u << 5) & 0x03E003E0u) | ((u << 10) & 0x80008000u);
+    if constexpr (WFMT == kE3M2) return ((u << 5) & 0x03E003E0u) | ((u << 10) & 0x80008000u);
     else if constexpr (WFMT == kE2M3) return ((u << 4) & 0x01F001F0u) | ((u << 10) & 0x80008000u);
     else return ((u << 4) & 0x07F007F0u) | ((u << 8) & 0x80008000u);
 }
@@ -104,17 +100,11 @@ __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
     return r;
 }
 
-// bf16x2 scale multiplier for one block: nvfp4 -> s * 2^119 (so the product is
-// value*s*2^-7); MX -> 2^(ue-11) (product value*2^(ue-127)*2^(116-P)).
+// bf16x2 scale multiplier for one MX block: 2^(ue-11), so the product is
+// value*2^(ue-127)*2^(116-P).
 template <int WFMT>
 __device__ __forceinline__ uint32_t scale_mult(uint32_t code) {
-    uint32_t b;
-    if constexpr (WFMT == kNvfp4) {
-        const float f = __fmul_rn(e4m3_to_f32(code & 0xFF), 0x1p119f);
-        b = f32_to_bf16_bits(f);   // exact: at most 4 significant bits
-    } else {
-        b = ((code & 0xFF) + 116u) << 7;
-    }
+    const uint32_t b = ((code & 0xFF) + 116u) << 7;
     return b | (b << 16);
 }
 
@@ -122,13 +112,7 @@ __device__ __forceinline__ uint32_t scale_mult(uint32_t code) {
 // P[q][j] holds codes (8q+j, 8q+j+4) of its 32-code range, scaled.
 template <int WFMT>
 __device__ __forceinline__ void decode_row(const RowRaw<WFMT>& rr, uint32_t (&P)[4][4]) {
-    if constexpr (WFMT == kNvfp4) {
-        const uint32_t s0 = scale_mult<kNvfp4>(rr.s & 0xFF), s1 = scale_mult<kNvfp4>(rr.s >> 8);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) P[q][j] = bmul2(place_pair<kNvfp4>(rr.w[q] >> (4 * j)), q < 2 ? s0 : s1);
-    } else {
+    {
         const uint32_t sm = scale_mult<WFMT>(rr.s);
         uint32_t C[8];   // byte containers of the 32 codes, 4 per word
         if constexpr (WFMT == kE4M3) {
@@ -255,7 +239,7 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
     }
 
     // ---- epilogue: undo the fixed power of two, apply gW, store y[m, n] ----
-    constexpr float kLift = WFMT == kNvfp4 ? 0x1p7f : WFMT == kE3M2 ? 0x1p8f : WFMT == kE2M3 ? 0x1p10f : 0x1p4f;
+    constexpr float kLift = WFMT == kE3M2 ? 0x1p8f : WFMT == kE2M3 ? 0x1p10f : 0x1p4f;
     const float f = __fmul_rn(kLift, gW ? __ldg(gW) : 1.0f);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -305,11 +289,6 @@ constexpr int kPitch = 36;          // 16-byte units per staged x row (32 used; 
 constexpr int kMaxRowBlocks = 3;    // 128-row scale blocks one tile can touch (R <= 256)
 constexpr int kSmemLimit = 232448;  // opt-in shared memory per CTA
 
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-    uint32_t r;
-    asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
-    return r;
-}
 // the four code pairs (bytes) of a word -> four f16x2
 __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
     asm("{ .reg .b8 b0, b1, b2, b3;\n"
