@@ -248,6 +248,22 @@ class Workload:
             fn(stream)
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time (every rank gets it): replicas report the
+    whole job's throughput over the time of the last one to finish."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step, world, ms):
+    """Whole-job throughput: every rank runs its own replica of the step."""
+    return units_per_step * world / (ms / 1e3)
+
+
 def run_bsq(args, rank, world, dev_index):
     import torch
     from block_scaled_precision_packed_gb300 import bsq
@@ -332,13 +348,9 @@ def run_bsq(args, rank, world, dev_index):
     launches = launches_per_step * args.steps
     if dist:
         dist.barrier()
-    step_ms = float(step_ms_all.mean())
-    if dist:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(float(step_ms_all.mean()), dist, dev)
     unit, per_step = wl.units
-    value = per_step * world / (step_ms / 1e3)
+    value = job_throughput(per_step, world, step_ms)
 
     # dominant op and its roofline
     mean_op = op_ms.mean(axis=0)
@@ -376,12 +388,8 @@ def run_bsq(args, rank, world, dev_index):
                 if i >= args.warmup:
                     e_ev[i - args.warmup][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(per_step * world / (e_ms / 1e3), 3), "unit": unit, "ms_per_step": round(e_ms, 4),
+        e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in e_ev])), dist, dev)
+        e2e = {"value": round(job_throughput(per_step, world, e_ms), 3), "unit": unit, "ms_per_step": round(e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     return dict(value=value, unit=unit, step_ms=step_ms, roofline=roof, per_op_us=per_op, e2e=e2e,
                 launches=launches, clocks=clk.summary(), wl=wl)
