@@ -144,6 +144,12 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ------------------------------------------------------- per-block encode ----
+// (lo * k, hi * k) in one packed fp32 multiply (two IEEE RN products).
+__device__ __forceinline__ void mul2_rn(float lo, float hi, float k, float& r_lo, float& r_hi) {
+    asm("{ .reg .b64 a, b, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %4}; mul.rn.f32x2 d, a, b; mov.b64 {%0, %1}, d; }"
+        : "=f"(r_lo), "=f"(r_hi) : "f"(lo), "f"(hi), "f"(k));
+}
+
 // Largest |bf16| magnitude bits among the 32 values of one 64-byte unit.
 __device__ __forceinline__ uint32_t absmax32_bits(const uint4 (&v)[4]) {
     const uint32_t m = 0x7FFF7FFFu;
@@ -183,7 +189,9 @@ __device__ __forceinline__ void mx_encode_words(const uint4 (&v)[4], float inv, 
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const uint32_t x2 = (&v[i >> 2].x)[i & 3];
-        p[i] = cvt_x2<FMT>(__fmul_rn(bf16_lo(x2), inv), __fmul_rn(bf16_hi(x2), inv));
+        float lo, hi;
+        mul2_rn(bf16_lo(x2), bf16_hi(x2), inv, lo, hi);
+        p[i] = cvt_x2<FMT>(lo, hi);
     }
     if constexpr (FMT == kE4M3) {
 #pragma unroll
@@ -229,14 +237,16 @@ __device__ __forceinline__ void nvfp4_encode_block(uint4 v0, uint4 v1, uint32_t 
     sc = cvt_x2<kE4M3>(__fdiv_rn(t, kMaxE2M1), 0.0f) & 0xFFu;
     if (sc == 0) return;
     const float inv = __fdiv_rn(gs, e4m3_to_f32(sc));
-    w0 = cvt_e2m1x2(__fmul_rn(bf16_lo(v0.x), inv), __fmul_rn(bf16_hi(v0.x), inv)) |
-         (cvt_e2m1x2(__fmul_rn(bf16_lo(v0.y), inv), __fmul_rn(bf16_hi(v0.y), inv)) << 8) |
-         (cvt_e2m1x2(__fmul_rn(bf16_lo(v0.z), inv), __fmul_rn(bf16_hi(v0.z), inv)) << 16) |
-         (cvt_e2m1x2(__fmul_rn(bf16_lo(v0.w), inv), __fmul_rn(bf16_hi(v0.w), inv)) << 24);
-    w1 = cvt_e2m1x2(__fmul_rn(bf16_lo(v1.x), inv), __fmul_rn(bf16_hi(v1.x), inv)) |
-         (cvt_e2m1x2(__fmul_rn(bf16_lo(v1.y), inv), __fmul_rn(bf16_hi(v1.y), inv)) << 8) |
-         (cvt_e2m1x2(__fmul_rn(bf16_lo(v1.z), inv), __fmul_rn(bf16_hi(v1.z), inv)) << 16) |
-         (cvt_e2m1x2(__fmul_rn(bf16_lo(v1.w), inv), __fmul_rn(bf16_hi(v1.w), inv)) << 24);
+    const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float lo, hi;
+        mul2_rn(bf16_lo(in[i]), bf16_hi(in[i]), inv, lo, hi);
+        c[i] = cvt_e2m1x2(lo, hi);
+    }
+    w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+    w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
 }
 
 // ------------------------------------------------------------------ MX ----
@@ -427,6 +437,10 @@ __device__ __forceinline__ void st_release_u64(uint32_t* p, uint64_t v) {
 __device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -461,7 +475,11 @@ __device__ __forceinline__ void load_unit(uint32_t addr, uint32_t u, uint4 (&v)[
     for (int k = 0; k < 4; ++k) v[k] = r2 ? t[(k + 2) & 3] : t[k];              // v[k] = piece k
 }
 
-template <int FMT>   // kE3M2 / kE2M3 / kE4M3, or kNvfp4
+// TRANSPOSE (every row a whole number of 4-slot groups, so slot and 64-byte
+// unit offsets coincide): step 2 also rewrites each warp's 32 units piece-major
+// (unit u's piece j at (u/32)*2048 + j*512 + (u%32)*16), so step 3 reads its
+// pieces in order, conflict-free, with no un-rotation.
+template <int FMT, bool TRANSPOSE>   // FMT: kE3M2 / kE2M3 / kE4M3, or kNvfp4
 __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __grid_constant__ OnePassArgs args) {
     extern __shared__ __align__(128) uint8_t slice[];
     __shared__ uint64_t bar[kMaxChunks];
@@ -539,18 +557,30 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
             }
             bm[it] = 0;
             const uint32_t s = s_t + it * kOneThreads;
-            if (s < s1 && r < a.M && b < units_row) {
-                const uint32_t u = (uint32_t)(r * units_row + b - f0);
-                const uint32_t addr = slice_addr + 64 * u, rot = (u >> 1) & 3;
+            const bool have = s < s1 && r < a.M && b < units_row;
+            const uint32_t u = have ? (uint32_t)(r * units_row + b - f0) : 0u;
+            const uint32_t rot = (u >> 1) & 3;
+            uint4 pv[4];
+            if (have) {
+                const uint32_t addr = slice_addr + 64 * u;
                 uint32_t mb[2] = {0, 0};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {          // rotated piece order: conflict-free
                     const uint32_t pc = (j + rot) & 3;
-                    const uint32_t x8 = absmax8_bits(lds128(addr + 16 * pc));
+                    pv[j] = lds128(addr + 16 * pc);
+                    const uint32_t x8 = absmax8_bits(pv[j]);
                     if (pc < 2) mb[0] = max(mb[0], x8); else mb[1] = max(mb[1], x8);
                 }
                 bm[it] = FMT == kNvfp4 ? (mb[0] | (mb[1] << 16)) : max(mb[0], mb[1]);
                 m = max(m, max(mb[0], mb[1]));
+            }
+            if constexpr (TRANSPOSE) {
+                __syncwarp();                          // the warp's 32 units are read
+                if (have) {
+                    const uint32_t gbase = slice_addr + (u >> 5) * 2048 + (u & 31) * 16;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sts128(gbase + ((j + rot) & 3) * 512, pv[j]);
+                }
             }
             b += db;
             r += dr;
@@ -616,7 +646,13 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
         uint4 v[4];
         if (valid) {
             const uint32_t u = (uint32_t)(r * units_row + b - f0);
-            load_unit(slice_addr + 64 * u, u, v);
+            if constexpr (TRANSPOSE) {
+                const uint32_t gbase = slice_addr + (u >> 5) * 2048 + (u & 31) * 16;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = lds128(gbase + j * 512);
+            } else {
+                load_unit(slice_addr + 64 * u, u, v);
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = make_uint4(0, 0, 0, 0);
@@ -725,9 +761,11 @@ bool onepass_batch(const DeviceInfo* info, const QTensor* ts, int n, uint32_t* w
     if ((size_t)(kCtlWord + 4) * sizeof(uint32_t) > ws_bytes || G + 1 > kCtlWord) return false;
     int64_t slots[kMaxBatch], spr[kMaxBatch];
     int cnt[kMaxBatch];
+    bool transpose = true;                 // every row a whole number of 4-slot groups
     for (int i = 0; i < n; ++i) {
         if (ts[i].K % 32 != 0) return false;
         spr[i] = FMT == kNvfp4 ? pad_to(ts[i].K / 16, 4) / 2 : pad_to(ts[i].K / 32, 4);
+        transpose = transpose && spr[i] == ts[i].K / 32;
         slots[i] = pad_to(ts[i].M, 128) * spr[i];
         if (slots[i] >= (int64_t(1) << 31)) return false;
         cnt[i] = 1;
@@ -756,13 +794,19 @@ bool onepass_batch(const DeviceInfo* info, const QTensor* ts, int n, uint32_t* w
     for (int i = n; i <= kMaxBatch; ++i) a.first_cta[i] = first;
     for (int i = n; i < kMaxBatch; ++i) a.t[i] = a.t[0];
     a.n = n; a.ws = ws; a.err = info->err;
-    const size_t smem = (size_t)(per_max * 64);
+    // the piece-major rewrite works on whole 32-unit groups
+    const size_t smem = (size_t)(transpose ? pad_to(per_max * 64, 2048) : per_max * 64);
+    if ((int64_t)smem > slice_max) return false;
     static std::once_flag once[64];
     static bool ok_dev[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     std::call_once(once[dev], [&] {
-        ok_dev[dev] = cudaFuncSetAttribute(quant_onepass_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        ok_dev[dev] = cudaFuncSetAttribute(quant_onepass_kernel<FMT, false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           info->max_smem_optin - 1024) == cudaSuccess &&
+                      cudaFuncSetAttribute(quant_onepass_kernel<FMT, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            info->max_smem_optin - 1024) == cudaSuccess;
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return false; }
@@ -776,7 +820,8 @@ bool onepass_batch(const DeviceInfo* info, const QTensor* ts, int n, uint32_t* w
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, quant_onepass_kernel<FMT>, a);
+    const cudaError_t e = transpose ? cudaLaunchKernelEx(&cfg, quant_onepass_kernel<FMT, true>, a)
+                                    : cudaLaunchKernelEx(&cfg, quant_onepass_kernel<FMT, false>, a);
     if (e != cudaSuccess) { (void)cudaGetLastError(); *st = BSQ_ERR_CUDA; return true; }
     count_launch(FMT == kNvfp4 ? BSQ_KERNEL_QUANT_NVFP4 : BSQ_KERNEL_QUANT_MX);
     *st = BSQ_OK;
