@@ -210,6 +210,28 @@ __device__ __forceinline__ void tc_mma_mxf4nvf4(uint32_t d, uint64_t adesc, uint
                  :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// Registers r[0..N) -> TMEM columns [col, col + N) of the warp's 32 lanes
+// (lane l of the warp writes its own TMEM lane); N a multiple of 4.
+template <int N>
+__device__ __forceinline__ void tc_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N % 4 == 0, "columns in groups of four");
+    if constexpr (N % 16 == 0) {
+#pragma unroll
+        for (int c = 0; c < N; c += 16)
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                         :: "r"(taddr + c), "r"(r[c]), "r"(r[c + 1]), "r"(r[c + 2]), "r"(r[c + 3]), "r"(r[c + 4]),
+                            "r"(r[c + 5]), "r"(r[c + 6]), "r"(r[c + 7]), "r"(r[c + 8]), "r"(r[c + 9]),
+                            "r"(r[c + 10]), "r"(r[c + 11]), "r"(r[c + 12]), "r"(r[c + 13]), "r"(r[c + 14]),
+                            "r"(r[c + 15]) : "memory");
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 4)
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
+                         :: "r"(taddr + c), "r"(r[c]), "r"(r[c + 1]), "r"(r[c + 2]), "r"(r[c + 3]) : "memory");
+    }
+}
 
 // 32 lanes x 32 columns of 32-bit words: thread i of the warp gets its lane's
 // 32 consecutive columns.

@@ -14,16 +14,23 @@
 //          (CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B), counting the 96 packed
 //          bytes of a 128-code row toward the stage's transaction.
 //
-// One persistent CTA per SM, warp-specialised (320 threads):
+// One persistent CTA per SM, warp-specialised (448 threads):
 //   warp 0      TMA producer: A / W tiles (128-byte swizzle) and the scale
 //               atoms (plain bulk copies) into an S-stage shared-memory ring.
-//   warp 1      owns the TMEM allocation; one lane issues tcgen05.cp (scale
-//               atoms -> TMEM) and tcgen05.mma, and commits each stage back to
-//               the producer and each finished tile to the epilogue.
+//   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma and
+//               commits each stage back to the producer and each finished
+//               tile to the epilogue.
 //   warps 2-9   epilogue (two warps per TMEM lane quarter, one per column
 //               half): tcgen05.ld the 128 x BN fp32 accumulator, scale by
 //               gA*gW, convert; for bf16 output the whole tile is held in
 //               registers so TMEM is released before the stores start.
+//   warps 10-13 scale factors: one warp per TMEM lane quarter moves each
+//               landed stage's scale atoms from shared memory into the
+//               stage's TMEM scale columns with tcgen05.st (every quarter gets
+//               the same 32 x 16-byte rows, the replicated layout the
+//               block-scaled MMA reads), then releases the stage to the MMA
+//               warp.  A tcgen05.cp of an atom occupies the tensor pipe for
+//               about as long as a 128x256 MMA; these stores do not.
 // Every wait is bounded (2 s); a timeout records its site in the device error
 // word, drains the copies in flight, frees TMEM and returns.
 //
@@ -40,7 +47,8 @@ namespace bsq {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kThreads = 320;     // producer warp, MMA warp, 8 epilogue warps
+constexpr int kThreads = 448;     // producer warp, MMA warp, 8 epilogue warps, 4 scale-factor warps
+constexpr int kSfWarp0 = 10;      // first scale-factor warp
 constexpr int kEpiThreads = 256;
 constexpr int kAtom = 512;          // bytes of one 128-row x 4-block scale atom
 constexpr uint32_t kTmemCols = 512;
@@ -92,12 +100,17 @@ __device__ __forceinline__ void cluster_sync() {
 // prologue; this kernel waits for the previous one's results before reading them.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t local_addr, uint32_t rank) {
+// The shared::cluster address of `local_addr` in the CTA of cluster rank `rank`
+// (a CTA's window is contiguous, so offsets add to the mapped base).
+__device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank) {
     uint32_t remote;
-    float4 v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    return remote;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
+    float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote));
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(cluster_addr));
     return v;
 }
 
@@ -124,6 +137,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint64_t* drain = acc_full + 2;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(acc_full + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
+    uint64_t* sf_full = acc_full + 4;                 // [kStages]: the stage's scales are in TMEM
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t M = args.M, N = args.N, K = args.K;
@@ -141,6 +155,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(smem_u32(full + s), 1);
             mbar_init(smem_u32(empty + s), 1);
         }
+        for (int s = 0; s < C::kStages; ++s) mbar_init(smem_u32(sf_full + s), 128);
         mbar_init(smem_u32(acc_full), 1);
         mbar_init(smem_u32(acc_empty), kEpiThreads);
         mbar_init(smem_u32(drain), 1);
@@ -211,13 +226,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else if (warp == 1) {
         if (lane == 0) {
             // --------------------------------------------------- MMA issue --
-            // Descriptors of stage 0's tiles and scale atoms; a stage, atom or
-            // K step is an offset in the 16-byte-unit address field (smem < 256 KB),
-            // so the single issuing thread spends one add per tcgen05 instruction.
+            // Descriptors of stage 0's tiles; a stage or K step is an offset in
+            // the 16-byte-unit address field (smem < 256 KB), so the single
+            // issuing thread spends one add per tcgen05 instruction.
             const uint64_t dA0 = smem_desc(smem_u32(sA_st), 16, 1024, 2);
             const uint64_t dB0 = smem_desc(smem_u32(sB_st), 16, 1024, 2);
-            const uint64_t dSA0 = smem_desc(smem_u32(sSfa), 0, 128, 0);
-            const uint64_t dSB0 = smem_desc(smem_u32(sSfb), 0, 128, 0);
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -225,33 +238,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 if (!mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, args.err, abort_flag, kErrGemmMma)) break;
                 tc_fence_after();
                 for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
-                    if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
+                    // the stage's operands have landed and its scales are in TMEM
+                    if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma) ||
+                        !mbar_wait(smem_u32(sf_full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sf_col = (uint32_t)(BN + stage * C::kSfColsPerStage);
-                    const uint64_t sa = dSA0 + (uint64_t)(stage * (C::kSfaBytes >> 4));
-                    const uint64_t sb = dSB0 + (uint64_t)(stage * (C::kSfbBytes >> 4));
-                    // scale atoms -> TMEM (4 columns each, replicated to all lane quarters)
-                    auto copy_atom = [&](int a) {
-                        tc_cp_scales(tmem + sf_col + 4 * a, sa + (uint64_t)(a * (kAtom >> 4)));
-#pragma unroll
-                        for (int rt = 0; rt < C::kRowTilesB; ++rt)
-                            tc_cp_scales(tmem + sf_col + C::kSfaCols + (a * C::kRowTilesB + rt) * 4,
-                                         sb + (uint64_t)((rt * C::kAtomsPerStage + a) * (kAtom >> 4)));
-                    };
                     const uint64_t a_st = dA0 + (uint64_t)(stage * (C::kABytes >> 4));
                     const uint64_t b_st = dB0 + (uint64_t)(stage * (C::kBBytes >> 4));
                     const int n_mma = NVF4 ? (int)imin64(4, (K - ks * C::kStageK) / 64) : 4;
-                    // MX: the stage's one atom per operand serves all 4 K steps
-                    if constexpr (!NVF4) copy_atom(0);
+                    // MX: the stage's one atom per operand serves all 4 K steps;
+                    // nvfp4: K step kk reads atom kk
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         if (kk >= n_mma) break;
-                        // nvfp4: each K step's own atoms right before its MMA, so the
-                        // next step's copies run while this MMA executes
-                        if constexpr (NVF4) copy_atom(kk);
                         const uint64_t ad = a_st + (uint64_t)(2 * kk);          // +32 bytes per K step
                         const uint64_t bd = b_st + (uint64_t)(2 * kk);
                         const uint32_t acc = (ks > ks_begin || kk > 0) ? 1u : 0u;
@@ -275,6 +277,44 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(smem_u32(drain), 0)) {
                 if (globaltimer() - t0 > kWaitLimitNs) { atomicCAS(args.err, 0u, (uint32_t)kErrGemmDrain); break; }
+            }
+        }
+    } else if (warp >= kSfWarp0) {
+        // -------------------------------------------------- scale factors --
+        // Lane l of the warp for lane quarter q writes TMEM lane 32q + l: row l
+        // (16 bytes = 4 columns) of every atom of the stage.
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t tile = tile_first; tile < num_tiles && ok; tile += tile_step) {
+            for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
+                if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sf_col = (uint32_t)(BN + stage * C::kSfColsPerStage);
+                const uint8_t* sa = sSfa + stage * C::kSfaBytes + 16 * lane;
+                const uint8_t* sb = sSfb + stage * C::kSfbBytes + 16 * lane;
+                uint32_t ra[4 * C::kAtomsPerStage];
+                uint32_t rb[4 * C::kAtomsPerStage * C::kRowTilesB];
+#pragma unroll
+                for (int a = 0; a < C::kAtomsPerStage; ++a) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(sa + a * kAtom);
+                    ra[4 * a] = v.x; ra[4 * a + 1] = v.y; ra[4 * a + 2] = v.z; ra[4 * a + 3] = v.w;
+#pragma unroll
+                    for (int rt = 0; rt < C::kRowTilesB; ++rt) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(sb + (rt * C::kAtomsPerStage + a) * kAtom);
+                        const int j = 4 * (a * C::kRowTilesB + rt);
+                        rb[j] = w.x; rb[j + 1] = w.y; rb[j + 2] = w.z; rb[j + 3] = w.w;
+                    }
+                }
+                tc_st_cols(lane_base + sf_col, ra);
+                tc_st_cols(lane_base + sf_col + C::kSfaCols, rb);
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(sf_full + stage));
+                if (++stage == C::kStages) { stage = 0; phase ^= 1; }
             }
         }
     } else {
@@ -408,17 +448,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         constexpr int kPitch = BN + 4;
         constexpr int kRows = kBM / SPLIT;
         const float f = __fmul_rn(args.gA ? __ldg(args.gA) : 1.0f, args.gW ? __ldg(args.gW) : 1.0f);
-        const uint32_t part = smem_u32(smem);
-        for (int it = threadIdx.x; it < kRows * (BN / 4); it += kThreads) {
+        // Each thread owns up to kPer float4 groups of this rank's rows; every
+        // rank's copy of all of them is requested before the first sum, so the
+        // distributed-shared-memory latency is paid once.
+        constexpr int kItems = kRows * (BN / 4);
+        constexpr int kPer = (kItems + kThreads - 1) / kThreads;
+        uint32_t base[SPLIT];
+#pragma unroll
+        for (int rk = 0; rk < SPLIT; ++rk) base[rk] = map_rank(smem_u32(smem), (uint32_t)rk);
+        float4 v[kPer][SPLIT];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int it = (int)threadIdx.x + j * kThreads;
+            if (it >= kItems) break;
             const int lr = (int)krank * kRows + it / (BN / 4), cg = it % (BN / 4);
             const uint32_t off = (uint32_t)((lr * kPitch + 4 * cg) * 4);
-            float4 v[SPLIT];
 #pragma unroll
-            for (int rk = 0; rk < SPLIT; ++rk) v[rk] = ld_dsmem_f4(part + off, rk);   // all in flight at once
-            float4 acc = v[0];
+            for (int rk = 0; rk < SPLIT; ++rk) v[j][rk] = ld_cluster_f4(base[rk] + off);
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int it = (int)threadIdx.x + j * kThreads;
+            if (it >= kItems) break;
+            const int lr = (int)krank * kRows + it / (BN / 4), cg = it % (BN / 4);
+            float4 acc = v[j][0];                          // rank order: deterministic
 #pragma unroll
             for (int rk = 1; rk < SPLIT; ++rk) {
-                acc.x += v[rk].x; acc.y += v[rk].y; acc.z += v[rk].z; acc.w += v[rk].w;
+                acc.x += v[j][rk].x; acc.y += v[j][rk].y; acc.z += v[j][rk].z; acc.w += v[j][rk].w;
             }
             const int64_t row = mb * kBM + lr, col = nb * BN + 4 * cg;
             if (row >= M || col >= N) continue;
