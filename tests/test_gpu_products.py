@@ -29,7 +29,7 @@ def mx_operand(R, K, fmt_name, seed):
 
 
 @pytest.mark.parametrize("M", [1, 2, 5, 8, 13, 32])
-@pytest.mark.parametrize("N,K", [(256, 256), (300, 320), (129, 1024), (1, 64), (200, 4160)])
+@pytest.mark.parametrize("N,K", [(256, 256), (300, 320), (129, 1024), (1, 64), (200, 4160), (1000, 2048)])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 def test_gemv_nvfp4(bsq, M, N, K, out):
     x = S.normal_bf16((M, K), 1.0, 7 + M)
