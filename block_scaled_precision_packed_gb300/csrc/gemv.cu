@@ -635,6 +635,16 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
 // else raw bf16) and stays in shared memory for the whole K walk, so the
 // stage loop has no x staging and no consumer-wide barrier.  The ring depth is
 // whatever the rest of shared memory holds (6..8 stages).
+//
+// SLOT (M = 1, f16 path): the block scale leaves the decode.  With one
+// activation row, seven of the MMA's eight B columns would be zero, so column j
+// instead carries x only for the K positions of blocks b with b % 8 == j (the
+// lane holding a column's fragment loads x or zero).  After every eight blocks
+// the fp32 tile holds, per weight row, the eight block partial sums
+// sum_k w[n, k] x[k] of unscaled e2m1 values; each is multiplied by its ue4m3
+// scale (decoded exactly to fp32 from its bits) and added to the row's
+// accumulators.  The per-pair f16 scale multiply and the per-chunk scale
+// conversions drop out of the stage loop.
 constexpr int kResMaxStages = 8;
 
 // both halves of a bf16x2 word zero or f16 normals (bf16 exponent field 113..142)
@@ -653,7 +663,13 @@ __device__ __forceinline__ bool bar_and(int id, int nthreads, bool ok) {
     return r != 0;
 }
 
-template <int CW>
+// ue4m3 byte -> fp32, exact: its 7 bits placed as an fp32 exponent/mantissa
+// (normal or subnormal) are the value times 2^-120.
+__device__ __forceinline__ float ue4m3_bits_to_f32(uint32_t b) {
+    return __fmul_rn(__uint_as_float((b & 0x7Fu) << 20), 0x1p120f);
+}
+
+template <int CW, bool SLOT>
 __global__ void __launch_bounds__((CW + 1) * 32, 1)
 gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, int n_stages, uint32_t x_pitch) {
     constexpr int R = 16 * CW;
@@ -816,12 +832,61 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, i
         }
     };
 
+    // SLOT: per-row block partial sums (columns 2t, 2t+1 of rows g, g+8), scaled
+    float acc_s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const uint32_t xrow0 = smem_u32(sX) + 16 * t;                       // x row 0
+    auto consume_slot = [&](auto tail_tag, uint32_t wst, uint32_t sst, int i) {
+        constexpr bool TAIL = decltype(tail_tag)::value;
+        const uint32_t xs = xrow0 + (uint32_t)i * 512;
+#pragma unroll
+        for (int G = 0; G < 2; ++G) {                                   // blocks 8G .. 8G+7 of the stage
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int cq = 0; cq < 2; ++cq) {
+                const int cp = 2 * G + cq;
+                uint32_t wr[4];
+                ldmatrix_x4(wst + mrow * 128 + (((2 * cp + mcol) ^ (mrow & 7)) << 4), wr);
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int chunk = 2 * cp + ch;                      // 32 codes: blocks 2chunk, 2chunk+1
+                    uint32_t Pp[2][4];
+                    e2m1x8_to_f16x2(wr[2 * ch], Pp[0]);
+                    e2m1x8_to_f16x2(wr[2 * ch + 1], Pp[1]);
+                    // this lane's codes 8t..8t+7 lie in block 2chunk + (t >> 1): column (that block) % 8
+                    const bool mine = g == ((2 * chunk + (t >> 1)) & 7);
+                    const uint4 xv = mine ? lds128(xs + 64 * chunk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint32_t a[4] = {Pp[0][2 * e], Pp[1][2 * e], Pp[0][2 * e + 1], Pp[1][2 * e + 1]};
+                        mma16816<true>(d, a, e ? xv.z : xv.x, e ? xv.w : xv.y);
+                    }
+                }
+            }
+            // columns 2t, 2t+1 of this group are blocks 8G + 2t + {0, 1}
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t two = lds32(sst + soff[r] + (2 * G + (t >> 1)) * 512) >> (16 * (t & 1));
+                float s0 = ue4m3_bits_to_f32(two & 0xFFu), s1 = ue4m3_bits_to_f32((two >> 8) & 0xFFu);
+                if constexpr (TAIL) {
+                    const int blk0 = 16 * i + 8 * G + 2 * t;
+                    if (blk0 >= nblocks32) s0 = 0.0f;
+                    if (blk0 + 1 >= nblocks32) s1 = 0.0f;
+                }
+                acc_s[2 * r] = __fmaf_rn(s0, d[2 * r], acc_s[2 * r]);
+                acc_s[2 * r + 1] = __fmaf_rn(s1, d[2 * r + 1], acc_s[2 * r + 1]);
+            }
+        }
+    };
+
     for (int i = 0; i < nst; ++i) {
         const int st = i % n_stages;
         if (mbar_wait(smem_u32(full + st), (i / n_stages) & 1, args.err, abort_flag, kErrGemvConsumer)) {
             const uint32_t wst = smem_u32(sWst + st * kWBytes), sst = smem_u32(sSst + st * kSBytes);
             const bool tail = 16 * (i + 1) > nblocks32;
-            if (use_f16) {
+            if (SLOT && use_f16) {
+                if (tail) consume_slot(std::true_type{}, wst, sst, i);
+                else consume_slot(std::false_type{}, wst, sst, i);
+            } else if (use_f16) {
                 if (tail) consume(std::true_type{}, std::true_type{}, wst, sst, i);
                 else consume(std::true_type{}, std::false_type{}, wst, sst, i);
             } else {
@@ -836,6 +901,26 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, i
     // ---- epilogue: the bf16 path's products carry 2^-7 ----
     if (*abort_flag) return;
     const float gw = __fmul_rn(args.gW ? __ldg(args.gW) : 1.0f, use_f16 ? 1.0f : 0x1p7f);
+    if (SLOT && use_f16) {
+        // a row's sum over its eight block columns: two per lane, then the four lanes t
+        float v0 = acc_s[0] + acc_s[1], v1 = acc_s[2] + acc_s[3];
+        v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
+        v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
+        v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 2);
+        v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 2);
+        if (t == 0) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int64_t n = r ? row1 : row0;
+                if (n < N) {
+                    const float v = __fmul_rn(r ? v1 : v0, gw);
+                    if (args.out_bf16) reinterpret_cast<uint16_t*>(args.y)[n] = f32_to_bf16_bits(v);
+                    else reinterpret_cast<float*>(args.y)[n] = v;
+                }
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int64_t m = 2 * t + (i & 1);
@@ -894,7 +979,7 @@ bsq_status launch_nvf4_nt(int cw, const CUtensorMap& tm, const nvf4::Args& a, cu
 
 // The resident-x kernel when x and a ring of >= 6 stages fit (M <= 2 at K = 8192);
 // returns -1 (nothing launched) when they do not.
-template <int CW>
+template <int CW, bool SLOT>
 int launch_nvf4_res_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
     constexpr int R = 16 * CW;
     constexpr int64_t kStage = R * 128 + nvf4::kMaxRowBlocks * 2048;
@@ -905,7 +990,7 @@ int launch_nvf4_res_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t
     if (stages > nvf4::kResMaxStages) stages = nvf4::kResMaxStages;
     if (stages < 6) return -1;                               // a shallower ring starves the consumers
     const size_t smem = (size_t)(fixed + stages * kStage);
-    auto kern = nvf4::gemv_nvf4_res_kernel<CW>;
+    auto kern = nvf4::gemv_nvf4_res_kernel<CW, SLOT>;
     static std::once_flag once[64];
     static bool ok_dev[64];
     int dev = 0;
@@ -920,13 +1005,18 @@ int launch_nvf4_res_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t
     return (int)launch_status();
 }
 
-int launch_nvf4_res(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+template <bool SLOT>
+int launch_nvf4_res_slot(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
     switch (cw) {
-    case 12: return launch_nvf4_res_cfg<12>(tm, a, s);
-    case 8: return launch_nvf4_res_cfg<8>(tm, a, s);
-    case 6: return launch_nvf4_res_cfg<6>(tm, a, s);
-    default: return launch_nvf4_res_cfg<4>(tm, a, s);
+    case 12: return launch_nvf4_res_cfg<12, SLOT>(tm, a, s);
+    case 8: return launch_nvf4_res_cfg<8, SLOT>(tm, a, s);
+    case 6: return launch_nvf4_res_cfg<6, SLOT>(tm, a, s);
+    default: return launch_nvf4_res_cfg<4, SLOT>(tm, a, s);
     }
+}
+
+int launch_nvf4_res(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+    return a.M == 1 ? launch_nvf4_res_slot<true>(cw, tm, a, s) : launch_nvf4_res_slot<false>(cw, tm, a, s);
 }
 
 bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t* W, const uint8_t* sW,
