@@ -391,8 +391,51 @@ def run_bsq(args, rank, world, dev_index):
         e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in e_ev])), dist, dev)
         e2e = {"value": round(job_throughput(per_step, world, e_ms), 3), "unit": unit, "ms_per_step": round(e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    small_m = small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) \
+        if args.workload == "w6a8_e4m3xe2m3_4096x14336x4096" else None
     return dict(value=value, unit=unit, step_ms=step_ms, roofline=roof, per_op_us=per_op, e2e=e2e,
-                launches=launches, clocks=clk.summary(), wl=wl)
+                launches=launches, clocks=clk.summary(), wl=wl, small_m=small_m)
+
+
+def small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
+    """The W6A8 layer's activation-side quantizer at decode sizes: bf16 [M, K]
+    -> e2m3 codes + UE8M0 scales for M in {1, 4, 16}, K = 4096 (one launch each),
+    timed like the step (a captured graph with event nodes at its ends, L2
+    flushed before every replay); mean microseconds per call."""
+    import torch
+    from block_scaled_precision_packed_gb300 import bsq, synthetic as S
+    K = wl.K
+    out = {}
+    for M in (1, 4, 16):
+        x = S.normal_bf16((M, K), wl.cfg["a_std"], wl.cfg["seed"] + 10 + M)
+        xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        codes = torch.empty((M, 3 * K // 4), dtype=torch.uint8, device=dev)
+        scales = torch.empty(bsq.scale_bytes(M, K // 32), dtype=torch.uint8, device=dev)
+        sg = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = torch.empty(max(16, bsq.quantize_workspace_bytes(M, K)), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            bsq.quantize_mxfp6_(xd, 1, codes, scales, sg, ws, stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True, external=True)
+        e1 = torch.cuda.Event(enable_timing=True, external=True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e0.record(stream)
+            bsq.quantize_mxfp6_(xd, 1, codes, scales, sg, ws, stream)
+            e1.record(stream)
+        ts = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(i + 2000)
+                torch.sum(flush_b, dim=0, dtype=torch.int64, out=flush_sink)
+                g.replay()
+            stream.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        out[f"M={M}"] = round(float(np.mean(ts)), 2)
+    out["K"] = K
+    out["format"] = "bf16 -> e2m3, UE8M0 per 32"
+    return out
 
 
 # ----------------------------------------------------------- CPU oracle arm ---
@@ -526,6 +569,8 @@ def main():
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "roofline": r["roofline"], "per_op_us": r["per_op_us"], "e2e": r["e2e"],
             "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "cpu_baseline": cpu}
+    if r["small_m"] is not None:
+        line["quantizer_small_m_us"] = r["small_m"]
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

@@ -109,3 +109,32 @@ def test_gemm_mx(bsq, fa, fw, M, N, K):
                            dev_tensor(W), fw, dev_tensor(sW), torch.tensor([gW], device="cuda"), K, out_dtype=out)
         want, s = O.gemm_mx(A, MX[fa], sA, gA, W, MX[fw], sW, gW, M, N, K)
         check_products(y, want, s, f"gemm_{fa}x{fw} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1100, 4315, 256), (1024, 9728, 128)])
+def test_gemm_nvfp4_many_tiles(bsq, M, N, K):
+    """At least one 256-wide tile per SM (the persistent 128 x 256 path) with
+    several row blocks, an odd row-block count with a ragged last block, and a
+    ragged N edge; every output checked."""
+    A, sA = nvfp4_operand(M, K, 91 + M)
+    W, sW = nvfp4_operand(N, K, 93 + N)
+    gA = torch.tensor([0.5], device="cuda")
+    gW = torch.tensor([0.75], device="cuda")
+    y = bsq.gemm_nvfp4(dev_tensor(A), dev_tensor(sA), gA, dev_tensor(W), dev_tensor(sW), gW, K,
+                       out_dtype=torch.bfloat16)
+    want, s = O.gemm_nvfp4(A, sA, 0.5, W, sW, 0.75, M, N, K)
+    check_products(y, want, s, f"gemm_nvfp4 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fa,fw", [("e4m3", "e2m3"), ("e3m2", "e3m2")])
+def test_gemm_mx_many_tiles(bsq, fa, fw):
+    """The persistent 128 x 256 path for MX operands (fp6 W included) on a
+    ragged shape with more tiles than SMs; every output checked."""
+    M, N, K = 1100, 4315, 256
+    A, sA, gA = mx_operand(M, K, fa, 95)
+    W, sW, gW = mx_operand(N, K, fw, 97)
+    y = bsq.gemm_mxfp6(dev_tensor(A), fa, dev_tensor(sA), torch.tensor([gA], device="cuda"),
+                       dev_tensor(W), fw, dev_tensor(sW), torch.tensor([gW], device="cuda"), K,
+                       out_dtype=torch.float32)
+    want, s = O.gemm_mx(A, MX[fa], sA, gA, W, MX[fw], sW, gW, M, N, K)
+    check_products(y, want, s, f"gemm_{fa}x{fw} {M}x{N}x{K}")
