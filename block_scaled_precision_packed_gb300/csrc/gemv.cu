@@ -933,6 +933,346 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, i
     }
 }
 
+
+// Tensor-core variant (17 <= M <= 32): the decoded weight becomes the A operand
+// of tcgen05.mma kind::f16 straight from tensor memory, so the warps that
+// decode do no MMA work, no x fragment loads and hold no accumulators.
+//  * CTA = one 128-row weight tile, two CTAs per SM; warp 0 issues TMA, warp 1
+//    owns TMEM and issues the MMAs, warps 2..9 decode (two per TMEM lane
+//    quarter: warp pair h takes K half h of every 256-code stage, a "granule").
+//  * Stage (256 codes): the codes (2-D box {128 B, 128 rows}, 128-byte
+//    swizzle), the tile's four scale atoms (bulk copy) and x as four 2-D boxes
+//    {64 values, NP rows} (128-byte swizzle, rows >= M zero-filled) -- x is
+//    already the K-major B operand of the MMA (N = NP = 16 or 32).
+//  * Granule (128 codes of every row): the pair checks whether its 2 x NP x 64
+//    x values are exact in f16 (one AND over its 128 threads); if so it
+//    rewrites them in place as f16 and decodes its codes with the hardware
+//    e2m1 -> f16 conversion times the ue4m3 scale (exact); else x stays bf16
+//    and the codes take the placed-bf16 decode (value * scale * 2^-7, exact),
+//    accumulating into a second fp32 tile that is lifted by 2^7 at the end.
+//    Thread (q, l) owns tile row 32q + l: four 16-byte chunks of its row ->
+//    64 f16x2 words -> tcgen05.st into TMEM lane 32q + l (column j holds K
+//    values 2j, 2j + 1), one of three 64-column granule slots.
+//  * MMA: per granule eight kind::f16 MMAs (M = 128, N = NP, K = 16, A from
+//    TMEM) into the f16 or the bf16 accumulator (NP columns each, zeroed by
+//    the decode warps first); each granule slot is released by a commit, each
+//    stage after its second granule.
+//  * Epilogue: the decode warps read both accumulators (tcgen05.ld), combine,
+//    scale by gW and store y[m, n] for m < M.
+// Every wait is bounded (2 s); a timeout records its site in the device error
+// word and the CTA drains what it issued before it leaves.
+namespace tc {
+
+constexpr int kStages = 3;
+constexpr int kDecWarps = 8;
+constexpr int kThreads = (2 + kDecWarps) * 32;
+constexpr uint32_t kTmemCols = 256;
+constexpr int kSlots = 3;                 // A granule slots (64 columns each)
+constexpr uint32_t kColDh = 192, kColDb = 224;
+
+template <int NP>
+struct Plan {
+    static constexpr int kW = 128 * 128;
+    static constexpr int kS = 4 * 512;
+    static constexpr int kXBox = NP * 128;
+    static constexpr int kX = 4 * kXBox;
+    static constexpr int kStage = kW + kS + kX;          // a multiple of 1024
+    static constexpr int kBytes = 1024 + kStages * kStage + 256;
+    static_assert(kStage % 1024 == 0, "1024-byte aligned stages (128-byte swizzle)");
+};
+
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;"
+                 :: "r"(d), "r"(a_tmem), "l"(bdesc), "r"(idesc) : "memory");
+}
+__device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+// Both bf16 halves of w are exactly f16 values: zero, or a magnitude in
+// [2^-17, 2^16) (exponent field 110..142), where every bf16 value has at most
+// 8 significant bits that an f16 normal or subnormal holds.
+__device__ __forceinline__ bool f16_exact_pair(uint32_t w) {
+    const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
+    return ((lo == 0) | (lo - (110u << 7) < (33u << 7))) & ((hi == 0) | (hi - (110u << 7) < (33u << 7)));
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
+    return r;
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 2)
+gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Args args) {
+    using P = Plan<NP>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * P::kStage);
+    uint64_t* empty = full + kStages;
+    uint64_t* a_full = empty + kStages;
+    uint64_t* a_empty = a_full + kSlots;
+    uint64_t* acc_full = a_empty + kSlots;
+    uint64_t* drain = acc_full + 1;
+    uint32_t* xflag = reinterpret_cast<uint32_t*>(drain + 1);        // [kSlots]: granule's x is f16
+    uint32_t* tmem_base_s = xflag + kSlots;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t M = args.M, N = args.N, K = args.K;
+    const int64_t row_base = (int64_t)blockIdx.x * 128;
+    const int nst = (int)((K + 255) / 256);
+    const int ngr = 2 * nst;
+    const int nblocks = (int)(K / 16);
+    const int64_t rb = row_base >> 7;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), 1);
+        }
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(smem_u32(a_full + i), 4);
+            mbar_init(smem_u32(a_empty + i), 1);
+        }
+        mbar_init(smem_u32(acc_full), 1);
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base_s;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmX);
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages &&
+                    !mbar_wait(smem_u32(empty + s), ((i / kStages) - 1) & 1, args.err, abort_flag, kErrGemvProducer))
+                    break;
+                const int64_t atoms_left = args.cpd4 - 4LL * i;
+                const uint32_t n_atoms = (uint32_t)(atoms_left < 4 ? atoms_left : 4);
+                uint8_t* st = smem + s * P::kStage;
+                const uint32_t fb = smem_u32(full + s);
+                mbar_arrive_expect_tx(fb, P::kW + n_atoms * 512 + P::kX);
+                tma_load_2d(smem_u32(st), &tmW, fb, i * 128, (int32_t)row_base);
+                bulk_load(smem_u32(st + P::kW), args.sW + (rb * args.cpd4 + 4LL * i) * 512, n_atoms * 512, fb);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tma_load_2d(smem_u32(st + P::kW + P::kS + j * P::kXBox), &tmX, fb, i * 256 + 64 * j, 0);
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                for (int i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i) {
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(full + i % kStages), (i / kStages) & 1) &&
+                           globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA --
+        if (lane == 0) {
+            const uint32_t id_h = (1u << 4) | ((uint32_t)(NP >> 3) << 17) | ((128u >> 4) << 24);
+            const uint32_t id_b = id_h | (1u << 7) | (1u << 10);
+            const uint64_t dX0 = smem_desc(smem_u32(smem + P::kW + P::kS), 16, 1024, 2);
+            for (int gi = 0; gi < ngr; ++gi) {
+                const int slot = gi % kSlots, i = gi >> 1, h = gi & 1, s = i % kStages;
+                if (h == 0 && !mbar_wait(smem_u32(full + s), (i / kStages) & 1, args.err, abort_flag, kErrGemvConsumer))
+                    break;
+                if (!mbar_wait(smem_u32(a_full + slot), (gi / kSlots) & 1, args.err, abort_flag, kErrGemvConsumer))
+                    break;
+                tc_fence_after();
+                const bool f16 = xflag[slot] != 0;
+                const uint32_t d = tmem + (f16 ? kColDh : kColDb);
+                const uint32_t idesc = f16 ? id_h : id_b;
+                const uint64_t xs = dX0 + (uint64_t)((s * P::kStage) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int box = 2 * h + (kk >> 2);
+                    mma_f16_ts(d, tmem + 64 * slot + 8 * kk, xs + (uint64_t)((box * P::kXBox) >> 4) + 2 * (kk & 3),
+                               idesc);
+                }
+                tc_commit(smem_u32(a_empty + slot));
+                if (h == 1 || gi == ngr - 1) tc_commit(smem_u32(empty + s));
+            }
+            tc_commit(smem_u32(acc_full));
+            tc_commit(smem_u32(drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(drain), 0)) {
+                if (globaltimer() - t0 > kWaitLimitNs) { atomicCAS(args.err, 0u, (uint32_t)kErrGemvConsumer); break; }
+            }
+        }
+    } else {
+        // --------------------------------------------------------- decode --
+        const int q = warp & 3;                        // TMEM lane quarter
+        const int h = (warp - 2) >> 2;                 // K half of every stage
+        const int ptid = (warp - 2 - 4 * h) * 32 + lane;   // 0..127 within the pair
+        const int r = 32 * q + lane;                   // tile row
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        if (h == 0) {   // both accumulators start at zero (every MMA accumulates), before
+                        // this pair's first granule is handed to the MMA warp
+            uint32_t z[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = 0;
+            tc_st_cols(lane_base + kColDh, z);
+            tc_st_cols(lane_base + kColDb, z);
+            tc_wait_st();
+        }
+        const uint32_t soff = (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4);
+        const int xunits = (int)(16 * M);            // 16-byte x units of rows < M in the pair's two boxes
+        constexpr int kXPer = NP / 8;                  // at most this many per pair thread
+        for (int gi = h; gi < ngr; gi += 2) {
+            const int slot = gi % kSlots, i = gi >> 1, s = i % kStages;
+            uint8_t* st = smem + s * P::kStage;
+            const bool have = mbar_wait(smem_u32(full + s), (i / kStages) & 1, args.err, abort_flag, kErrGemvConsumer);
+            // x boxes 2h, 2h + 1: exact in f16?  (the named barrier runs even after a failed wait)
+            uint8_t* xb = st + P::kW + P::kS + 2 * h * P::kXBox;
+            // unit v: box 2h + v / (8M), row (v % (8M)) / 8, 16-byte piece v % 8 (rows >= M are zero fill)
+            auto xaddr = [&](int v) {                       // v < 16M: two boxes of 8M units
+                const int half = 8 * (int)M;
+                return v < half ? xb + v * 16 : xb + P::kXBox + (v - half) * 16;
+            };
+            uint4 xv[kXPer];
+            bool ok = true;
+#pragma unroll
+            for (int u = 0; u < kXPer; ++u) {
+                const int v = ptid + 128 * u;
+                xv[u] = make_uint4(0, 0, 0, 0);
+                if (have && v < xunits) xv[u] = *reinterpret_cast<const uint4*>(xaddr(v));
+                ok &= f16_exact_pair(xv[u].x) & f16_exact_pair(xv[u].y) & f16_exact_pair(xv[u].z) &
+                      f16_exact_pair(xv[u].w);
+            }
+            const bool f16 = bar_and(1 + h, 128, ok);
+            if (gi >= kSlots &&
+                !mbar_wait(smem_u32(a_empty + slot), ((gi / kSlots) - 1) & 1, args.err, abort_flag, kErrGemvConsumer))
+                continue;
+            if (!have) continue;
+            if (f16) {
+#pragma unroll
+                for (int u = 0; u < kXPer; ++u) {
+                    const int v = ptid + 128 * u;
+                    if (v < xunits)
+                        *reinterpret_cast<uint4*>(xaddr(v)) =
+                            make_uint4(bf16x2_to_f16x2(xv[u].x), bf16x2_to_f16x2(xv[u].y), bf16x2_to_f16x2(xv[u].z),
+                                       bf16x2_to_f16x2(xv[u].w));
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            // the row's 4 chunks of this granule: chunk c = 4h + cc (32 codes, blocks 2c, 2c + 1 of the stage)
+            const uint32_t wrow = smem_u32(st) + r * 128;
+            const uint8_t* srow = st + P::kW + soff;
+            const bool tail = 16 * (i + 1) > nblocks;        // uniform: only the last stage
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = 4 * h + cc;
+                const uint4 w = lds128(wrow + ((c ^ (r & 7)) << 4));
+                uint32_t two = *reinterpret_cast<const uint16_t*>(srow + (c >> 1) * 512 + ((2 * c) & 3));
+                if (tail) {                                   // blocks past K: scale 0
+                    const int blk0 = 16 * i + 2 * c;
+                    if (blk0 >= nblocks) two &= 0xFF00u;
+                    if (blk0 + 1 >= nblocks) two &= 0x00FFu;
+                }
+                uint32_t a[16];
+                if (f16) {
+                    const uint32_t sf = e4m3x2_to_f16x2(two);
+                    const uint32_t s0 = __byte_perm(sf, sf, 0x1010), s1 = __byte_perm(sf, sf, 0x3232);
+                    uint32_t t4[4];
+                    e2m1x8_to_f16x2(w.x, t4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[j] = hmul2(t4[j], s0);
+                    e2m1x8_to_f16x2(w.y, t4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[4 + j] = hmul2(t4[j], s0);
+                    e2m1x8_to_f16x2(w.z, t4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[8 + j] = hmul2(t4[j], s1);
+                    e2m1x8_to_f16x2(w.w, t4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[12 + j] = hmul2(t4[j], s1);
+                } else {
+                    const uint32_t b0 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32(two & 0xFF), 0x1p119f));
+                    const uint32_t b1 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32((two >> 8) & 0xFF), 0x1p119f));
+                    const uint32_t s0 = b0 | (b0 << 16), s1 = b1 | (b1 << 16);
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            a[4 * k + j] = bmul2(place_byte_bf16x2((ww[k] >> (8 * j)) & 0xFFu), k < 2 ? s0 : s1);
+                }
+                tc_st_cols(lane_base + 64 * slot + 16 * cc, a);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (warp - 2 - 4 * h == 0) xflag[slot] = f16 ? 1u : 0u;   // read after a_full completes
+                mbar_arrive(smem_u32(a_full + slot));
+            }
+        }
+        // ------------------------------------------------------- epilogue --
+        if (mbar_wait(smem_u32(acc_full), 0, args.err, abort_flag, kErrGemvConsumer) && !*abort_flag) {
+            tc_fence_after();
+            const float gw = args.gW ? __ldg(args.gW) : 1.0f;
+            const int64_t n = row_base + r;
+            // pair h stores activation rows [h NP/2, (h+1) NP/2)
+            constexpr int kHalf = NP / 2;
+            float v[kHalf];
+            if constexpr (kHalf == 16) {
+                uint32_t dh[16], db[16];
+                tc_ld_32x32b_x16(lane_base + kColDh + 16 * h, dh);
+                tc_ld_32x32b_x16(lane_base + kColDb + 16 * h, db);
+                tc_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    v[j] = __fmaf_rn(__uint_as_float(db[j]), 0x1p7f, __uint_as_float(dh[j]));
+            } else {
+                uint32_t dh[16], db[16];
+                tc_ld_32x32b_x16(lane_base + kColDh, dh);
+                tc_ld_32x32b_x16(lane_base + kColDb, db);
+                tc_wait_ld();
+#pragma unroll
+                for (int j = 0; j < kHalf; ++j) {
+                    const int jj = kHalf * h + j;
+                    v[j] = __fmaf_rn(__uint_as_float(db[jj]), 0x1p7f, __uint_as_float(dh[jj]));
+                }
+            }
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < kHalf; ++j) {
+                    const int64_t m = kHalf * h + j;
+                    if (m < M) {
+                        const float o = __fmul_rn(v[j], gw);
+                        if (args.out_bf16) reinterpret_cast<uint16_t*>(args.y)[m * N + n] = f32_to_bf16_bits(o);
+                        else reinterpret_cast<float*>(args.y)[m * N + n] = o;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace tc
+
 }  // namespace nvf4
 
 // Consumer warps per CTA (16 rows each) for the nvfp4 GEMV: the choice in
@@ -1019,6 +1359,38 @@ int launch_nvf4_res(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStre
     return a.M == 1 ? launch_nvf4_res_slot<true>(cw, tm, a, s) : launch_nvf4_res_slot<false>(cw, tm, a, s);
 }
 
+
+// The tensor-core kernel (17 <= M <= 32); -1 when it cannot be launched here.
+template <int NP>
+int launch_nvf4_tc_cfg(const DeviceInfo* info, const CUtensorMap& tmW, const uint16_t* x, const nvf4::Args& a,
+                       cudaStream_t s) {
+    using P = nvf4::tc::Plan<NP>;
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return -1;
+    CUtensorMap tmX;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K * 2)};
+    const cuuint32_t box[2] = {64, (cuuint32_t)NP};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(x), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return -1;
+    auto kern = nvf4::tc::gemv_nvf4_tc_kernel<NP>;
+    static std::once_flag once[64];
+    static bool ok_dev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
+    std::call_once(once[dev], [&] {
+        ok_dev[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kBytes) == cudaSuccess;
+    });
+    if (!ok_dev[dev]) { (void)cudaGetLastError(); return -1; }
+    (void)info;
+    const dim3 grid((unsigned)((a.N + 127) / 128));
+    kern<<<grid, nvf4::tc::kThreads, P::kBytes, s>>>(tmW, tmX, a);
+    return (int)launch_status();
+}
+
 bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t* W, const uint8_t* sW,
                        const float* gW, void* y, int out, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
     const int cw = nvf4_warps(N, info->num_sms);
@@ -1037,6 +1409,18 @@ bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t*
     a.x = x; a.sW = sW; a.gW = gW; a.y = y; a.err = info->err; a.M = M; a.N = N; a.K = K;
     a.cpd4 = pad_to(K / 16, 4) / 4;
     a.out_bf16 = out;
+    if (M > 16) {
+        // 17..32 activation rows: the tensor-core kernel (mma.sync issue would
+        // bound the register-decode kernels); it reads the weight in 128-row tiles
+        CUtensorMap tm128;
+        const cuuint32_t box128[2] = {128, 128};
+        if (enc(&tm128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), dims, strides, box128, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+            const int st = launch_nvf4_tc_cfg<32>(info, tm128, x, a, s);
+            if (st >= 0) return (bsq_status)st;
+        }
+    }
     if (M <= 8) {
         const int st = launch_nvf4_res(cw, tm, a, s);
         if (st >= 0) return (bsq_status)st;

@@ -28,7 +28,7 @@ def mx_operand(R, K, fmt_name, seed):
     return O.quantize_mx(x, MX[fmt_name])
 
 
-@pytest.mark.parametrize("M", [1, 2, 5, 8, 13, 32])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 13, 17, 32])
 @pytest.mark.parametrize("N,K", [(256, 256), (300, 320), (129, 1024), (1, 64), (200, 4160), (1000, 2048)])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 def test_gemv_nvfp4(bsq, M, N, K, out):
