@@ -393,8 +393,58 @@ def run_bsq(args, rank, world, dev_index):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     small_m = small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) \
         if args.workload == "w6a8_e4m3xe2m3_4096x14336x4096" else None
+    fused_act = fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) \
+        if args.workload == "mxfp6_e3m2_w6a6_128x4096x4096" else None
     return dict(value=value, unit=unit, step_ms=step_ms, roofline=roof, per_op_us=per_op, e2e=e2e,
-                launches=launches, clocks=clk.summary(), wl=wl, small_m=small_m)
+                launches=launches, clocks=clk.summary(), wl=wl, small_m=small_m, fused_act=fused_act)
+
+
+def graph_call_us(fn, stream, flush, flush_b, flush_sink, args):
+    """Mean device time of one call of fn(stream), captured as a graph with
+    event nodes at its ends and replayed with the L2 flushed before each run."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn(stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True, external=True)
+    e1 = torch.cuda.Event(enable_timing=True, external=True)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        e0.record(stream)
+        fn(stream)
+        e1.record(stream)
+    ts = []
+    for i in range(args.warmup + args.steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(i + 3000)
+            torch.sum(flush_b, dim=0, dtype=torch.int64, out=flush_sink)
+            g.replay()
+        stream.synchronize()
+        if i >= args.warmup:
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    return float(np.mean(ts))
+
+
+def fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
+    """The W6A6 layer's activation side with the activation fused into the
+    quantizer (bsq_quantize_mxfp6_act): ReLU^2 of [M, K] and SiLU(gate) * up of
+    [M, 2K] -> e3m2 codes + UE8M0 scales, M = 128, K = 4096, inputs N(0, 1)."""
+    import torch
+    from block_scaled_precision_packed_gb300 import bsq, synthetic as S
+    M, K = wl.M, wl.K
+    out = {"M": M, "K": K, "format": "e3m2, UE8M0 per 32"}
+    for name, act, kin in (("relu2", bsq.ACT_RELU2, K), ("silu_mul", bsq.ACT_SILU_MUL, 2 * K)):
+        x = S.normal_bf16((M, kin), 1.0, wl.cfg["seed"] + 20 + act)
+        xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        codes = torch.empty((M, 3 * K // 4), dtype=torch.uint8, device=dev)
+        scales = torch.empty(bsq.scale_bytes(M, K // 32), dtype=torch.uint8, device=dev)
+        sg = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = torch.empty(max(16, bsq.quantize_workspace_bytes(M, K)), dtype=torch.uint8, device=dev)
+        us = graph_call_us(lambda s: bsq.quantize_mxfp6_act_(xd, K, act, 0, codes, scales, sg, None, ws, s),
+                           stream, flush, flush_b, flush_sink, args)
+        by = M * kin * 2 + M * 3 * K // 4 + bsq.scale_bytes(M, K // 32)
+        out[name] = {"us": round(us, 2), "algorithmic_bytes": by, "GB/s": round(by / (us * 1e-6) / 1e9, 1)}
+    return out
 
 
 def small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
@@ -571,6 +621,8 @@ def main():
             "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "cpu_baseline": cpu}
     if r["small_m"] is not None:
         line["quantizer_small_m_us"] = r["small_m"]
+    if r["fused_act"] is not None:
+        line["fused_activation_quantizer"] = r["fused_act"]
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

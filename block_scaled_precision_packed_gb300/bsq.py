@@ -60,6 +60,7 @@ def load(path: str | None = None):
             "bsq_quantize_mxfp6": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_nvfp4": (i32, [vp, i64, i64, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_mxfp6_noalloc": (i32, [vp, i64, i64, i32, vp, vp, vp, vp]),
+            "bsq_quantize_mxfp6_act": (i32, [vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_batch_workspace_bytes": (sz, []),
             "bsq_quantize_mxfp6_batch": (i32, [vp, i32, i32, vp, sz, vp]),
             "bsq_quantize_nvfp4_batch": (i32, [vp, i32, vp, sz, vp]),
@@ -120,6 +121,18 @@ def quantize_mxfp6_noalloc_(x, fmt, codes, scales, s_global, stream=None):
     M, K = x.shape
     _check("bsq_quantize_mxfp6_noalloc", load().bsq_quantize_mxfp6_noalloc(
         _p(x), M, K, fmt, _p(codes), _p(scales), _p(s_global), _stream(stream)))
+
+
+ACT_RELU2, ACT_SILU_MUL = 1, 2
+
+
+def quantize_mxfp6_act_(x, K, act, fmt, codes, scales, s_global, act_out=None, workspace=None, stream=None):
+    """Fused activation + MX quantize: x [M, K] (ReLU^2) or [M, 2K] (SiLU(gate) * up)."""
+    M = x.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("bsq_quantize_mxfp6_act", load().bsq_quantize_mxfp6_act(
+        _p(x), M, K, act, fmt, _p(codes), _p(scales), _p(s_global), _p(act_out), _p(workspace), ws_bytes,
+        _stream(stream)))
 
 
 def quantize_nvfp4_(x, codes, scales, s_global, workspace=None, stream=None):
@@ -228,6 +241,22 @@ def quantize_mxfp6(x, fmt="e3m2"):
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev) if wsb else None
     quantize_mxfp6_(x, f, codes, scales, g, ws)
     return codes, scales, g
+
+
+def quantize_mxfp6_act(x, act, fmt="e3m2", want_act=False):
+    """Fused activation + MX quantize of a bf16 CUDA tensor: (codes, scales,
+    s_global[, activated bf16])."""
+    fmt_id = {"e3m2": 0, "e2m3": 1, "e4m3": 2}[fmt]
+    M, Kin = x.shape
+    K = Kin if act == ACT_RELU2 else Kin // 2
+    dev = x.device
+    codes = torch.empty((M, K if fmt_id == 2 else 3 * K // 4), dtype=torch.uint8, device=dev)
+    scales = torch.empty(scale_bytes(M, K // 32), dtype=torch.uint8, device=dev)
+    sg = torch.empty(1, dtype=torch.float32, device=dev)
+    a = torch.empty((M, K), dtype=torch.bfloat16, device=dev) if want_act else None
+    ws = torch.empty(max(16, quantize_workspace_bytes(M, K)), dtype=torch.uint8, device=dev)
+    quantize_mxfp6_act_(_bf16_bits(x), K, act, fmt_id, codes, scales, sg, a, ws)
+    return (codes, scales, sg, a) if want_act else (codes, scales, sg)
 
 
 def quantize_nvfp4(x):

@@ -125,6 +125,18 @@ bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt
     return quantize_mx_launch(x, M, K, fmt, codes, scales, s_global, workspace, workspace_bytes, stream);
 }
 
+bsq_status bsq_quantize_mxfp6_act(const uint16_t* x, int64_t M, int64_t K, bsq_act act, bsq_mxfmt fmt,
+                                  uint8_t* codes, uint8_t* scales, float* s_global, uint16_t* act_out,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!x || !codes || !scales || !s_global || !valid_mx(fmt)) return BSQ_ERR_INVALID_ARG;
+    if (act != BSQ_ACT_RELU2 && act != BSQ_ACT_SILU_MUL) return BSQ_ERR_INVALID_ARG;
+    if (M < 1 || K < 32 || K % 32 || M >= kMaxDim || 2 * K >= kMaxDim) return BSQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (act_out && !aligned16(act_out)))
+        return BSQ_ERR_MISALIGNED;
+    return quantize_mx_act_launch(x, M, K, (int)act, fmt, codes, scales, s_global, act_out, workspace,
+                                  workspace_bytes, stream);
+}
+
 size_t bsq_quantize_batch_workspace_bytes(void) { return quantize_batch_workspace_bytes(); }
 
 static bsq_status quantize_batch(const bsq_qtensor* t, int n, int fmt, void* ws, size_t ws_bytes, cudaStream_t s) {

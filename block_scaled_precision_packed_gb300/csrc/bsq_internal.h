@@ -48,6 +48,10 @@ struct QTensor {
 // Entry points implemented per translation unit.
 bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, uint8_t* codes,
                               uint8_t* scales, float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
+// act: 1 = ReLU^2, 2 = SiLU(gate) * up (x rows of 2K); act_out optional
+bsq_status quantize_mx_act_launch(const uint16_t* x, int64_t M, int64_t K, int act, int fmt, uint8_t* codes,
+                                  uint8_t* scales, float* s_global, uint16_t* act_out, void* ws, size_t ws_bytes,
+                                  cudaStream_t s);
 bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,
                                  float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t quantize_workspace_bytes(int64_t M, int64_t K);

@@ -682,6 +682,140 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
     }
 }
 
+// ------------------------------------------------- fused activation ----
+// Activation + MX quantize (b12x _lib/fp6.py relu2_quantize_grouped_mxfp6_torch,
+// silu_mul_quantize_grouped_mxfp6_torch): the activation is evaluated in f32
+// and rounded to bf16 (the input dtype), and that tensor -- never stored, unless
+// the caller asks for it -- goes through the same amax / scale / encode steps.
+//   ReLU^2:    max(x, 0)^2 (one f32 product, exact), x [M, K].
+//   SiLU * up: fl(fl(g / fl(1 + exp(-g))) * u), x [M, 2K] = gate | up per row;
+//              exp is CUDA's expf (not a fast approximation).
+// Two launch shapes as for the plain MX quantizer: one 16-CTA cluster for small
+// tensors, else an amax pass over the activated values into the workspace and
+// an encode pass that evaluates the activation again (same instructions, same
+// bits) -- the input is read twice, the activated tensor never.
+constexpr int kActRelu2 = 1, kActSiluMul = 2;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float relu2_f32(float v) {
+    const float r = v > 0.0f ? v : 0.0f;
+    return __fmul_rn(r, r);
+}
+__device__ __forceinline__ float silu_mul_f32(float g, float u) {
+    const float e = expf(-g);
+    const float d = __fadd_rn(1.0f, e);
+    return __fmul_rn(__fdiv_rn(g, d), u);
+}
+// Activated outputs (row, col .. col + 7) as bf16 bits; K = output columns.
+template <int ACT>
+__device__ __forceinline__ uint4 act8(const uint16_t* __restrict__ x, int64_t row, int64_t col, int64_t K) {
+    if constexpr (ACT == kActRelu2) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + row * K + col));
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(relu2_f32(bf16_lo(in[i])), relu2_f32(bf16_hi(in[i])));
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+        const uint4 gv = __ldg(reinterpret_cast<const uint4*>(x + row * 2 * K + col));
+        const uint4 uv = __ldg(reinterpret_cast<const uint4*>(x + row * 2 * K + K + col));
+        const uint32_t g[4] = {gv.x, gv.y, gv.z, gv.w}, u[4] = {uv.x, uv.y, uv.z, uv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = pack_bf16x2(silu_mul_f32(bf16_lo(g[i]), bf16_lo(u[i])), silu_mul_f32(bf16_hi(g[i]), bf16_hi(u[i])));
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+// Max |activated| over output units [lo, hi) (a unit = 8 outputs of one row).
+template <int ACT>
+__device__ __forceinline__ uint32_t act_absmax_units(const uint16_t* __restrict__ x, int64_t K, int64_t lo,
+                                                     int64_t hi, int64_t step) {
+    const int64_t upr = K / 8;
+    uint32_t m = 0;
+    for (int64_t i = lo; i < hi; i += step) {
+        const int64_t row = i / upr, col = 8 * (i - row * upr);
+        m = max(m, absmax8_bits(act8<ACT>(x, row, col, K)));
+    }
+    return m;
+}
+
+template <int ACT>
+__global__ void __launch_bounds__(kThreads) act_amax_partial_kernel(const uint16_t* __restrict__ x, int64_t M,
+                                                                    int64_t K, uint32_t* __restrict__ partial) {
+    __shared__ uint32_t red[32];
+    launch_dependents();
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    uint32_t m = act_absmax_units<ACT>(x, K, (int64_t)blockIdx.x * kThreads + threadIdx.x, M * K / 8, stride);
+    m = block_max(m, red);
+    if (threadIdx.x == 0) partial[blockIdx.x] = m;
+}
+
+template <int FMT, bool FUSED, int ACT>
+__global__ void __launch_bounds__(kEncThreads)
+quant_mx_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint32_t* __restrict__ partial,
+                    int n_partial, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                    float* __restrict__ s_global, uint16_t* __restrict__ act_out) {
+    __shared__ uint32_t red[32];
+    __shared__ uint32_t xchg;
+    uint32_t am_bits;
+    if constexpr (FUSED) {
+        const uint32_t rank = cluster_rank(), csize = cluster_size();
+        const int64_t n8 = M * K / 8;
+        const int64_t lo = n8 * rank / csize, hi = n8 * (rank + 1) / csize;
+        uint32_t m = act_absmax_units<ACT>(x, K, lo + threadIdx.x, hi, blockDim.x);
+        m = block_max(m, red);
+        if (threadIdx.x == 0) xchg = m;
+        cluster_sync();                              // every CTA's partial is visible
+        uint32_t all = 0;
+        if (threadIdx.x < csize) all = ld_dsmem_u32(smem_u32(&xchg), threadIdx.x);
+        am_bits = block_max(all, red);
+        cluster_sync();                              // no CTA leaves while others read it
+    } else {
+        wait_prerequisite_grid();
+        uint32_t m = 0;
+        for (int i = threadIdx.x; i < n_partial; i += blockDim.x) m = max(m, partial[i]);
+        am_bits = block_max(m, red);
+    }
+    const float amax = bf16_bits_to_f32(am_bits);
+    const float gs = amax > 0.0f ? __fdiv_rn(gs_numerator(FMT), amax) : 0.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = gs != 0.0f ? __fdiv_rn(1.0f, gs) : 0.0f;
+
+    const int lane = threadIdx.x & 31;
+    const uint32_t nb = (uint32_t)(K / 32);
+    const int64_t cpd4 = pad_to(nb, 4) / 4;
+    const uint32_t nbp = (uint32_t)pad_to(nb, 4);
+    const uint32_t total = (uint32_t)pad_to(M, 128) * nbp;
+    const int64_t row_bytes = FMT == kE4M3 ? K : 3 * K / 4;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t gb = blockIdx.x * blockDim.x + threadIdx.x; gb < total; gb += stride) {
+        const uint32_t r = gb / nbp, b = gb - r * nbp;
+        const bool valid = r < M && b < nb;
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = valid ? act8<ACT>(x, r, 32 * (int64_t)b + 8 * i, K) : make_uint4(0, 0, 0, 0);
+        if (act_out && valid) {
+            uint4* dst = reinterpret_cast<uint4*>(act_out + (int64_t)r * K + 32 * (int64_t)b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = v[i];
+        }
+        uint32_t ue;
+        float inv;
+        mx_block_scale<FMT>(absmax32_bits(v), gs, ue, inv);
+        uint32_t w[8];
+        mx_encode_words<FMT>(v, inv, w);
+        if (valid) mx_store_words<FMT>(codes + (int64_t)r * row_bytes + (FMT == kE4M3 ? 32 : 24) * (int64_t)b, w);
+        const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
+                            (__shfl_down_sync(0xFFFFFFFFu, ue, 2) << 16) | (__shfl_down_sync(0xFFFFFFFFu, ue, 3) << 24);
+        if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(scales + swz_offset(r, b, cpd4)) = s4;
+    }
+}
+
 // ------------------------------------------------------------ launching ----
 // One cluster of kFusedCluster CTAs (16 needs the non-portable opt-in; a
 // device that refuses it gets 8).
@@ -714,10 +848,10 @@ cudaError_t launch_cluster(KernelT kernel, cudaStream_t s, Args... args) {
 // The encode pass, launched so that it may start while the amax pass runs; it
 // waits (griddepcontrol.wait) for the amax pass before reading the partials.
 template <typename KernelT, typename... Args>
-cudaError_t launch_dependent(KernelT kernel, int grid, cudaStream_t s, Args... args) {
+cudaError_t launch_dependent_n(KernelT kernel, int grid, int threads, cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kEncThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -726,6 +860,10 @@ cudaError_t launch_dependent(KernelT kernel, int grid, cudaStream_t s, Args... a
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+template <typename KernelT, typename... Args>
+cudaError_t launch_dependent(KernelT kernel, int grid, cudaStream_t s, Args... args) {
+    return launch_dependent_n(kernel, grid, kEncThreads, s, args...);
 }
 
 // The amax pass runs at full occupancy (8 x 256 threads per SM, <= 32
@@ -911,6 +1049,67 @@ bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, 
     count_launch(fused ? BSQ_KERNEL_QUANT_SMALL : BSQ_KERNEL_QUANT_MX);
     if (e != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
     return launch_status();
+}
+
+
+template <int FMT, int ACT>
+bsq_status quantize_mx_act_fmt(const DeviceInfo* info, const uint16_t* x, int64_t M, int64_t K, uint8_t* codes,
+                               uint8_t* scales, float* s_global, uint16_t* act_out, uint32_t* partial,
+                               cudaStream_t s) {
+    // The activation (an expf and a division per value for SiLU) dominates these
+    // passes, so both spread it thinly: about one 8-value unit (amax pass) or
+    // one 32-value block (encode pass) per thread, up to 4 x 256-thread CTAs per SM.
+    const bool fused = M * K <= kFusedMaxElems;
+    int n_partial = 0;
+    const int64_t cap = (int64_t)info->num_sms * 4;
+    if (!fused) {
+        const int64_t units = M * K / 8;
+        int64_t g = (units + kThreads - 1) / kThreads;
+        if (g > cap) g = cap;
+        if (g > kMaxPartials) g = kMaxPartials;
+        n_partial = (int)g;
+        act_amax_partial_kernel<ACT><<<n_partial, kThreads, 0, s>>>(x, M, K, partial);
+        count_launch(BSQ_KERNEL_AMAX);
+        if (launch_status() != BSQ_OK) return BSQ_ERR_CUDA;
+    }
+    cudaError_t e;
+    if (fused) {
+        e = launch_cluster(quant_mx_act_kernel<FMT, true, ACT>, s, x, M, K, (const uint32_t*)nullptr, 0, codes,
+                           scales, s_global, act_out);
+    } else {
+        const int64_t slots = pad_to(M, 128) * pad_to(K / 32, 4);
+        int64_t g = (slots + kThreads - 1) / kThreads;
+        if (g > cap) g = cap;
+        e = launch_dependent_n(quant_mx_act_kernel<FMT, false, ACT>, (int)g, kThreads, s, x, M, K,
+                               (const uint32_t*)partial, n_partial, codes, scales, s_global, act_out);
+    }
+    count_launch(fused ? BSQ_KERNEL_QUANT_SMALL : BSQ_KERNEL_QUANT_MX);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
+    return launch_status();
+}
+
+bsq_status quantize_mx_act_launch(const uint16_t* x, int64_t M, int64_t K, int act, int fmt, uint8_t* codes,
+                                  uint8_t* scales, float* s_global, uint16_t* act_out, void* ws, size_t ws_bytes,
+                                  cudaStream_t s) {
+    bsq_status st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
+    uint32_t* partial = static_cast<uint32_t*>(ws);
+    if (M * K > kFusedMaxElems) {
+        if (!ws || ws_bytes < quantize_workspace_bytes(M, K)) return BSQ_ERR_WORKSPACE;
+        if (!aligned16(ws)) return BSQ_ERR_MISALIGNED;
+    }
+#define BSQ_QACT(F)                                                                                           \
+    return act == kActRelu2 ? quantize_mx_act_fmt<F, kActRelu2>(info, x, M, K, codes, scales, s_global, act_out, \
+                                                                 partial, s)                                  \
+                            : quantize_mx_act_fmt<F, kActSiluMul>(info, x, M, K, codes, scales, s_global, act_out, \
+                                                                   partial, s);
+    switch (fmt) {
+    case kE3M2: BSQ_QACT(kE3M2);
+    case kE2M3: BSQ_QACT(kE2M3);
+    default: BSQ_QACT(kE4M3);
+    }
+#undef BSQ_QACT
 }
 
 bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,

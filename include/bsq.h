@@ -116,6 +116,31 @@ BSQ_API bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, b
                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * bsq_quantize_mxfp6_act -- fused activation + MX quantize.
+ * b12x _lib/fp6.py: relu2_quantize_grouped_mxfp6_torch and
+ * silu_mul_quantize_grouped_mxfp6_torch (one group): the activation is
+ * evaluated in f32 and rounded to bf16 (the input dtype), and that [M, K]
+ * tensor is quantized exactly as by bsq_quantize_mxfp6 (amax recipe, exact
+ * ceil UE8M0).  The activated tensor is not stored unless asked for.
+ *   act = BSQ_ACT_RELU2:    a = max(x, 0)^2;             x [M, K] bf16.
+ *   act = BSQ_ACT_SILU_MUL: a = fl(fl(g / fl(1 + exp(-g))) * u), g = x[m, k],
+ *                           u = x[m, K + k];             x [M, 2K] bf16.
+ *   act_out  NULL, or [M, K] bf16 (16-byte aligned): the activated tensor.
+ *   codes, scales, s_global, workspace: as bsq_quantize_mxfp6 for this M, K
+ *            (bsq_quantize_workspace_bytes(M, K)).
+ * ReLU^2 results are bit-identical to the CPU oracle.  SiLU uses CUDA's expf,
+ * whose last-place rounding can differ from a C library's, so an activated
+ * value may sit one bf16 ulp from the oracle's; codes, scales and s_global are
+ * bit-identical to the MX quantizer applied to act_out.
+ * Errors: BSQ_ERR_INVALID_ARG (null pointer, act or fmt out of range, M < 1,
+ * K % 32), BSQ_ERR_MISALIGNED, BSQ_ERR_WORKSPACE, BSQ_ERR_CUDA.
+ */
+typedef enum bsq_act { BSQ_ACT_RELU2 = 1, BSQ_ACT_SILU_MUL = 2 } bsq_act;
+BSQ_API bsq_status bsq_quantize_mxfp6_act(const uint16_t* x, int64_t M, int64_t K, bsq_act act, bsq_mxfmt fmt,
+                                          uint8_t* codes, uint8_t* scales, float* s_global, uint16_t* act_out,
+                                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * bsq_quantize_mxfp6_noalloc -- bsq_quantize_mxfp6 for callers that cannot
  * allocate device memory on this path (no counterpart on the pages; this is a
  * library convenience).  Same arguments, results and validation minus the

@@ -75,6 +75,8 @@ def _declare(L):
         "bsqo_gemm_mx_at": (i, [p, i, p, d, p, i, p, d, i64, p, p, i64, p, p, i]),
         "bsqo_gemv_nvfp4_at": (i, [p, p, p, d, i64, p, p, i64, p, p, i]),
         "bsqo_gemv_mx_at": (i, [p, p, i, p, d, i64, p, p, i64, p, p, i]),
+        "bsqo_activate": (i, [p, i64, i64, i, p]),
+        "bsqo_quantize_mx_act": (i, [p, i64, i64, i, i, p, p, p, p]),
         "bsqo_f32_to_bf16": (ctypes.c_uint16, [f]),
         "bsqo_double_to_bf16": (ctypes.c_uint16, [d]),
     }
@@ -170,6 +172,35 @@ def quantize_mx(x_bf16: np.ndarray, fmt: int):
     g = np.zeros(1, dtype=np.float32)
     _check(lib().bsqo_quantize_mx(_ptr(x), M, K, fmt, _ptr(codes), _ptr(scales), _ptr(g)), "quantize_mx")
     return codes, scales, float(g[0])
+
+
+ACT_RELU2, ACT_SILU_MUL = 1, 2
+
+
+def activate(x_bf16: np.ndarray, act: int) -> np.ndarray:
+    """The activation of the fused quantizers, rounded to bf16: ReLU^2 of x [M, K],
+    or SiLU(gate) * up of x [M, 2K] (gate = columns [0, K), up = [K, 2K))."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, Kin = x.shape
+    K = Kin if act == ACT_RELU2 else Kin // 2
+    out = np.empty((M, K), dtype=np.uint16)
+    _check(lib().bsqo_activate(_ptr(x), M, K, act, _ptr(out)), "activate")
+    return out
+
+
+def quantize_mx_act(x_bf16: np.ndarray, act: int, fmt: int):
+    """Fused activation + MX quantizer: (codes, swizzled scales, s_global, activated bf16)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, Kin = x.shape
+    K = Kin if act == ACT_RELU2 else Kin // 2
+    row_bytes = K if fmt == E4M3 else 3 * K // 4
+    codes = np.empty((M, row_bytes), dtype=np.uint8)
+    scales = np.empty(scale_bytes(M, K // 32), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    a = np.empty((M, K), dtype=np.uint16)
+    _check(lib().bsqo_quantize_mx_act(_ptr(x), M, K, act, fmt, _ptr(codes), _ptr(scales), _ptr(g), _ptr(a)),
+           "quantize_mx_act")
+    return codes, scales, float(g[0]), a
 
 
 def quantize_mx_rows(x_bf16: np.ndarray, fmt: int, rows):

@@ -21,7 +21,8 @@
  *        _encode_fp6_nearest, pack_4_fp6_codes, mxfp6_swizzled_scale_offset,
  *        unswizzle_mxfp6_scales, dequant_mxfp6_torch,
  *        quantize_grouped_mxfp6_torch, fp6_block_ue8m0_exact,
- *        ue8m0_output_scale_exact, quantize_block_fp6_*_fast.
+ *        ue8m0_output_scale_exact, quantize_block_fp6_*_fast,
+ *        relu2_quantize_grouped_mxfp6_torch, silu_mul_quantize_grouped_mxfp6_torch.
  *   [P3] Winery-Strata elementwise_parity.cpp: the f32 -> bf16 RNE rule.
  *
  * Parity status of each function (what pins it is in tests/test_oracle_*.py):
@@ -600,6 +601,55 @@ BSQO_API int bsqo_gemv_mx_at(const uint16_t* x, const uint8_t* W, int fw, const 
     operand a = {0, 0, x, NULL, 1.0}, w = {2, fw, W, sW, gW};
     product_at(&a, &w, K, mi, ni, cnt, y, s, nthreads);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fused activation + quantize ([P2] relu2_quantize_grouped_mxfp6_torch and  */
+/* silu_mul_quantize_grouped_mxfp6_torch): the activation is evaluated in f32 */
+/* and rounded to the input dtype (bf16), and that bf16 tensor is quantized   */
+/* by the MX recipe above.                                                    */
+/*   ReLU^2:    a = max(x, 0)^2 (one f32 product; exact, <= 16 significant    */
+/*              bits), rounded to bf16.                                        */
+/*   SiLU * up: the input row holds gate [0, K) then up [K, 2K);              */
+/*              a = fl(fl(g / fl(1 + exp(-g))) * u), rounded to bf16.  SiLU   */
+/*              is written as one division, g / (1 + e^-g), the logistic form */
+/*              of g * sigmoid(g); exp is the C library's expf.               */
+/* ------------------------------------------------------------------------ */
+enum { BSQO_ACT_RELU2 = 1, BSQO_ACT_SILU_MUL = 2 };
+
+BSQO_API uint16_t bsqo_f32_to_bf16(float f);
+
+BSQO_API int bsqo_activate(const uint16_t* x, int64_t M, int64_t K, int act, uint16_t* out) {
+    if (!x || !out || M < 1 || K < 1 || (act != BSQO_ACT_RELU2 && act != BSQO_ACT_SILU_MUL)) return -1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            volatile float a;
+            if (act == BSQO_ACT_RELU2) {
+                const float v = bf16_to_f32(x[m * K + k]);
+                const float r = v > 0.0f ? v : 0.0f;
+                a = r * r;
+            } else {
+                const float g = bf16_to_f32(x[m * 2 * K + k]);
+                const float u = bf16_to_f32(x[m * 2 * K + K + k]);
+                volatile float e = expf(-g);
+                volatile float d = 1.0f + e;
+                volatile float sg = g / d;
+                a = sg * u;
+            }
+            out[m * K + k] = bsqo_f32_to_bf16(a);
+        }
+    return 0;
+}
+
+BSQO_API int bsqo_quantize_mx_act(const uint16_t* x, int64_t M, int64_t K, int act, int fmt, uint8_t* codes,
+                                  uint8_t* scales, float* s_global, uint16_t* act_out) {
+    if (M < 1 || K < 32 || K % 32) return -1;
+    uint16_t* a = act_out ? act_out : (uint16_t*)malloc((size_t)(M * K) * sizeof(uint16_t));
+    if (!a) return -1;
+    int rc = bsqo_activate(x, M, K, act, a);
+    if (rc == 0) rc = bsqo_quantize_mx(a, M, K, fmt, codes, scales, s_global);
+    if (!act_out) free(a);
+    return rc;
 }
 
 /* ------------------------------------------------------------------------ */
