@@ -61,6 +61,7 @@ def load(path: str | None = None):
             "bsq_quantize_nvfp4": (i32, [vp, i64, i64, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_mxfp6_noalloc": (i32, [vp, i64, i64, i32, vp, vp, vp, vp]),
             "bsq_quantize_mxfp6_act": (i32, [vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
+            "bsq_quantize_mxfp6_containers": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_batch_workspace_bytes": (sz, []),
             "bsq_quantize_mxfp6_batch": (i32, [vp, i32, i32, vp, sz, vp]),
             "bsq_quantize_nvfp4_batch": (i32, [vp, i32, vp, sz, vp]),
@@ -121,6 +122,14 @@ def quantize_mxfp6_noalloc_(x, fmt, codes, scales, s_global, stream=None):
     M, K = x.shape
     _check("bsq_quantize_mxfp6_noalloc", load().bsq_quantize_mxfp6_noalloc(
         _p(x), M, K, fmt, _p(codes), _p(scales), _p(s_global), _stream(stream)))
+
+
+def quantize_mxfp6_containers_(x, fmt, codes, scales, s_global, workspace=None, stream=None):
+    """The MX quantizer with fp6 codes one per byte: codes [M, K]."""
+    M, K = x.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("bsq_quantize_mxfp6_containers", load().bsq_quantize_mxfp6_containers(
+        _p(x), M, K, fmt, _p(codes), _p(scales), _p(s_global), _p(workspace), ws_bytes, _stream(stream)))
 
 
 ACT_RELU2, ACT_SILU_MUL = 1, 2

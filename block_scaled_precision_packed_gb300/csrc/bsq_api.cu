@@ -125,6 +125,15 @@ bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt
     return quantize_mx_launch(x, M, K, fmt, codes, scales, s_global, workspace, workspace_bytes, stream);
 }
 
+bsq_status bsq_quantize_mxfp6_containers(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt fmt, uint8_t* codes,
+                                         uint8_t* scales, float* s_global, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+    if (!x || !codes || !scales || !s_global || (fmt != BSQ_E3M2 && fmt != BSQ_E2M3)) return BSQ_ERR_INVALID_ARG;
+    if (M < 1 || K < 32 || K % 32 || M >= kMaxDim || K >= kMaxDim) return BSQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return BSQ_ERR_MISALIGNED;
+    return quantize_mx_containers_launch(x, M, K, fmt, codes, scales, s_global, workspace, workspace_bytes, stream);
+}
+
 bsq_status bsq_quantize_mxfp6_act(const uint16_t* x, int64_t M, int64_t K, bsq_act act, bsq_mxfmt fmt,
                                   uint8_t* codes, uint8_t* scales, float* s_global, uint16_t* act_out,
                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {

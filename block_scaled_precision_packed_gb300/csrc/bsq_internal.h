@@ -52,6 +52,9 @@ bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, 
 bsq_status quantize_mx_act_launch(const uint16_t* x, int64_t M, int64_t K, int act, int fmt, uint8_t* codes,
                                   uint8_t* scales, float* s_global, uint16_t* act_out, void* ws, size_t ws_bytes,
                                   cudaStream_t s);
+bsq_status quantize_mx_containers_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, uint8_t* codes,
+                                         uint8_t* scales, float* s_global, void* ws, size_t ws_bytes,
+                                         cudaStream_t s);
 bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,
                                  float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t quantize_workspace_bytes(int64_t M, int64_t K);

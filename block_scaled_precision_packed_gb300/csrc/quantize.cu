@@ -178,7 +178,8 @@ __device__ __forceinline__ void mx_block_scale(uint32_t amax_bits, float gs, uin
 // All zero when inv == 0.  The conversion leaves each 6-bit code in its own
 // byte with the top two bits clear, so a pair p = c0 | c1<<8 compacts to
 // c0 | c1<<6 as p - (p>>8)*192, and disjoint fields combine by multiply-add.
-template <int FMT>
+// CONT: fp6 codes left one per byte (b12x fp6.py pack_32_byte_containers_to_4xu64).
+template <int FMT, bool CONT = false>
 __device__ __forceinline__ void mx_encode_words(const uint4 (&v)[4], float inv, uint32_t (&w)[8]) {
     if (inv == 0.0f) {
 #pragma unroll
@@ -193,7 +194,7 @@ __device__ __forceinline__ void mx_encode_words(const uint4 (&v)[4], float inv, 
         mul2_rn(bf16_lo(x2), bf16_hi(x2), inv, lo, hi);
         p[i] = cvt_x2<FMT>(lo, hi);
     }
-    if constexpr (FMT == kE4M3) {
+    if constexpr (FMT == kE4M3 || CONT) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) w[k] = p[2 * k] + (p[2 * k + 1] << 16);
     } else {
@@ -214,9 +215,9 @@ __device__ __forceinline__ void mx_encode_words(const uint4 (&v)[4], float inv, 
 }
 
 // Store one MX block's words at codes + row offset + block offset (24 or 32 bytes).
-template <int FMT>
+template <int FMT, bool CONT = false>
 __device__ __forceinline__ void mx_store_words(uint8_t* __restrict__ dst, const uint32_t (&w)[8]) {
-    if constexpr (FMT == kE4M3) {
+    if constexpr (FMT == kE4M3 || CONT) {
         reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
         reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
     } else {
@@ -255,7 +256,7 @@ __device__ __forceinline__ void nvfp4_encode_block(uint4 v0, uint4 v1, uint32_t 
 // gets the same work (+-1 block).  A block is 32 values = 64 contiguous bytes
 // (four 16-byte loads whose sectors the neighbouring lanes' loads share); the
 // block amax needs no shuffle and the scale math is done once per 32 values.
-template <int FMT, bool FUSED>
+template <int FMT, bool FUSED, bool CONT = false>
 __global__ void __launch_bounds__(kEncThreads)
 quant_mx_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint32_t* __restrict__ partial,
                 int n_partial, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
@@ -272,7 +273,7 @@ quant_mx_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint
     const int64_t cpd4 = pad_to(nb, 4) / 4;
     const uint32_t nbp = (uint32_t)pad_to(nb, 4);                 // block slots per row
     const uint32_t total = (uint32_t)pad_to(M, 128) * nbp;        // a multiple of 128
-    const int64_t row_bytes = FMT == kE4M3 ? K : 3 * K / 4;
+    const int64_t row_bytes = FMT == kE4M3 || CONT ? K : 3 * K / 4;
     const uint32_t stride = gridDim.x * blockDim.x;
 
     for (uint32_t gb = blockIdx.x * blockDim.x + threadIdx.x; gb < total; gb += stride) {
@@ -291,8 +292,9 @@ quant_mx_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint
         float inv;
         mx_block_scale<FMT>(absmax32_bits(v), gs, ue, inv);
         uint32_t w[8];
-        mx_encode_words<FMT>(v, inv, w);
-        if (valid) mx_store_words<FMT>(codes + (int64_t)r * row_bytes + (FMT == kE4M3 ? 32 : 24) * (int64_t)b, w);
+        mx_encode_words<FMT, CONT>(v, inv, w);
+        if (valid)
+            mx_store_words<FMT, CONT>(codes + (int64_t)r * row_bytes + (FMT == kE4M3 || CONT ? 32 : 24) * (int64_t)b, w);
         // four consecutive blocks' scale bytes (four consecutive lanes, the same
         // row: nbp % 4 == 0) -> one 32-bit store
         const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
@@ -1110,6 +1112,41 @@ bsq_status quantize_mx_act_launch(const uint16_t* x, int64_t M, int64_t K, int a
     default: BSQ_QACT(kE4M3);
     }
 #undef BSQ_QACT
+}
+
+// fp6 codes one per byte: the cluster launch for small tensors, else the amax
+// pass and the encode pass (the one-pass kernel writes packed codes only).
+bsq_status quantize_mx_containers_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, uint8_t* codes,
+                                         uint8_t* scales, float* s_global, void* ws, size_t ws_bytes,
+                                         cudaStream_t s) {
+    bsq_status st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
+    const bool fused = M * K <= kFusedMaxElems;
+    uint32_t* partial = static_cast<uint32_t*>(ws);
+    int n_partial = 0;
+    if (!fused) {
+        if (!ws || ws_bytes < quantize_workspace_bytes(M, K)) return BSQ_ERR_WORKSPACE;
+        if (!aligned16(ws)) return BSQ_ERR_MISALIGNED;
+        n_partial = amax_grid(info, M * K);
+        amax_partial_kernel<<<n_partial, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), M * K / 8, partial);
+        count_launch(BSQ_KERNEL_AMAX);
+        if (launch_status() != BSQ_OK) return BSQ_ERR_CUDA;
+    }
+    cudaError_t e;
+    const int grid = encode_grid(info, M, K);
+#define BSQ_QCONT(F)                                                                                            \
+    if (fused)                                                                                                  \
+        e = launch_cluster(quant_mx_kernel<F, true, true>, s, x, M, K, (const uint32_t*)nullptr, 0, codes, scales, \
+                           s_global);                                                                           \
+    else                                                                                                        \
+        e = launch_dependent(quant_mx_kernel<F, false, true>, grid, s, x, M, K, (const uint32_t*)partial,      \
+                             n_partial, codes, scales, s_global);
+    if (fmt == kE3M2) { BSQ_QCONT(kE3M2); } else { BSQ_QCONT(kE2M3); }
+#undef BSQ_QCONT
+    count_launch(fused ? BSQ_KERNEL_QUANT_SMALL : BSQ_KERNEL_QUANT_MX);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
+    return launch_status();
 }
 
 bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,

@@ -116,6 +116,20 @@ BSQ_API bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, b
                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * bsq_quantize_mxfp6_containers -- bsq_quantize_mxfp6 with fp6 byte-container
+ * output: b12x _lib/fp6.py quantize_block_fp6_e3m2_bytes / _e2m3_bytes with
+ * pack_32_byte_containers_to_4xu64 -- identical quantization, each 6-bit code
+ * in its own byte (bits [5:0], bits [7:6] zero), K order, instead of four codes
+ * in three bytes (the layout warp-level fp6 MMAs read without an expansion).
+ *   fmt      BSQ_E3M2 or BSQ_E2M3 only.
+ *   codes    [M, K] bytes; x, scales, s_global, workspace as bsq_quantize_mxfp6.
+ * Results are bit-identical to the CPU oracle.
+ */
+BSQ_API bsq_status bsq_quantize_mxfp6_containers(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt fmt,
+                                                 uint8_t* codes, uint8_t* scales, float* s_global,
+                                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * bsq_quantize_mxfp6_act -- fused activation + MX quantize.
  * b12x _lib/fp6.py: relu2_quantize_grouped_mxfp6_torch and
  * silu_mul_quantize_grouped_mxfp6_torch (one group): the activation is

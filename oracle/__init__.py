@@ -76,6 +76,7 @@ def _declare(L):
         "bsqo_gemv_nvfp4_at": (i, [p, p, p, d, i64, p, p, i64, p, p, i]),
         "bsqo_gemv_mx_at": (i, [p, p, i, p, d, i64, p, p, i64, p, p, i]),
         "bsqo_activate": (i, [p, i64, i64, i, p]),
+        "bsqo_quantize_mx_containers": (i, [p, i64, i64, i, p, p, p]),
         "bsqo_quantize_mx_act": (i, [p, i64, i64, i, i, p, p, p, p]),
         "bsqo_f32_to_bf16": (ctypes.c_uint16, [f]),
         "bsqo_double_to_bf16": (ctypes.c_uint16, [d]),
@@ -171,6 +172,18 @@ def quantize_mx(x_bf16: np.ndarray, fmt: int):
     scales = np.empty(scale_bytes(M, K // 32), dtype=np.uint8)
     g = np.zeros(1, dtype=np.float32)
     _check(lib().bsqo_quantize_mx(_ptr(x), M, K, fmt, _ptr(codes), _ptr(scales), _ptr(g)), "quantize_mx")
+    return codes, scales, float(g[0])
+
+
+def quantize_mx_containers(x_bf16: np.ndarray, fmt: int):
+    """The MX quantizer with fp6 codes one per byte: (codes [M, K], scales, s_global)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x.shape
+    codes = np.empty((M, K), dtype=np.uint8)
+    scales = np.empty(scale_bytes(M, K // 32), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    _check(lib().bsqo_quantize_mx_containers(_ptr(x), M, K, fmt, _ptr(codes), _ptr(scales), _ptr(g)),
+           "quantize_mx_containers")
     return codes, scales, float(g[0])
 
 

@@ -316,7 +316,7 @@ static float tensor_amax(const uint16_t* x, int64_t n) {
  * codes: [M, 3K/4] (fp6) or [M, K] (e4m3); scales: pad128(M)*pad4(K/32).    */
 /* One row of the MX quantizer: codes (packed row) and the row's UE8M0 bytes. */
 static void quantize_mx_row(const uint16_t* xr, int64_t K, int fmt, float gs,
-                            uint8_t* codes_row, uint8_t* ue_row) {
+                            uint8_t* codes_row, uint8_t* ue_row, int containers) {
     const float fmax = fmt_max(fmt);
     uint8_t blk[32];
     for (int64_t b = 0; b < K / 32; ++b) {
@@ -339,7 +339,7 @@ static void quantize_mx_row(const uint16_t* xr, int64_t K, int fmt, float gs,
                 blk[i] = (uint8_t)bsqo_encode(fmt, q);
             }
         }
-        if (fmt == FMT_E4M3) memcpy(codes_row + b * 32, blk, 32);
+        if (fmt == FMT_E4M3 || containers) memcpy(codes_row + b * 32, blk, 32);
         else bsqo_pack_fp6(blk, 32, codes_row + b * 24);
         ue_row[b] = (uint8_t)ue;
     }
@@ -373,7 +373,28 @@ BSQO_API int bsqo_quantize_mx(const uint16_t* x, int64_t M, int64_t K, int fmt,
     memset(scales, 0, (size_t)bsqo_scale_bytes(M, nb));
     uint8_t* ue_row = (uint8_t*)malloc((size_t)(nb > 0 ? nb : 1));
     for (int64_t r = 0; r < M; ++r) {
-        quantize_mx_row(x + r * K, K, fmt, gs, codes + r * row_bytes, ue_row);
+        quantize_mx_row(x + r * K, K, fmt, gs, codes + r * row_bytes, ue_row, 0);
+        for (int64_t b = 0; b < nb; ++b) scales[bsqo_swz_offset(r, b, nb)] = ue_row[b];
+    }
+    free(ue_row);
+    *s_global = gs != 0.0f ? 1.0f / gs : 0.0f;
+    return 0;
+}
+
+/* [P2] quantize_block_fp6_e3m2_bytes / _e2m3_bytes with
+ * pack_32_byte_containers_to_4xu64: the same quantizer, fp6 codes written one
+ * per byte (bits [5:0], bits [7:6] zero) in K order instead of four in three
+ * bytes.  codes: [M, K] bytes; scales and s_global as bsqo_quantize_mx.      */
+BSQO_API int bsqo_quantize_mx_containers(const uint16_t* x, int64_t M, int64_t K, int fmt,
+                                         uint8_t* codes, uint8_t* scales, float* s_global) {
+    if (fmt != FMT_E3M2 && fmt != FMT_E2M3) return 1;
+    if (M < 0 || K < 0 || K % 32) return 1;
+    const int64_t nb = K / 32;
+    const float gs = mx_global_scale(x, M * K, fmt);
+    memset(scales, 0, (size_t)bsqo_scale_bytes(M, nb));
+    uint8_t* ue_row = (uint8_t*)malloc((size_t)(nb > 0 ? nb : 1));
+    for (int64_t r = 0; r < M; ++r) {
+        quantize_mx_row(x + r * K, K, fmt, gs, codes + r * K, ue_row, 1);
         for (int64_t b = 0; b < nb; ++b) scales[bsqo_swz_offset(r, b, nb)] = ue_row[b];
     }
     free(ue_row);
@@ -391,7 +412,7 @@ BSQO_API int bsqo_quantize_mx_rows(const uint16_t* x, int64_t M, int64_t K, int 
     const int64_t row_bytes = fmt == FMT_E4M3 ? K : 3 * K / 4;
     const float gs = mx_global_scale(x, M * K, fmt);
     for (int64_t i = 0; i < n_rows; ++i)
-        quantize_mx_row(x + rows[i] * K, K, fmt, gs, codes + i * row_bytes, ue + i * (K / 32));
+        quantize_mx_row(x + rows[i] * K, K, fmt, gs, codes + i * row_bytes, ue + i * (K / 32), 0);
     *s_global = gs != 0.0f ? 1.0f / gs : 0.0f;
     return 0;
 }

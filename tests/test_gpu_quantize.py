@@ -218,3 +218,25 @@ def test_one_pass_accepts_any_workspace_contents(bsq, fill):
         assert np.array_equal(host_bytes(codes).reshape(oc.shape), oc)
         assert np.array_equal(host_bytes(scales), os_)
         assert np.float32(g.item()) == np.float32(og)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])                       # e3m2, e2m3
+@pytest.mark.parametrize("M,K", [(16, 4096), (3, 96), (1000, 2048), (129, 4160)])
+def test_quantize_byte_containers_bit_exact(bsq, fmt, M, K):
+    """bsq_quantize_mxfp6_containers: one fp6 code per byte, bit-identical to the
+    oracle and to the unpacked codes of the packed quantizer."""
+    x = S.normal_bf16((M, K), 0.02, 501 + M + K, outlier_frac=0.01)
+    xd = dev_tensor(x)
+    codes = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(bsq.scale_bytes(M, K // 32), dtype=torch.uint8, device="cuda")
+    sg = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(16, bsq.quantize_workspace_bytes(M, K)), dtype=torch.uint8, device="cuda")
+    bsq.quantize_mxfp6_containers_(xd, fmt, codes, scales, sg, ws)
+    torch.cuda.synchronize()
+    oc, osc, og = O.quantize_mx_containers(x, (O.E3M2, O.E2M3)[fmt])
+    assert np.array_equal(host_bytes(codes), oc)
+    assert np.array_equal(host_bytes(scales), osc)
+    assert float(sg.item()) == og
+    pc, _, _ = bsq.quantize_mxfp6(xd.view(torch.bfloat16), ("e3m2", "e2m3")[fmt])
+    torch.cuda.synchronize()
+    assert np.array_equal(O.unpack_fp6(host_bytes(pc), M * K), host_bytes(codes).ravel())

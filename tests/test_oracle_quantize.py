@@ -263,3 +263,16 @@ def test_ties_to_lower_rival_is_observable():
     mags = magnitudes(O.E3M2)
     a, b = mags[1], mags[2]                     # codes 1 (odd) and 2 (even)
     assert O.encode(O.E3M2, (a + b) / 2) == 2   # ties to even, not to the lower code
+
+
+@pytest.mark.parametrize("fmt", [O.E3M2, O.E2M3])
+def test_byte_container_output_is_the_unpacked_codes(fmt):
+    """b12x fp6.py quantize_block_fp6_*_bytes: identical quantization, one code
+    per byte (bits [5:0]) in K order instead of the 4-in-3 packing."""
+    x = S.normal_bf16((48, 320), 0.02, 77, outlier_frac=0.01)
+    c, s, g = O.quantize_mx_containers(x, fmt)
+    p, s2, g2 = O.quantize_mx(x, fmt)
+    assert c.shape == (48, 320)
+    assert not (c & 0xC0).any()
+    assert np.array_equal(c.ravel(), O.unpack_fp6(p, 48 * 320))
+    assert np.array_equal(s, s2) and g == g2
