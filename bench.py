@@ -70,14 +70,15 @@ def src_sha():
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel, workload):
+def traffic_for(kernel, workload, m=None):
     """DRAM bytes per launch from a committed ncu capture, if it was taken on
-    the kernel sources as they are now (else None)."""
+    the kernel sources as they are now (else None); m: the decode GEMV's rows."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    e = d.get(f"{kernel}@{workload}")
+    e = d.get(f"{kernel}@{workload}@M{m}") if m is not None else None
+    e = e or d.get(f"{kernel}@{workload}")
     if not e or e.get("src_sha") != src_sha():
         return None
     return e.get("bytes_per_launch")
@@ -363,7 +364,9 @@ def run_bsq(args, rank, world, dev_index):
         achieved, peak, ru = fl / dur_s / 1e12, tensor_peak(pkind, pk), "TFLOP/s"
     roof = {"bound": bound, "kernel": name, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": ru,
             "frac": round(achieved / peak, 4), "peak_source": pk["src"] + (" (burst)" if bound == "tensor" else ""),
-            "algorithmic": by if bound == "hbm" else fl, "traffic": traffic_for(name, args.workload),
+            "algorithmic": by if bound == "hbm" else fl,
+            "traffic": traffic_for(name, args.workload,
+                                   args.gemv_m if args.workload == "nvfp4_decode_gemv_Mx28672x8192" else None),
             "ms": round(float(mean_op[d]), 5)}
     per_op = {ops[j][0]: round(float(mean_op[j]) * 1e3, 2) for j in range(n_ops)}
 
@@ -393,10 +396,12 @@ def run_bsq(args, rank, world, dev_index):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     small_m = small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) \
         if args.workload == "w6a8_e4m3xe2m3_4096x14336x4096" else None
-    fused_act = fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) \
-        if args.workload == "mxfp6_e3m2_w6a6_128x4096x4096" else None
+    w6a6 = args.workload == "mxfp6_e3m2_w6a6_128x4096x4096"
+    fused_act = fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
+    containers = byte_container_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
     return dict(value=value, unit=unit, step_ms=step_ms, roofline=roof, per_op_us=per_op, e2e=e2e,
-                launches=launches, clocks=clk.summary(), wl=wl, small_m=small_m, fused_act=fused_act)
+                launches=launches, clocks=clk.summary(), wl=wl, small_m=small_m, fused_act=fused_act,
+                containers=containers)
 
 
 def graph_call_us(fn, stream, flush, flush_b, flush_sink, args):
@@ -445,6 +450,23 @@ def fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
         by = M * kin * 2 + M * 3 * K // 4 + bsq.scale_bytes(M, K // 32)
         out[name] = {"us": round(us, 2), "algorithmic_bytes": by, "GB/s": round(by / (us * 1e-6) / 1e9, 1)}
     return out
+
+
+def byte_container_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
+    """The W6A6 weight quantized with fp6 byte-container output
+    (bsq_quantize_mxfp6_containers): bf16 [N, K] -> e3m2 codes one per byte."""
+    import torch
+    from block_scaled_precision_packed_gb300 import bsq
+    N, K = wl.N, wl.K
+    codes = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    scales = torch.empty(bsq.scale_bytes(N, K // 32), dtype=torch.uint8, device=dev)
+    sg = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, bsq.quantize_workspace_bytes(N, K)), dtype=torch.uint8, device=dev)
+    us = graph_call_us(lambda s: bsq.quantize_mxfp6_containers_(wl.w, 0, codes, scales, sg, ws, s),
+                       stream, flush, flush_b, flush_sink, args)
+    by = N * K * 2 + N * K + bsq.scale_bytes(N, K // 32)
+    return {"N": N, "K": K, "format": "e3m2 byte containers, UE8M0 per 32", "us": round(us, 2),
+            "algorithmic_bytes": by, "GB/s": round(by / (us * 1e-6) / 1e9, 1)}
 
 
 def small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
@@ -623,6 +645,8 @@ def main():
         line["quantizer_small_m_us"] = r["small_m"]
     if r["fused_act"] is not None:
         line["fused_activation_quantizer"] = r["fused_act"]
+    if r["containers"] is not None:
+        line["byte_container_quantizer"] = r["containers"]
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
