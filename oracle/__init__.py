@@ -77,6 +77,7 @@ def _declare(L):
         "bsqo_gemv_mx_at": (i, [p, p, i, p, d, i64, p, p, i64, p, p, i]),
         "bsqo_activate": (i, [p, i64, i64, i, p]),
         "bsqo_quantize_mx_containers": (i, [p, i64, i64, i, p, p, p]),
+        "bsqo_quantize_grouped_mx": (i, [p, i64, i64, i64, p, p, i, p, p, p]),
         "bsqo_quantize_mx_act": (i, [p, i64, i64, i, i, p, p, p, p]),
         "bsqo_f32_to_bf16": (ctypes.c_uint16, [f]),
         "bsqo_double_to_bf16": (ctypes.c_uint16, [d]),
@@ -173,6 +174,41 @@ def quantize_mx(x_bf16: np.ndarray, fmt: int):
     g = np.zeros(1, dtype=np.float32)
     _check(lib().bsqo_quantize_mx(_ptr(x), M, K, fmt, _ptr(codes), _ptr(scales), _ptr(g)), "quantize_mx")
     return codes, scales, float(g[0])
+
+
+def quantize_grouped_mx(x_bf16: np.ndarray, row_counts, gs, fmt: int):
+    """Grouped MX quantizer (b12x fp6.py quantize_grouped_mxfp6_torch): x [G, R, C]
+    bf16, per-group row counts and global scales -> (codes [G, R, row_bytes]
+    group-major, scales [G, pad128(R)*pad4(C/32)], s_global [G] = 1/gs)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    G, R, C = x.shape
+    rc = np.ascontiguousarray(row_counts, dtype=np.int64)
+    g32 = np.ascontiguousarray(gs, dtype=np.float32)
+    row_bytes = C if fmt == E4M3 else 3 * C // 4
+    codes = np.empty((G, R, row_bytes), dtype=np.uint8)
+    scales = np.empty((G, scale_bytes(R, C // 32)), dtype=np.uint8)
+    sg = np.empty(G, dtype=np.float32)
+    _check(lib().bsqo_quantize_grouped_mx(_ptr(x), G, R, C, _ptr(rc), _ptr(g32), fmt, _ptr(codes), _ptr(scales),
+                                          _ptr(sg)), "quantize_grouped_mx")
+    return codes, scales, sg
+
+
+def gemm_grouped_mx(A, fa, sA, gA, W, fw, sW, gW, row_counts, K):
+    """Grouped product: for each group g, the plain product of its first
+    row_counts[g] A rows with its W: Y [G, R, N] and S (rows past the count 0)."""
+    G, R = A.shape[0], A.shape[1]
+    N = W.shape[1]
+    y = np.zeros((G, R, N))
+    S = np.zeros((G, R, N))
+    for g in range(G):
+        rc = int(row_counts[g])
+        if rc == 0:
+            continue
+        want, s = gemm_mx(np.ascontiguousarray(A[g, :rc]), fa, np.ascontiguousarray(sA[g]), float(gA[g]),
+                          np.ascontiguousarray(W[g]), fw, np.ascontiguousarray(sW[g]), float(gW[g]), rc, N, K)
+        y[g, :rc] = np.asarray(want).reshape(rc, N)
+        S[g, :rc] = np.asarray(s).reshape(rc, N)
+    return y, S
 
 
 def quantize_mx_containers(x_bf16: np.ndarray, fmt: int):

@@ -402,6 +402,39 @@ BSQO_API int bsqo_quantize_mx_containers(const uint16_t* x, int64_t M, int64_t K
     return 0;
 }
 
+/* [P2] quantize_grouped_mxfp6_torch (several groups) and
+ * as_grouped_mxfp6_scale_view: x [G, R, C] bf16; group g's first row_counts[g]
+ * rows are quantized with the group's own global scale gs[g] (given, as on the
+ * page -- not derived from an amax), rows past row_counts[g] are zero codes and
+ * zero scales.  codes: [G, R, row_bytes] group-major (the page stores
+ * [R, 3C/4, G]; codes_page[r, j, g] = codes[g, r, j]); scales: G consecutive
+ * swizzled buffers of pad128(R)*pad4(C/32) bytes (the page's 6-D view is this
+ * storage); s_global[g] = 1/gs[g] (0 if gs[g] == 0).                        */
+BSQO_API int bsqo_quantize_grouped_mx(const uint16_t* x, int64_t G, int64_t R, int64_t C,
+                                      const int64_t* row_counts, const float* gs, int fmt,
+                                      uint8_t* codes, uint8_t* scales, float* s_global) {
+    if (fmt != FMT_E3M2 && fmt != FMT_E2M3 && fmt != FMT_E4M3) return 1;
+    if (G < 1 || R < 1 || C < 32 || C % 32) return 1;
+    const int64_t nb = C / 32;
+    const int64_t row_bytes = fmt == FMT_E4M3 ? C : 3 * C / 4;
+    const int64_t sbytes = bsqo_scale_bytes(R, nb);
+    memset(codes, 0, (size_t)(G * R * row_bytes));
+    memset(scales, 0, (size_t)(G * sbytes));
+    uint8_t* ue_row = (uint8_t*)malloc((size_t)nb);
+    for (int64_t g = 0; g < G; ++g) {
+        const int64_t valid = row_counts[g] < 0 ? 0 : (row_counts[g] > R ? R : row_counts[g]);
+        for (int64_t r = 0; r < valid; ++r) {
+            quantize_mx_row(x + (g * R + r) * C, C, fmt, gs[g], codes + (g * R + r) * row_bytes, ue_row, 0);
+            for (int64_t b = 0; b < nb; ++b) scales[g * sbytes + bsqo_swz_offset(r, b, nb)] = ue_row[b];
+        }
+        volatile float inv = 0.0f;
+        if (gs[g] != 0.0f) inv = 1.0f / gs[g];
+        s_global[g] = inv;
+    }
+    free(ue_row);
+    return 0;
+}
+
 /* The same quantizer for a subset of rows (the tensor amax still spans all
  * M rows): codes [n_rows, row_bytes] and plain row-major scales [n_rows, K/32]. */
 BSQO_API int bsqo_quantize_mx_rows(const uint16_t* x, int64_t M, int64_t K, int fmt,
