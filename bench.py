@@ -399,9 +399,10 @@ def run_bsq(args, rank, world, dev_index):
     w6a6 = args.workload == "mxfp6_e3m2_w6a6_128x4096x4096"
     fused_act = fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
     containers = byte_container_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
+    grouped = grouped_moe_us(wl, dev, stream, flush, flush_b, flush_sink, args, peaks()) if w6a6 else None
     return dict(value=value, unit=unit, step_ms=step_ms, roofline=roof, per_op_us=per_op, e2e=e2e,
                 launches=launches, clocks=clk.summary(), wl=wl, small_m=small_m, fused_act=fused_act,
-                containers=containers)
+                containers=containers, grouped=grouped)
 
 
 def graph_call_us(fn, stream, flush, flush_b, flush_sink, args):
@@ -450,6 +451,46 @@ def fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
         by = M * kin * 2 + M * 3 * K // 4 + bsq.scale_bytes(M, K // 32)
         out[name] = {"us": round(us, 2), "algorithmic_bytes": by, "GB/s": round(by / (us * 1e-6) / 1e9, 1)}
     return out
+
+
+def grouped_moe_us(wl, dev, stream, flush, flush_b, flush_sink, args, pk):
+    """The W6A6 layer as 8 experts (grouped MoE layout): A [8, 512, 4096] with
+    seeded row counts (mean ~256 routed rows per expert), W [8, 4096, 4096],
+    both e3m2.  Times the grouped activation quantizer (per-expert global scales
+    given) and the grouped tcgen05 GEMM over all experts; TFLOP/s counts only the
+    routed rows."""
+    import torch
+    from block_scaled_precision_packed_gb300 import bsq, synthetic as S
+    G, R, N, K = 8, 512, wl.N, wl.K
+    rc = np.random.default_rng(wl.cfg["seed"] + 40).integers(64, 449, G).astype(np.int32)
+    rct = torch.from_numpy(rc).to(dev)
+    x = torch.from_numpy(S.normal_bf16((G * R, K), 1.0, wl.cfg["seed"] + 41).view(np.int16)).to(dev)
+    x = x.view(torch.bfloat16).view(G, R, K)
+    A = torch.empty((G, R, 3 * K // 4), dtype=torch.uint8, device=dev)
+    sA = torch.empty((G, bsq.scale_bytes(R, K // 32)), dtype=torch.uint8, device=dev)
+    gA = torch.empty(G, dtype=torch.float32, device=dev)
+    gsa = torch.full((G,), 12544.0 / 4.5, dtype=torch.float32, device=dev)
+    W = torch.empty((G, N, 3 * K // 4), dtype=torch.uint8, device=dev)
+    sW = torch.empty((G, bsq.scale_bytes(N, K // 32)), dtype=torch.uint8, device=dev)
+    gW = torch.empty(G, dtype=torch.float32, device=dev)
+    for g in range(G):                                  # weights: quantized once, outside the timing
+        wg = torch.from_numpy(S.normal_bf16((N, K), 0.02, wl.cfg["seed"] + 50 + g).view(np.int16)).to(dev)
+        wg = wg.view(torch.bfloat16).view(1, N, K)
+        gsw = torch.full((1,), 12544.0 / float(wg.float().abs().max()), dtype=torch.float32, device=dev)
+        bsq.quantize_grouped_mxfp6_(wg, torch.tensor([N], dtype=torch.int32, device=dev), gsw, 0, W[g:g + 1],
+                                    sW[g:g + 1], gW[g:g + 1])
+        del wg
+    Y = torch.empty((G, R, N), dtype=torch.bfloat16, device=dev)
+    q_us = graph_call_us(lambda s: bsq.quantize_grouped_mxfp6_(x, rct, gsa, 0, A, sA, gA, s),
+                         stream, flush, flush_b, flush_sink, args)
+    g_us = graph_call_us(lambda s: bsq.gemm_grouped_mxfp6_(A, 0, sA, gA, W, 0, sW, gW, rct, Y, G, R, N, K, s),
+                         stream, flush, flush_b, flush_sink, args)
+    flops = 2.0 * float(rc.sum()) * N * K
+    tf = flops / (g_us * 1e-6) / 1e12
+    peak = tensor_peak("fp8f6", pk)
+    return {"experts": G, "rows_per_expert": R, "routed_rows": [int(v) for v in rc], "N": N, "K": K,
+            "format": "e3m2 x e3m2, UE8M0 per 32", "quantize_us": round(q_us, 2), "gemm_us": round(g_us, 2),
+            "gemm_TFLOP/s": round(tf, 1), "gemm_frac_of_fp8f6_peak": round(tf / peak, 4)}
 
 
 def byte_container_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
@@ -647,6 +688,8 @@ def main():
         line["fused_activation_quantizer"] = r["fused_act"]
     if r["containers"] is not None:
         line["byte_container_quantizer"] = r["containers"]
+    if r["grouped"] is not None:
+        line["grouped_moe"] = r["grouped"]
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

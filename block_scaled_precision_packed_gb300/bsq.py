@@ -62,6 +62,9 @@ def load(path: str | None = None):
             "bsq_quantize_mxfp6_noalloc": (i32, [vp, i64, i64, i32, vp, vp, vp, vp]),
             "bsq_quantize_mxfp6_act": (i32, [vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
             "bsq_quantize_mxfp6_containers": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
+            "bsq_quantize_grouped_mxfp6": (i32, [vp, i64, i64, i64, vp, vp, i32, vp, vp, vp, vp]),
+            "bsq_gemm_grouped_mxfp6": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, i32, i64, i64, i64, i64,
+                                             vp]),
             "bsq_quantize_batch_workspace_bytes": (sz, []),
             "bsq_quantize_mxfp6_batch": (i32, [vp, i32, i32, vp, sz, vp]),
             "bsq_quantize_nvfp4_batch": (i32, [vp, i32, vp, sz, vp]),
@@ -122,6 +125,21 @@ def quantize_mxfp6_noalloc_(x, fmt, codes, scales, s_global, stream=None):
     M, K = x.shape
     _check("bsq_quantize_mxfp6_noalloc", load().bsq_quantize_mxfp6_noalloc(
         _p(x), M, K, fmt, _p(codes), _p(scales), _p(s_global), _stream(stream)))
+
+
+def quantize_grouped_mxfp6_(x, row_counts, gs, fmt, codes, scales, s_global, stream=None):
+    """Grouped MX quantize: x [G, R, C] bf16, row_counts [G] int32, gs [G] float."""
+    G, R, C = x.shape
+    _check("bsq_quantize_grouped_mxfp6", load().bsq_quantize_grouped_mxfp6(
+        _p(x), G, R, C, _p(row_counts), _p(gs), fmt, _p(codes), _p(scales), _p(s_global), _stream(stream)))
+
+
+def gemm_grouped_mxfp6_(A, fa, sA, gA, W, fw, sW, gW, row_counts, Y, G, R, N, K, stream=None):
+    """Grouped GEMM: Y [G, R, N] (fp32 or bf16) from grouped MX operands."""
+    out = 1 if Y.dtype == torch.bfloat16 else 0
+    _check("bsq_gemm_grouped_mxfp6", load().bsq_gemm_grouped_mxfp6(
+        _p(A), fa, _p(sA), _p(gA), _p(W), fw, _p(sW), _p(gW), _p(row_counts), _p(Y), out, G, R, N, K,
+        _stream(stream)))
 
 
 def quantize_mxfp6_containers_(x, fmt, codes, scales, s_global, workspace=None, stream=None):

@@ -125,6 +125,32 @@ bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt
     return quantize_mx_launch(x, M, K, fmt, codes, scales, s_global, workspace, workspace_bytes, stream);
 }
 
+bsq_status bsq_quantize_grouped_mxfp6(const uint16_t* x, int64_t G, int64_t R, int64_t C, const int32_t* row_counts,
+                                      const float* gs, bsq_mxfmt fmt, uint8_t* codes, uint8_t* scales,
+                                      float* s_global, cudaStream_t stream) {
+    if (!x || !row_counts || !gs || !codes || !scales || !s_global || !valid_mx(fmt)) return BSQ_ERR_INVALID_ARG;
+    if (G < 1 || R < 1 || C < 32 || C % 32 || G * R >= kMaxDim || C >= kMaxDim) return BSQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (reinterpret_cast<uintptr_t>(row_counts) & 3u) ||
+        (reinterpret_cast<uintptr_t>(gs) & 3u) || (reinterpret_cast<uintptr_t>(s_global) & 3u))
+        return BSQ_ERR_MISALIGNED;
+    return quantize_grouped_mx_launch(x, G, R, C, row_counts, gs, fmt, codes, scales, s_global, stream);
+}
+
+bsq_status bsq_gemm_grouped_mxfp6(const uint8_t* A, bsq_mxfmt fa, const uint8_t* sA, const float* gA, const uint8_t* W,
+                                  bsq_mxfmt fw, const uint8_t* sW, const float* gW, const int32_t* row_counts, void* Y,
+                                  bsq_outtype out, int64_t G, int64_t R, int64_t N, int64_t K, cudaStream_t stream) {
+    if (!A || !sA || !gA || !W || !sW || !gW || !row_counts || !Y || !valid_mx(fa) || !valid_mx(fw) || !valid_out(out))
+        return BSQ_ERR_INVALID_ARG;
+    if (G < 1 || G > 256 || R < 1 || N < 1 || K < 128 || K % 128 || G * R >= kMaxDim || G * N >= kMaxDim ||
+        K >= kMaxDim)
+        return BSQ_ERR_INVALID_ARG;
+    if (!aligned16(sA) || !aligned16(sW) || !aligned16(Y)) return BSQ_ERR_MISALIGNED;
+    if (!(fa == BSQ_E4M3 ? aligned16(A) : aligned32(A)) || !(fw == BSQ_E4M3 ? aligned16(W) : aligned32(W)))
+        return BSQ_ERR_MISALIGNED;
+    // every group's scale buffer (a multiple of 512 bytes) starts 16-byte aligned
+    return gemm_grouped_launch(A, fa, sA, gA, W, fw, sW, gW, row_counts, Y, out, G, R, N, K, false, stream);
+}
+
 bsq_status bsq_quantize_mxfp6_containers(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt fmt, uint8_t* codes,
                                          uint8_t* scales, float* s_global, void* workspace, size_t workspace_bytes,
                                          cudaStream_t stream) {

@@ -55,6 +55,9 @@ bsq_status quantize_mx_act_launch(const uint16_t* x, int64_t M, int64_t K, int a
 bsq_status quantize_mx_containers_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, uint8_t* codes,
                                          uint8_t* scales, float* s_global, void* ws, size_t ws_bytes,
                                          cudaStream_t s);
+bsq_status quantize_grouped_mx_launch(const uint16_t* x, int64_t G, int64_t R, int64_t C, const int32_t* row_counts,
+                                      const float* gs, int fmt, uint8_t* codes, uint8_t* scales, float* s_global,
+                                      cudaStream_t s);
 bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,
                                  float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t quantize_workspace_bytes(int64_t M, int64_t K);
@@ -65,6 +68,10 @@ bsq_status quantize_batch_launch(const QTensor* ts, int n, int fmt, void* ws, si
 bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA, const void* W, int fw,
                        const uint8_t* sW, const float* gW, void* Y, int out, int64_t M, int64_t N,
                        int64_t K, bool nvfp4, cudaStream_t s);
+
+bsq_status gemm_grouped_launch(const void* A, int fa, const uint8_t* sA, const float* gA, const void* W, int fw,
+                               const uint8_t* sW, const float* gW, const int32_t* row_counts, void* Y, int out,
+                               int64_t G, int64_t R, int64_t N, int64_t K, bool nvf4, cudaStream_t s);
 
 bsq_status gemv_launch(const uint16_t* x, const void* W, int fw, const uint8_t* sW, const float* gW, void* y,
                        int out, int64_t M, int64_t N, int64_t K, bool nvfp4, cudaStream_t s);

@@ -31,6 +31,12 @@
 //               block-scaled MMA reads), then releases the stage to the MMA
 //               warp.  A tcgen05.cp of an atom occupies the tensor pipe for
 //               about as long as a 128x256 MMA; these stores do not.
+// GROUPED (MoE experts, b12x fp6.py's grouped layout): A holds G groups of R
+// rows ([G*R, K]), W holds G weights of N rows ([G*N, K]), each with its own
+// swizzled scale buffer and global factor; group g contributes the first
+// row_counts[g] rows of its A.  The persistent CTAs walk the tiles of every
+// group (the per-group row-block counts, read from the device row counts, are
+// prefix-summed in shared memory at the start) and store only valid rows.
 // Every wait is bounded (2 s); a timeout records its site in the device error
 // word, drains the copies in flight, frees TMEM and returns.
 //
@@ -74,13 +80,18 @@ struct Cfg {
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 };
 
+constexpr int kMaxGroups = 256;
+
 struct GemmArgs {
     const uint8_t* sA;
     const uint8_t* sW;
-    const float* gA;
-    const float* gW;
+    const float* gA;           // grouped: [G]
+    const float* gW;           // grouped: [G]
     void* Y;
-    int64_t M, N, K;
+    int64_t M, N, K;           // grouped: M = R, the rows per group of A
+    const int32_t* row_counts; // grouped: [G] valid A rows per group
+    int64_t G;                 // groups (1 when not grouped)
+    int64_t sa_group, sw_group;   // grouped: bytes of one group's scale buffer
     int64_t cpd4;          // scale atoms along K per 128-row tile (pad4(blocks)/4)
     int out_bf16;
     uint32_t idesc;        // instruction descriptor without the scale-id fields
@@ -119,7 +130,7 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
 //            runs K stages [r*S/SPLIT, (r+1)*S/SPLIT), and the fp32 partial
 //            tiles are summed (rank order, deterministic) through distributed
 //            shared memory -- no workspace, no atomics.
-template <bool NVF4, int BN, int SPLIT>
+template <bool NVF4, int BN, int SPLIT, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const GemmArgs args) {
     using C = Cfg<NVF4, BN>;
@@ -149,6 +160,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int64_t ks_begin = nks_all * krank / SPLIT, ks_end = nks_all * (krank + 1) / SPLIT;
     const int64_t tile_first = SPLIT > 1 ? (int64_t)(blockIdx.x / SPLIT) : (int64_t)blockIdx.x;
     const int64_t tile_step = SPLIT > 1 ? num_tiles : (int64_t)gridDim.x;
+    static_assert(!GROUPED || SPLIT == 1, "grouped products are persistent, not split-K");
+    // grouped: mb_first[g] = row blocks of the groups before g (prefix sums)
+    __shared__ int32_t mb_first[GROUPED ? kMaxGroups + 1 : 1];
+    int64_t n_units = num_tiles, n_mt = num_mb;      // units: tiles; row-block count of the unit space
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -175,6 +190,38 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // the setup above overlaps the previous kernel; its outputs (A, W, their
     // scales and global factors) are read only after this
     pdl_wait();
+    if constexpr (GROUPED) {
+        if (threadIdx.x == 0) {
+            int32_t acc = 0;
+            for (int64_t g = 0; g < args.G; ++g) {
+                mb_first[g] = acc;
+                int64_t rc = args.row_counts[g];
+                rc = rc < 0 ? 0 : (rc > M ? M : rc);
+                acc += (int32_t)((rc + kBM - 1) / kBM);
+            }
+            mb_first[args.G] = acc;
+        }
+        __syncthreads();
+        n_mt = mb_first[args.G];
+        n_units = n_mt * num_nb;
+    }
+    // unit -> (group, row block within the group, column block)
+    auto unit_at = [&](int64_t u, int64_t& g, int64_t& mb, int64_t& nb) {
+        nb = u / n_mt;
+        const int64_t mt = u - nb * n_mt;
+        g = 0;
+        if constexpr (GROUPED) {
+            int64_t lo = 0, hi = args.G - 1;                 // the last g with mb_first[g] <= mt
+            while (lo < hi) {
+                const int64_t mid = (lo + hi + 1) >> 1;
+                if (mb_first[mid] <= mt) lo = mid; else hi = mid - 1;
+            }
+            g = lo;
+            mb = mt - mb_first[g];
+        } else {
+            mb = mt;
+        }
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -184,8 +231,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             uint32_t issued_parity[8] = {0};
             bool issued_any[8] = {false};
             bool ok = true;
-            for (int64_t tile = tile_first; tile < num_tiles && ok; tile += tile_step) {
-                const int64_t mb = tile % num_mb, nb = tile / num_mb;
+            for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
+                int64_t grp, mb, nb;
+                unit_at(tile, grp, mb, nb);
+                const int64_t a_row0 = grp * M + mb * kBM, w_row0 = grp * N + nb * BN;
+                const uint8_t* sa_base = args.sA + grp * args.sa_group;
+                const uint8_t* sw_base = args.sW + grp * args.sw_group;
                 for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
                     if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, args.err, abort_flag, kErrGemmProducer)) {
                         ok = false;
@@ -197,16 +248,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t fb = smem_u32(full + stage);
                     mbar_arrive_expect_tx(fb, bytes);
                     const int32_t kx = (int32_t)(ks * (NVF4 ? 128 : C::kStageK));   // bytes (nvfp4) / elements
-                    tma_load_2d(smem_u32(sA_st + stage * C::kABytes), &tmA, fb, kx, (int32_t)(mb * kBM));
-                    tma_load_2d(smem_u32(sB_st + stage * C::kBBytes), &tmW, fb, kx, (int32_t)(nb * BN));
-                    bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), args.sA + (mb * args.cpd4 + kg) * kAtom,
+                    tma_load_2d(smem_u32(sA_st + stage * C::kABytes), &tmA, fb, kx, (int32_t)a_row0);
+                    tma_load_2d(smem_u32(sB_st + stage * C::kBBytes), &tmW, fb, kx, (int32_t)w_row0);
+                    bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), sa_base + (mb * args.cpd4 + kg) * kAtom,
                               natoms * kAtom, fb);
 #pragma unroll
                     for (int rt = 0; rt < C::kRowTilesB; ++rt) {
                         int64_t wrt = nb * C::kRowTilesB + rt;
                         if (wrt >= rt_total) wrt = nb * C::kRowTilesB;    // rows beyond N: any finite scales
                         bulk_load(smem_u32(sSfb + stage * C::kSfbBytes + rt * C::kAtomsPerStage * kAtom),
-                                  args.sW + (wrt * args.cpd4 + kg) * kAtom, natoms * kAtom, fb);
+                                  sw_base + (wrt * args.cpd4 + kg) * kAtom, natoms * kAtom, fb);
                     }
                     issued_parity[stage] = phase;
                     issued_any[stage] = true;
@@ -234,7 +285,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int64_t tile = tile_first; tile < num_tiles && ok; tile += tile_step) {
+            for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
                 if (!mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, args.err, abort_flag, kErrGemmMma)) break;
                 tc_fence_after();
                 for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
@@ -287,7 +338,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int64_t tile = tile_first; tile < num_tiles && ok; tile += tile_step) {
+        for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
             for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
                 if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
                     ok = false;
@@ -349,11 +400,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 tc_fence_before();
             }
         }
-        for (int64_t tile = tile_first; tile < num_tiles && SPLIT == 1; tile += tile_step) {
-            const int64_t mb = tile % num_mb, nb = tile / num_mb;
+        for (int64_t tile = tile_first; tile < n_units && SPLIT == 1; tile += tile_step) {
+            int64_t grp, mb, nb;
+            unit_at(tile, grp, mb, nb);
             if (!mbar_wait(smem_u32(acc_full), acc_phase, args.err, abort_flag, kErrGemmEpilogue)) break;
             tc_fence_after();
-            const int64_t row = mb * kBM + 32 * q + lane;
+            const int64_t lrow = mb * kBM + 32 * q + lane;              // row within the group
+            int64_t rows_valid = M;
+            float fg = f;
+            if constexpr (GROUPED) {
+                const int64_t rc = args.row_counts[grp];
+                rows_valid = rc < 0 ? 0 : (rc > M ? M : rc);
+                fg = __fmul_rn(__ldg(args.gA + grp), __ldg(args.gW + grp));
+            }
+            const bool row_ok = lrow < rows_valid;
+            const int64_t row = grp * M + lrow;                         // output row
             if (args.out_bf16) {
                 // Drain the whole accumulator row into registers as bf16 pairs,
                 // hand TMEM back to the MMA warp, then store: the next tile's
@@ -366,13 +427,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     tc_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        packed[16 * c + e] = (uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r0[2 * e]), f)) |
-                                             ((uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r0[2 * e + 1]), f)) << 16);
+                        packed[16 * c + e] = (uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r0[2 * e]), fg)) |
+                                             ((uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r0[2 * e + 1]), fg)) << 16);
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(acc_empty));
                 acc_phase ^= 1;
-                if (row < M) {
+                if (row_ok) {
                     uint16_t* yr = static_cast<uint16_t*>(args.Y) + row * N + nb * BN + kHalf * half;
 #pragma unroll
                     for (int c = 0; c < kHalf / 32; ++c) {
@@ -399,7 +460,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kHalf * half + 32 * c), r);
                 tc_wait_ld();
                 const int64_t col0 = nb * BN + kHalf * half + 32 * c;
-                if (row < M && col0 < N) {
+                if (row_ok && col0 < N) {
                     if (args.out_bf16) {
                         uint16_t* yr = static_cast<uint16_t*>(args.Y) + row * N + col0;
                         if (vec && col0 + 32 <= N) {
@@ -408,15 +469,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                 uint32_t p[4];
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const float lo = __fmul_rn(__uint_as_float(r[8 * v + 2 * e]), f);
-                                    const float hi = __fmul_rn(__uint_as_float(r[8 * v + 2 * e + 1]), f);
+                                    const float lo = __fmul_rn(__uint_as_float(r[8 * v + 2 * e]), fg);
+                                    const float hi = __fmul_rn(__uint_as_float(r[8 * v + 2 * e + 1]), fg);
                                     p[e] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
                                 }
                                 *reinterpret_cast<uint4*>(yr + 8 * v) = make_uint4(p[0], p[1], p[2], p[3]);
                             }
                         } else {
                             for (int e = 0; e < 32 && col0 + e < N; ++e)
-                                yr[e] = f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[e]), f));
+                                yr[e] = f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[e]), fg));
                         }
                     } else {
                         float* yr = static_cast<float*>(args.Y) + row * N + col0;
@@ -424,12 +485,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
                             for (int v = 0; v < 8; ++v)
                                 *reinterpret_cast<float4*>(yr + 4 * v) =
-                                    make_float4(__fmul_rn(__uint_as_float(r[4 * v]), f),
-                                                __fmul_rn(__uint_as_float(r[4 * v + 1]), f),
-                                                __fmul_rn(__uint_as_float(r[4 * v + 2]), f),
-                                                __fmul_rn(__uint_as_float(r[4 * v + 3]), f));
+                                    make_float4(__fmul_rn(__uint_as_float(r[4 * v]), fg),
+                                                __fmul_rn(__uint_as_float(r[4 * v + 1]), fg),
+                                                __fmul_rn(__uint_as_float(r[4 * v + 2]), fg),
+                                                __fmul_rn(__uint_as_float(r[4 * v + 3]), fg));
                         } else {
-                            for (int e = 0; e < 32 && col0 + e < N; ++e) yr[e] = __fmul_rn(__uint_as_float(r[e]), f);
+                            for (int e = 0; e < 32 && col0 + e < N; ++e) yr[e] = __fmul_rn(__uint_as_float(r[e]), fg);
                         }
                     }
                 }
@@ -548,7 +609,7 @@ bool operand_map(CUtensorMap* map, const void* p, int fmt, bool nvf4, int64_t ro
                       (uint64_t)(3 * K / 4), 128, box_rows);
 }
 
-template <bool NVF4, int BN, int SPLIT>
+template <bool NVF4, int BN, int SPLIT, bool GROUPED = false>
 bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a,
                        cudaStream_t s) {
     using C = Cfg<NVF4, BN>;
@@ -557,8 +618,8 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
     std::call_once(flags[dev], [&] {
-        ok_dev[dev] = cudaFuncSetAttribute(gemm_kernel<NVF4, BN, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::kSmemBytes) == cudaSuccess;
+        ok_dev[dev] = cudaFuncSetAttribute(gemm_kernel<NVF4, BN, SPLIT, GROUPED>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) == cudaSuccess;
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
     const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
@@ -572,7 +633,10 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if constexpr (SPLIT == 1) {
+    if constexpr (GROUPED) {
+        // the tile count depends on the device row counts: one persistent CTA per SM
+        cfg.gridDim = dim3((unsigned)imin64(a.G * tiles, info->num_sms), 1, 1);
+    } else if constexpr (SPLIT == 1) {
         cfg.gridDim = dim3((unsigned)imin64(tiles, info->num_sms), 1, 1);
     } else {
         cfg.gridDim = dim3((unsigned)(tiles * SPLIT), 1, 1);
@@ -584,7 +648,7 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    if (cudaLaunchKernelEx(&cfg, gemm_kernel<NVF4, BN, SPLIT>, ta, tw, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, gemm_kernel<NVF4, BN, SPLIT, GROUPED>, ta, tw, a) != cudaSuccess) {
         (void)cudaGetLastError();
         return BSQ_ERR_CUDA;
     }
@@ -615,6 +679,7 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
     GemmArgs a;
     a.sA = sA; a.sW = sW; a.gA = gA; a.gW = gW; a.Y = Y;
     a.M = M; a.N = N; a.K = K;
+    a.row_counts = nullptr; a.G = 1; a.sa_group = 0; a.sw_group = 0;
     a.cpd4 = pad_to(K / (nvf4 ? 16 : 32), 4) / 4;
     a.out_bf16 = out == BSQ_OUT_BF16;
     a.idesc = make_idesc(nvf4, fa, fw, bn);
@@ -637,6 +702,39 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
         else if (split == 2) r = launch_gemm<false, 128, 2>(info, ta, tw, a, s);
         else r = launch_gemm<false, 128, 1>(info, ta, tw, a, s);
     }
+    count_launch(nvf4 ? BSQ_KERNEL_GEMM_NVFP4 : BSQ_KERNEL_GEMM_MX);
+    return r;
+}
+
+
+bsq_status gemm_grouped_launch(const void* A, int fa, const uint8_t* sA, const float* gA, const void* W, int fw,
+                               const uint8_t* sW, const float* gW, const int32_t* row_counts, void* Y, int out,
+                               int64_t G, int64_t R, int64_t N, int64_t K, bool nvf4, cudaStream_t s) {
+    bsq_status st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
+    // 256-wide W tiles when the groups' full row blocks would still give every SM one
+    const int64_t full256 = G * ((R + kBM - 1) / kBM) * ((N + 255) / 256);
+    const int bn = full256 >= info->num_sms ? 256 : 128;
+    CUtensorMap ta, tw;
+    if (!operand_map(&ta, A, fa, nvf4, G * R, K, kBM) || !operand_map(&tw, W, fw, nvf4, G * N, K, (uint32_t)bn))
+        return BSQ_ERR_CUDA;
+    const int64_t nblk = K / (nvf4 ? 16 : 32);
+    GemmArgs a;
+    a.sA = sA; a.sW = sW; a.gA = gA; a.gW = gW; a.Y = Y;
+    a.M = R; a.N = N; a.K = K;
+    a.row_counts = row_counts; a.G = G;
+    a.sa_group = pad_to(R, 128) * pad_to(nblk, 4);
+    a.sw_group = pad_to(N, 128) * pad_to(nblk, 4);
+    a.cpd4 = pad_to(nblk, 4) / 4;
+    a.out_bf16 = out == BSQ_OUT_BF16;
+    a.idesc = make_idesc(nvf4, fa, fw, bn);
+    a.err = info->err;
+    auto row_tx = [&](int f) { return (uint32_t)(nvf4 || f == kE4M3 ? 128 : 96); };
+    a.tx_ab = kBM * row_tx(fa) + (uint32_t)bn * row_tx(fw);
+    bsq_status r;
+    if (nvf4) r = bn == 256 ? launch_gemm<true, 256, 1, true>(info, ta, tw, a, s) : launch_gemm<true, 128, 1, true>(info, ta, tw, a, s);
+    else r = bn == 256 ? launch_gemm<false, 256, 1, true>(info, ta, tw, a, s) : launch_gemm<false, 128, 1, true>(info, ta, tw, a, s);
     count_launch(nvf4 ? BSQ_KERNEL_GEMM_NVFP4 : BSQ_KERNEL_GEMM_MX);
     return r;
 }

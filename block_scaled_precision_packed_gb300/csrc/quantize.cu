@@ -818,6 +818,54 @@ quant_mx_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const 
     }
 }
 
+// ------------------------------------------------------------- grouped ----
+// Grouped (MoE) MX quantizer (b12x _lib/fp6.py quantize_grouped_mxfp6_torch):
+// x [G, R, C]; group g's first row_counts[g] rows are quantized with the
+// caller's global scale gs[g] (no amax pass: the scale is given), the other
+// rows get zero codes and zero scales.  Codes are group-major [G, R, row_bytes]
+// and every group has its own swizzled scale buffer of pad128(R) x pad4(C/32)
+// bytes, so each group is an operand the (grouped) GEMM reads in place.  One
+// lane per 32-value block slot over all groups' padded grids.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+quant_grouped_mx_kernel(const uint16_t* __restrict__ x, int64_t G, int64_t R, int64_t C,
+                        const int32_t* __restrict__ row_counts, const float* __restrict__ gs_in,
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ s_global) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = C / 32, nbp = pad_to(nb, 4), cpd4 = nbp / 4;
+    const int64_t per_group = pad_to(R, 128) * nbp;           // = the group's scale bytes
+    const int64_t row_bytes = FMT == kE4M3 ? C : 3 * C / 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t gb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gb < G * per_group; gb += stride) {
+        const int64_t g = gb / per_group, rem = gb - g * per_group;
+        const int64_t r = rem / nbp, b = rem - r * nbp;
+        int64_t rc = __ldg(row_counts + g);
+        rc = rc < 0 ? 0 : (rc > R ? R : rc);
+        const float gs = __ldg(gs_in + g);
+        if (rem == 0) s_global[g] = gs != 0.0f ? __fdiv_rn(1.0f, gs) : 0.0f;
+        const bool live = r < rc && b < nb;
+        uint4 v[4];
+        if (live) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + ((g * R + r) * C + 32 * b));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
+        }
+        uint32_t ue;
+        float inv;
+        mx_block_scale<FMT>(absmax32_bits(v), gs, ue, inv);
+        if (!live) { ue = 0; inv = 0.0f; }
+        uint32_t w[8];
+        mx_encode_words<FMT>(v, inv, w);
+        if (r < R && b < nb) mx_store_words<FMT>(codes + (g * R + r) * row_bytes + (FMT == kE4M3 ? 32 : 24) * b, w);
+        const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
+                            (__shfl_down_sync(0xFFFFFFFFu, ue, 2) << 16) | (__shfl_down_sync(0xFFFFFFFFu, ue, 3) << 24);
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(scales + g * per_group + swz_offset(r, b, cpd4)) = s4;
+    }
+}
+
 // ------------------------------------------------------------ launching ----
 // One cluster of kFusedCluster CTAs (16 needs the non-portable opt-in; a
 // device that refuses it gets 8).
@@ -1146,6 +1194,26 @@ bsq_status quantize_mx_containers_launch(const uint16_t* x, int64_t M, int64_t K
 #undef BSQ_QCONT
     count_launch(fused ? BSQ_KERNEL_QUANT_SMALL : BSQ_KERNEL_QUANT_MX);
     if (e != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
+    return launch_status();
+}
+
+bsq_status quantize_grouped_mx_launch(const uint16_t* x, int64_t G, int64_t R, int64_t C, const int32_t* row_counts,
+                                      const float* gs, int fmt, uint8_t* codes, uint8_t* scales, float* s_global,
+                                      cudaStream_t s) {
+    bsq_status st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
+    const int64_t slots = G * pad_to(R, 128) * pad_to(C / 32, 4);
+    int64_t grid = (slots + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)info->num_sms * 8;
+    if (grid > cap) grid = cap;
+    if (fmt == kE3M2)
+        quant_grouped_mx_kernel<kE3M2><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global);
+    else if (fmt == kE2M3)
+        quant_grouped_mx_kernel<kE2M3><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global);
+    else
+        quant_grouped_mx_kernel<kE4M3><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global);
+    count_launch(BSQ_KERNEL_QUANT_MX);
     return launch_status();
 }
 

@@ -116,6 +116,49 @@ BSQ_API bsq_status bsq_quantize_mxfp6(const uint16_t* x, int64_t M, int64_t K, b
                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * bsq_quantize_grouped_mxfp6 -- grouped (MoE) MX quantize.
+ * b12x _lib/fp6.py quantize_grouped_mxfp6_torch and as_grouped_mxfp6_scale_view:
+ * group g's first row_counts[g] rows are quantized with the caller's global
+ * scale gs[g] (not derived from an amax: the page takes it as an argument):
+ * per 32-block ue = exact ceil of log2(fl(fl(amax_b*gs[g])/fmt_max)) + 127,
+ * inv = gs[g] * 2^(127-ue), code = cvt.rn.satfinite(fl(x * inv)); rows past
+ * row_counts[g] get zero codes and zero scales.
+ *   x          [G, R, C] bf16 (16-byte aligned), C % 32 == 0.
+ *   row_counts [G] int32 (device); values clamp to [0, R].
+ *   gs         [G] float (device): each group's global scale (codes ~ x*gs/scale).
+ *   codes      [G, R, row_bytes] bytes, group-major (row_bytes = 3C/4, or C for
+ *              e4m3).  The page's [R, 3C/4, G] order is codes transposed.
+ *   scales     G consecutive swizzled buffers of bsq_scale_bytes(R, C/32) bytes
+ *              (the storage under the page's 6-D grouped scale view).
+ *   s_global   [G] float (device): 1/gs[g] (0 if gs[g] == 0), the factor the
+ *              products multiply by.
+ * One launch, no workspace.  Results are bit-identical to the CPU oracle.
+ */
+BSQ_API bsq_status bsq_quantize_grouped_mxfp6(const uint16_t* x, int64_t G, int64_t R, int64_t C,
+                                              const int32_t* row_counts, const float* gs, bsq_mxfmt fmt,
+                                              uint8_t* codes, uint8_t* scales, float* s_global,
+                                              cudaStream_t stream);
+
+/*
+ * bsq_gemm_grouped_mxfp6 -- grouped block-scaled GEMM over experts: for every
+ * group g and row r < row_counts[g],
+ *   Y[g, r, n] = gA[g] * gW[g] * sum_k A[g, r, k] * W[g, n, k]
+ * with A and W in the grouped layouts of bsq_quantize_grouped_mxfp6 (A [G, R,
+ * K], W [G, N, K], each group its own swizzled scale buffer and factor); rows
+ * r >= row_counts[g] of Y are not written.  tcgen05 block-scaled MMA, one
+ * persistent launch over every group's tiles (the row counts are read on the
+ * device, so a routing step can produce them without a host round trip).
+ *   fa, fw     MX formats of A and W; K % 128 == 0; G <= 256.
+ *   gA, gW     [G] floats (device), e.g. the quantizers' s_global arrays.
+ *   Y          [G, R, N] fp32 or bf16.
+ * Tolerances as bsq_gemm_mxfp6 (fp32: 1e-5 * sum|a*w| per output).
+ */
+BSQ_API bsq_status bsq_gemm_grouped_mxfp6(const uint8_t* A, bsq_mxfmt fa, const uint8_t* sA, const float* gA,
+                                          const uint8_t* W, bsq_mxfmt fw, const uint8_t* sW, const float* gW,
+                                          const int32_t* row_counts, void* Y, bsq_outtype out, int64_t G,
+                                          int64_t R, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * bsq_quantize_mxfp6_containers -- bsq_quantize_mxfp6 with fp6 byte-container
  * output: b12x _lib/fp6.py quantize_block_fp6_e3m2_bytes / _e2m3_bytes with
  * pack_32_byte_containers_to_4xu64 -- identical quantization, each 6-bit code
