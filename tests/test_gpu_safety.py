@@ -130,6 +130,16 @@ def test_bad_arguments_return_status_and_launch_nothing(bsq):
     assert L.bsq_gemv_nvfp4(p(x), p(c), p(s), null, p(g), 1, 33, 8, 64, st) == 1             # M > 32
     assert L.bsq_gemm_nvfp4(p(c), p(s), null, p(c), p(s), null, p(g), 1, 4, 4, 96, st) == 1  # K % 64
     assert L.bsq_gemm_mxfp6(p(c), 0, p(s), null, p(c), 0, p(s), null, p(g), 1, 4, 4, 64, st) == 1  # K % 128
+    assert L.bsq_quantize_mxfp6_act(p(x), 4, 64, 3, 0, p(c), p(s), p(g), null, null, 0, st) == 1      # bad activation
+    assert L.bsq_quantize_mxfp6_act(p(x), 4, 48, 1, 0, p(c), p(s), p(g), null, null, 0, st) == 1      # K % 32
+    assert L.bsq_quantize_mxfp6_containers(p(x), 4, 64, 2, p(c), p(s), p(g), null, 0, st) == 1       # e4m3 has bytes
+    rc = torch.zeros(2, dtype=torch.int32, device="cuda")
+    assert L.bsq_quantize_grouped_mxfp6(p(x), 0, 2, 64, p(rc), p(g), 0, p(c), p(s), p(g), st) == 1   # G < 1
+    assert L.bsq_quantize_grouped_mxfp6(p(x), 2, 2, 64, null, p(g), 0, p(c), p(s), p(g), st) == 1    # no counts
+    assert L.bsq_gemm_grouped_mxfp6(p(c), 0, p(s), p(g), p(c), 0, p(s), p(g), p(rc), p(g), 0,
+                                    2, 2, 4, 64, st) == 1                                            # K % 128
+    assert L.bsq_gemm_grouped_mxfp6(p(c), 0, p(s), p(g), p(c), 0, p(s), p(g), p(rc), p(g), 0,
+                                    300, 2, 4, 128, st) == 1                                         # G > 256
     assert sum(bsq.launch_count(k) for k in bsq.KERNEL_IDS) == 0
 
 
