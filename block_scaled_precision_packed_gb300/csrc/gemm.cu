@@ -228,8 +228,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             // ------------------------------------------------ TMA producer --
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_parity[8] = {0};
-            bool issued_any[8] = {false};
+            uint32_t issued_parity = 0, issued_any = 0;   // bit s: stage s's last parity / ever issued
             bool ok = true;
             for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
                 int64_t grp, mb, nb;
@@ -259,17 +258,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         bulk_load(smem_u32(sSfb + stage * C::kSfbBytes + rt * C::kAtomsPerStage * kAtom),
                                   sw_base + (wrt * args.cpd4 + kg) * kAtom, natoms * kAtom, fb);
                     }
-                    issued_parity[stage] = phase;
-                    issued_any[stage] = true;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    issued_any |= 1u << stage;
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
                 }
             }
             if (*abort_flag) {
                 // drain: every copy issued must land before the CTA retires
                 for (int s = 0; s < C::kStages; ++s) {
-                    if (!issued_any[s]) continue;
+                    if (!((issued_any >> s) & 1u)) continue;
                     const uint64_t t0 = globaltimer();
-                    while (!mbar_try_wait(smem_u32(full + s), issued_parity[s]) && globaltimer() - t0 < kWaitLimitNs) {
+                    while (!mbar_try_wait(smem_u32(full + s), (issued_parity >> s) & 1u) && globaltimer() - t0 < kWaitLimitNs) {
                     }
                 }
             }
@@ -419,16 +418,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 // Drain the whole accumulator row into registers as bf16 pairs,
                 // hand TMEM back to the MMA warp, then store: the next tile's
                 // MMAs overlap these stores.
+                // (16 columns per TMEM load keeps the 256-wide tile's drain
+                // within the register budget)
                 uint32_t packed[kHalf / 2];
 #pragma unroll
-                for (int c = 0; c < kHalf / 32; ++c) {
-                    uint32_t r0[32];
-                    tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kHalf * half + 32 * c), r0);
+                for (int c = 0; c < kHalf / 16; ++c) {
+                    uint32_t r0[16];
+                    tc_ld_32x32b_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kHalf * half + 16 * c), r0);
                     tc_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        packed[16 * c + e] = (uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r0[2 * e]), fg)) |
-                                             ((uint32_t)f32_to_bf16_bits(__fmul_rn(__uint_as_float(r0[2 * e + 1]), fg)) << 16);
+                    for (int e = 0; e < 8; ++e)
+                        packed[8 * c + e] = f32x2_to_bf16x2_bits(__fmul_rn(__uint_as_float(r0[2 * e]), fg),
+                                                                __fmul_rn(__uint_as_float(r0[2 * e + 1]), fg));
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(acc_empty));
@@ -445,10 +446,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                     make_uint4(packed[16 * c + 4 * v], packed[16 * c + 4 * v + 1],
                                                packed[16 * c + 4 * v + 2], packed[16 * c + 4 * v + 3]);
                         } else {
+                            // ragged columns: constant register indices only
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (col0 + e < N)
-                                    yr[32 * c + e] = (uint16_t)(packed[16 * c + e / 2] >> (16 * (e & 1)));
+                            for (int e = 0; e < 16; ++e) {
+                                const uint32_t two = packed[16 * c + e];
+                                if (col0 + 2 * e < N) yr[32 * c + 2 * e] = (uint16_t)(two & 0xFFFFu);
+                                if (col0 + 2 * e + 1 < N) yr[32 * c + 2 * e + 1] = (uint16_t)(two >> 16);
+                            }
                         }
                     }
                 }
@@ -471,13 +475,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                 for (int e = 0; e < 4; ++e) {
                                     const float lo = __fmul_rn(__uint_as_float(r[8 * v + 2 * e]), fg);
                                     const float hi = __fmul_rn(__uint_as_float(r[8 * v + 2 * e + 1]), fg);
-                                    p[e] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+                                    p[e] = f32x2_to_bf16x2_bits(lo, hi);
                                 }
                                 *reinterpret_cast<uint4*>(yr + 8 * v) = make_uint4(p[0], p[1], p[2], p[3]);
                             }
                         } else {
-                            for (int e = 0; e < 32 && col0 + e < N; ++e)
-                                yr[e] = f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[e]), fg));
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (col0 + e < N) yr[e] = f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[e]), fg));
                         }
                     } else {
                         float* yr = static_cast<float*>(args.Y) + row * N + col0;
@@ -490,7 +495,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                                 __fmul_rn(__uint_as_float(r[4 * v + 2]), fg),
                                                 __fmul_rn(__uint_as_float(r[4 * v + 3]), fg));
                         } else {
-                            for (int e = 0; e < 32 && col0 + e < N; ++e) yr[e] = __fmul_rn(__uint_as_float(r[e]), fg);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (col0 + e < N) yr[e] = __fmul_rn(__uint_as_float(r[e]), fg);
                         }
                     }
                 }
@@ -544,8 +551,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 uint16_t* y = static_cast<uint16_t*>(args.Y) + row * N + col;
                 if (col + 4 <= N && (N % 4) == 0) {
                     *reinterpret_cast<uint2*>(y) =
-                        make_uint2((uint32_t)f32_to_bf16_bits(o[0]) | ((uint32_t)f32_to_bf16_bits(o[1]) << 16),
-                                   (uint32_t)f32_to_bf16_bits(o[2]) | ((uint32_t)f32_to_bf16_bits(o[3]) << 16));
+                        make_uint2(f32x2_to_bf16x2_bits(o[0], o[1]), f32x2_to_bf16x2_bits(o[2], o[3]));
                 } else {
                     for (int e = 0; e < 4 && col + e < N; ++e) y[e] = f32_to_bf16_bits(o[e]);
                 }
