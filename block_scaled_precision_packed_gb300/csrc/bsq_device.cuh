@@ -117,6 +117,14 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     return r;
 }
 
+// One 32-byte global store (a full sector; sm_100's 256-bit vector
+// store); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7) : "memory");
+}
+
 // two values, round to nearest even: lo in bits 0-15, hi in bits 16-31
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
     uint32_t r;

@@ -25,8 +25,10 @@
 //               gA*gW, convert; for bf16 output the whole tile is held in
 //               registers so TMEM is released before the stores start.
 //   warps 10-13 scale factors: one warp per TMEM lane quarter moves each
-//               landed stage's scale atoms from shared memory into the
-//               stage's TMEM scale columns with tcgen05.st (every quarter gets
+//               stage's scale atoms, as soon as they land (they are copied
+//               ahead of the operand tiles, on a barrier of their own), from
+//               shared memory into the stage's TMEM scale columns with
+//               tcgen05.st (every quarter gets
 //               the same 32 x 16-byte rows, the replicated layout the
 //               block-scaled MMA reads), then releases the stage to the MMA
 //               warp.  A tcgen05.cp of an atom occupies the tensor pipe for
@@ -78,6 +80,9 @@ struct Cfg {
     static constexpr int kSfColsPerStage = kSfaCols + kSfbCols;
     static_assert(BN + kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM budget");
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+    // barriers: full, empty, sf_full, sf_land per stage; acc_full, acc_empty,
+    // drain; the TMEM base and abort flag (one slot)
+    static_assert((4 * kStages + 4) * 8 <= 256, "barrier slots");
 };
 
 constexpr int kMaxGroups = 256;
@@ -149,6 +154,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(acc_full + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
     uint64_t* sf_full = acc_full + 4;                 // [kStages]: the stage's scales are in TMEM
+    uint64_t* sf_land = sf_full + C::kStages;         // [kStages]: the stage's scale atoms are in smem
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t M = args.M, N = args.N, K = args.K;
@@ -170,7 +176,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(smem_u32(full + s), 1);
             mbar_init(smem_u32(empty + s), 1);
         }
-        for (int s = 0; s < C::kStages; ++s) mbar_init(smem_u32(sf_full + s), 128);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(sf_full + s), 128);
+            mbar_init(smem_u32(sf_land + s), 1);
+        }
         mbar_init(smem_u32(acc_full), 1);
         mbar_init(smem_u32(acc_empty), kEpiThreads);
         mbar_init(smem_u32(drain), 1);
@@ -243,21 +252,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     }
                     const int64_t kg = ks * C::kAtomsPerStage;             // first scale atom along K
                     const int natoms = (int)imin64(C::kAtomsPerStage, args.cpd4 - kg);
-                    const uint32_t bytes = args.tx_ab + (uint32_t)natoms * kAtom * (1 + C::kRowTilesB);
-                    const uint32_t fb = smem_u32(full + stage);
-                    mbar_arrive_expect_tx(fb, bytes);
-                    const int32_t kx = (int32_t)(ks * (NVF4 ? 128 : C::kStageK));   // bytes (nvfp4) / elements
-                    tma_load_2d(smem_u32(sA_st + stage * C::kABytes), &tmA, fb, kx, (int32_t)a_row0);
-                    tma_load_2d(smem_u32(sB_st + stage * C::kBBytes), &tmW, fb, kx, (int32_t)w_row0);
+                    // The scale atoms go first, on their own barrier: the
+                    // scale-factor warps move them into TMEM while the
+                    // operand tiles are still in flight.
+                    const uint32_t lb = smem_u32(sf_land + stage);
+                    mbar_arrive_expect_tx(lb, (uint32_t)natoms * kAtom * (1 + C::kRowTilesB));
                     bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), sa_base + (mb * args.cpd4 + kg) * kAtom,
-                              natoms * kAtom, fb);
+                              natoms * kAtom, lb);
 #pragma unroll
                     for (int rt = 0; rt < C::kRowTilesB; ++rt) {
                         int64_t wrt = nb * C::kRowTilesB + rt;
                         if (wrt >= rt_total) wrt = nb * C::kRowTilesB;    // rows beyond N: any finite scales
                         bulk_load(smem_u32(sSfb + stage * C::kSfbBytes + rt * C::kAtomsPerStage * kAtom),
-                                  sw_base + (wrt * args.cpd4 + kg) * kAtom, natoms * kAtom, fb);
+                                  sw_base + (wrt * args.cpd4 + kg) * kAtom, natoms * kAtom, lb);
                     }
+                    const uint32_t fb = smem_u32(full + stage);
+                    mbar_arrive_expect_tx(fb, args.tx_ab);
+                    const int32_t kx = (int32_t)(ks * (NVF4 ? 128 : C::kStageK));   // bytes (nvfp4) / elements
+                    tma_load_2d(smem_u32(sA_st + stage * C::kABytes), &tmA, fb, kx, (int32_t)a_row0);
+                    tma_load_2d(smem_u32(sB_st + stage * C::kBBytes), &tmW, fb, kx, (int32_t)w_row0);
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     issued_any |= 1u << stage;
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -269,6 +282,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     if (!((issued_any >> s) & 1u)) continue;
                     const uint64_t t0 = globaltimer();
                     while (!mbar_try_wait(smem_u32(full + s), (issued_parity >> s) & 1u) && globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                    while (!mbar_try_wait(smem_u32(sf_land + s), (issued_parity >> s) & 1u) &&
+                           globaltimer() - t0 < kWaitLimitNs) {
                     }
                 }
             }
@@ -339,7 +355,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         bool ok = true;
         for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
             for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
-                if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
+                if (!mbar_wait(smem_u32(sf_land + stage), phase, args.err, abort_flag, kErrGemmMma)) {
                     ok = false;
                     break;
                 }
@@ -375,6 +391,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const float f = __fmul_rn(args.gA ? __ldg(args.gA) : 1.0f, args.gW ? __ldg(args.gW) : 1.0f);
         uint32_t acc_phase = 0;
         const bool vec = args.out_bf16 ? (N % 8 == 0) : (N % 4 == 0);
+        // Each thread writes one output row: 32-byte stores (whole sectors)
+        // halve the memory requests of 16-byte ones.
+        const bool vec32 = (N % (args.out_bf16 ? 16 : 8) == 0) && ((reinterpret_cast<uintptr_t>(args.Y) & 31) == 0);
         if constexpr (SPLIT > 1) {
             // Partial tile -> this CTA's shared memory (the operand ring is idle:
             // the single tile's last MMA has completed), then sum across the
@@ -434,7 +453,44 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 tc_fence_before();
                 mbar_arrive(smem_u32(acc_empty));
                 acc_phase ^= 1;
-                if (row_ok) {
+                if (vec32) {
+                    // Whole 128-byte lines: within each group of four lanes
+                    // (four consecutive rows) the 32-byte chunks are
+                    // transposed with two butterfly exchanges, so that lane i
+                    // of the group holds chunk i of 64 columns of each of the
+                    // four rows; one store then writes 8 rows x 128 bytes.
+                    const int gi = lane & 3;
+                    const int64_t lrow0 = mb * kBM + 32 * q + (lane & ~3);  // the group's first row (within the group)
+                    uint16_t* ybase = static_cast<uint16_t*>(args.Y) + (grp * M + lrow0) * N + nb * BN + kHalf * half;
+#pragma unroll
+                    for (int h = 0; h < kHalf / 64; ++h) {
+                        uint32_t* x = packed + 32 * h;                        // chunk j: x[8j .. 8j+7]
+#pragma unroll
+                        for (int j = 0; j < 4; j += 2) {                      // exchange with lane ^ 1
+#pragma unroll
+                            for (int w = 0; w < 8; ++w) {
+                                const uint32_t send = (gi & 1) ? x[8 * j + w] : x[8 * (j + 1) + w];
+                                const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+                                if (gi & 1) x[8 * j + w] = recv; else x[8 * (j + 1) + w] = recv;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {                         // exchange with lane ^ 2
+#pragma unroll
+                            for (int w = 0; w < 8; ++w) {
+                                const uint32_t send = (gi & 2) ? x[8 * j + w] : x[8 * (j + 2) + w];
+                                const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+                                if (gi & 2) x[8 * j + w] = recv; else x[8 * (j + 2) + w] = recv;
+                            }
+                        }
+                        const int64_t col = nb * BN + kHalf * half + 64 * h + 16 * gi;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)                           // row lrow0 + j, columns col .. col+15
+                            if (lrow0 + j < rows_valid && col + 16 <= N)
+                                st_global_v8(ybase + j * N + 64 * h + 16 * gi, x[8 * j], x[8 * j + 1], x[8 * j + 2],
+                                             x[8 * j + 3], x[8 * j + 4], x[8 * j + 5], x[8 * j + 6], x[8 * j + 7]);
+                    }
+                } else if (row_ok) {
                     uint16_t* yr = static_cast<uint16_t*>(args.Y) + row * N + nb * BN + kHalf * half;
 #pragma unroll
                     for (int c = 0; c < kHalf / 32; ++c) {
@@ -465,40 +521,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 tc_wait_ld();
                 const int64_t col0 = nb * BN + kHalf * half + 32 * c;
                 if (row_ok && col0 < N) {
-                    if (args.out_bf16) {
-                        uint16_t* yr = static_cast<uint16_t*>(args.Y) + row * N + col0;
-                        if (vec && col0 + 32 <= N) {
+                    // fp32 output (the bf16 case returned above)
+                    float* yr = static_cast<float*>(args.Y) + row * N + col0;
+                    float o[32];
 #pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                uint32_t p[4];
+                    for (int e = 0; e < 32; ++e) o[e] = __fmul_rn(__uint_as_float(r[e]), fg);
+                    if (vec32 && col0 + 32 <= N) {
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float lo = __fmul_rn(__uint_as_float(r[8 * v + 2 * e]), fg);
-                                    const float hi = __fmul_rn(__uint_as_float(r[8 * v + 2 * e + 1]), fg);
-                                    p[e] = f32x2_to_bf16x2_bits(lo, hi);
-                                }
-                                *reinterpret_cast<uint4*>(yr + 8 * v) = make_uint4(p[0], p[1], p[2], p[3]);
-                            }
-                        } else {
+                        for (int v = 0; v < 4; ++v)
+                            st_global_v8(yr + 8 * v, __float_as_uint(o[8 * v]), __float_as_uint(o[8 * v + 1]),
+                                         __float_as_uint(o[8 * v + 2]), __float_as_uint(o[8 * v + 3]),
+                                         __float_as_uint(o[8 * v + 4]), __float_as_uint(o[8 * v + 5]),
+                                         __float_as_uint(o[8 * v + 6]), __float_as_uint(o[8 * v + 7]));
+                    } else if (vec && col0 + 32 <= N) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (col0 + e < N) yr[e] = f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[e]), fg));
-                        }
+                        for (int v = 0; v < 8; ++v)
+                            *reinterpret_cast<float4*>(yr + 4 * v) = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
                     } else {
-                        float* yr = static_cast<float*>(args.Y) + row * N + col0;
-                        if (vec && col0 + 32 <= N) {
 #pragma unroll
-                            for (int v = 0; v < 8; ++v)
-                                *reinterpret_cast<float4*>(yr + 4 * v) =
-                                    make_float4(__fmul_rn(__uint_as_float(r[4 * v]), fg),
-                                                __fmul_rn(__uint_as_float(r[4 * v + 1]), fg),
-                                                __fmul_rn(__uint_as_float(r[4 * v + 2]), fg),
-                                                __fmul_rn(__uint_as_float(r[4 * v + 3]), fg));
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (col0 + e < N) yr[e] = __fmul_rn(__uint_as_float(r[e]), fg);
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            if (col0 + e < N) yr[e] = o[e];
                     }
                 }
             }

@@ -86,7 +86,7 @@ def test_gemv_mx(bsq, fmt, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (200, 333, 320), (1, 256, 64), (256, 512, 1024),
-                                   (384, 1024, 512), (130, 4096, 256)])
+                                   (384, 1024, 512), (130, 4096, 256), (200, 336, 256)])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 def test_gemm_nvfp4(bsq, M, N, K, out):
     A, sA = nvfp4_operand(M, K, 51 + M)
@@ -111,7 +111,7 @@ def test_gemm_mx(bsq, fa, fw, M, N, K):
         check_products(y, want, s, f"gemm_{fa}x{fw} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(1100, 4315, 256), (1024, 9728, 128)])
+@pytest.mark.parametrize("M,N,K", [(1100, 4315, 256), (1024, 9728, 128), (1100, 4400, 128)])
 def test_gemm_nvfp4_many_tiles(bsq, M, N, K):
     """At least one 256-wide tile per SM (the persistent 128 x 256 path) with
     several row blocks, an odd row-block count with a ragged last block, and a
@@ -126,15 +126,38 @@ def test_gemm_nvfp4_many_tiles(bsq, M, N, K):
     check_products(y, want, s, f"gemm_nvfp4 {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("fa,fw", [("e4m3", "e2m3"), ("e3m2", "e3m2")])
-def test_gemm_mx_many_tiles(bsq, fa, fw):
+@pytest.mark.parametrize("fa,fw,N,out", [("e4m3", "e2m3", 4315, torch.float32), ("e3m2", "e3m2", 4315, torch.float32),
+                                         ("e4m3", "e2m3", 4400, torch.bfloat16), ("e3m2", "e3m2", 4315, torch.bfloat16)])
+def test_gemm_mx_many_tiles(bsq, fa, fw, N, out):
     """The persistent 128 x 256 path for MX operands (fp6 W included) on a
-    ragged shape with more tiles than SMs; every output checked."""
-    M, N, K = 1100, 4315, 256
+    ragged shape with more tiles than SMs; every output checked.  N = 4400 (a
+    multiple of 16, not of the tile) takes the whole-line bf16 stores up to a
+    ragged column edge."""
+    M, K = 1100, 256
     A, sA, gA = mx_operand(M, K, fa, 95)
     W, sW, gW = mx_operand(N, K, fw, 97)
     y = bsq.gemm_mxfp6(dev_tensor(A), fa, dev_tensor(sA), torch.tensor([gA], device="cuda"),
                        dev_tensor(W), fw, dev_tensor(sW), torch.tensor([gW], device="cuda"), K,
-                       out_dtype=torch.float32)
+                       out_dtype=out)
     want, s = O.gemm_mx(A, MX[fa], sA, gA, W, MX[fw], sW, gW, M, N, K)
     check_products(y, want, s, f"gemm_{fa}x{fw} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_gemm_output_16_byte_aligned_only(bsq, out):
+    """Y 16-byte but not 32-byte aligned: the epilogue falls back from
+    32-byte stores to 16-byte ones; the words around Y are not touched."""
+    M, N, K = 1100, 4400, 128
+    A, sA = nvfp4_operand(M, K, 99)
+    W, sW = nvfp4_operand(N, K, 98)
+    gA = torch.tensor([0.5], device="cuda")
+    gW = torch.tensor([0.75], device="cuda")
+    pad = 16 // torch.tensor([], dtype=out).element_size()
+    buf = torch.full((M * N + 2 * pad,), 7.0, dtype=out, device="cuda")
+    Y = buf[pad:pad + M * N].view(M, N)
+    assert Y.data_ptr() % 32 == 16
+    bsq.gemm_nvfp4_(dev_tensor(A), dev_tensor(sA), gA, dev_tensor(W), dev_tensor(sW), gW, Y, M, N, K)
+    torch.cuda.synchronize()
+    want, s = O.gemm_nvfp4(A, sA, 0.5, W, sW, 0.75, M, N, K)
+    check_products(Y, want, s, f"gemm_nvfp4 {M}x{N}x{K}, Y at 16 mod 32")
+    assert (buf[:pad] == 7.0).all() and (buf[pad + M * N:] == 7.0).all()
