@@ -28,11 +28,14 @@
 //               stage's scale atoms, as soon as they land (they are copied
 //               ahead of the operand tiles, on a barrier of their own), from
 //               shared memory into the stage's TMEM scale columns with
-//               tcgen05.st (every quarter gets
-//               the same 32 x 16-byte rows, the replicated layout the
-//               block-scaled MMA reads), then releases the stage to the MMA
-//               warp.  A tcgen05.cp of an atom occupies the tensor pipe for
-//               about as long as a 128x256 MMA; these stores do not.
+//               tcgen05.st (every quarter gets the same 32 x 16-byte rows,
+//               the replicated layout the block-scaled MMA reads); once the
+//               stage's operand tiles have landed too, one arrival per warp
+//               releases it to the MMA thread, which so waits on a single
+//               barrier per stage (each wait is a fixed cost in the one
+//               thread that feeds the tensor pipe).  A tcgen05.cp of an atom
+//               occupies the tensor pipe for about as long as a 128x256 MMA;
+//               these stores do not.
 // GROUPED (MoE experts, b12x fp6.py's grouped layout): A holds G groups of R
 // rows ([G*R, K]), W holds G weights of N rows ([G*N, K]), each with its own
 // swizzled scale buffer and global factor; group g contributes the first
@@ -153,7 +156,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint64_t* drain = acc_full + 2;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(acc_full + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
-    uint64_t* sf_full = acc_full + 4;                 // [kStages]: the stage's scales are in TMEM
+    uint64_t* sf_full = acc_full + 4;                 // [kStages]: scales in TMEM and operands landed
     uint64_t* sf_land = sf_full + C::kStages;         // [kStages]: the stage's scale atoms are in smem
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,7 +180,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(smem_u32(empty + s), 1);
         }
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(sf_full + s), 128);
+            mbar_init(smem_u32(sf_full + s), 4);
             mbar_init(smem_u32(sf_land + s), 1);
         }
         mbar_init(smem_u32(acc_full), 1);
@@ -305,8 +308,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 tc_fence_after();
                 for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
                     // the stage's operands have landed and its scales are in TMEM
-                    if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma) ||
-                        !mbar_wait(smem_u32(sf_full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
+                    // one wait per stage: the scale-factor warps release the
+                    // stage once its scales are in TMEM and its tiles landed
+                    if (!mbar_wait(smem_u32(sf_full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
                         ok = false;
                         break;
                     }
@@ -379,7 +383,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 tc_st_cols(lane_base + sf_col + C::kSfaCols, rb);
                 tc_wait_st();
                 tc_fence_before();
-                mbar_arrive(smem_u32(sf_full + stage));
+                // relay the operand tiles' landing, so that the MMA thread
+                // waits on one barrier per stage
+                if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmMma)) {
+                    ok = false;
+                    break;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(sf_full + stage));
                 if (++stage == C::kStages) { stage = 0; phase ^= 1; }
             }
         }
