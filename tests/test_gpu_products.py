@@ -73,6 +73,22 @@ def test_gemv_nvfp4_activations_outside_f16(bsq, M):
         check_products(y, want, s, f"gemv_nvfp4 mixed chunks M{M}")
 
 
+@pytest.mark.parametrize("M", [17, 32])
+def test_gemv_nvfp4_tensor_core_many_tiles(bsq, M):
+    """The tensor-core decode product with more 128-row weight tiles than SMs
+    (two CTAs per SM) and a ragged last tile; activations outside f16 in one
+    256-wide K chunk take the bf16 decode in the same call."""
+    N, K = 2 * 152 * 128 + 100, 512
+    x = S.normal_bf16((M, K), 1.0, 50 + M)
+    x[:, 300] = 0x4B80          # > f16 max: that 256-wide chunk takes the bf16 decode
+    W, sc = nvfp4_operand(N, K, 52)
+    g = torch.tensor([0.625], device="cuda")
+    want, s = O.gemv_nvfp4(x, W, sc, 0.625, M, N, K)
+    for out in (torch.float32, torch.bfloat16):
+        y = bsq.gemv_nvfp4(dev_tensor(x), dev_tensor(W), dev_tensor(sc), g, K, out_dtype=out)
+        check_products(y, want, s, f"gemv_nvfp4 many tiles M{M}")
+
+
 @pytest.mark.parametrize("fmt", ["e3m2", "e2m3", "e4m3"])
 @pytest.mark.parametrize("M,N,K", [(1, 256, 256), (8, 300, 512), (32, 129, 384)])
 def test_gemv_mx(bsq, fmt, M, N, K):
