@@ -140,6 +140,27 @@ def test_quantize_mx_batch_bit_exact(bsq, name, fmt):
         assert np.float32(g.item()) == np.float32(og)
 
 
+@pytest.mark.parametrize("name,fmt", MX)
+def test_quantize_mx_batch_w6a6_size_bit_exact(bsq, name, fmt):
+    """The W6A6 step's batch at full size -- A [128, 4096] and W [4096, 4096]
+    (N(0, 0.02), 1% outliers x20) in one one-pass launch, rows a whole number of
+    4-block groups, so whole warps store their codes through shared memory --
+    every code, scale and global factor bit-exact."""
+    shapes = [(128, 4096), (4096, 4096)]
+    xs = [S.normal_bf16(sh, 0.02, 700 + i, outlier_frac=0.01, outlier_mult=20.0) for i, sh in enumerate(shapes)]
+    outs = [_mx_outputs(M, K, name) for M, K in shapes]
+    ws = torch.empty(bsq.quantize_batch_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    bsq.reset_launch_counts()
+    bsq.quantize_mxfp6_batch_([(dev_tensor(x),) + o for x, o in zip(xs, outs)], bsq.FMT_IDS[name], ws)
+    torch.cuda.synchronize()
+    assert bsq.launch_count("quant_mx") == 1 and bsq.launch_count("amax") == 0
+    for x, (codes, scales, g) in zip(xs, outs):
+        oc, os_, og = O.quantize_mx(x, fmt)
+        assert np.array_equal(host_bytes(codes).reshape(oc.shape), oc)
+        assert np.array_equal(host_bytes(scales), os_)
+        assert np.float32(g.item()) == np.float32(og)
+
+
 def test_quantize_nvfp4_batch_bit_exact(bsq):
     shapes = BATCH + [(7, 4096)]
     xs = [fixture(M, K, 600 + i, std=1.0) for i, (M, K) in enumerate(shapes)]
