@@ -400,9 +400,10 @@ def run_bsq(args, rank, world, dev_index):
     fused_act = fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
     containers = byte_container_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
     grouped = grouped_moe_us(wl, dev, stream, flush, flush_b, flush_sink, args, peaks()) if w6a6 else None
+    quant_a = fused_quant_a_gemm_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
     return dict(value=value, unit=unit, step_ms=step_ms, roofline=roof, per_op_us=per_op, e2e=e2e,
                 launches=launches, clocks=clk.summary(), wl=wl, small_m=small_m, fused_act=fused_act,
-                containers=containers, grouped=grouped)
+                containers=containers, grouped=grouped, quant_a=quant_a)
 
 
 def graph_call_us(fn, stream, flush, flush_b, flush_sink, args):
@@ -451,6 +452,37 @@ def fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
         by = M * kin * 2 + M * 3 * K // 4 + bsq.scale_bytes(M, K // 32)
         out[name] = {"us": round(us, 2), "algorithmic_bytes": by, "GB/s": round(by / (us * 1e-6) / 1e9, 1)}
     return out
+
+
+def fused_quant_a_gemm_us(wl, dev, stream, flush, flush_b, flush_sink, args):
+    """The W6A6 product with the activation quantizer fused into the GEMM
+    (bsq_gemm_mxfp6_quant_a: x bf16 [128, 4096] quantized to e3m2 inside the
+    GEMM against the e3m2 weight), beside the same product as two calls
+    (bsq_quantize_mxfp6 of x, then bsq_gemm_mxfp6); W is quantized beforehand."""
+    import torch
+    from block_scaled_precision_packed_gb300 import bsq, synthetic as S
+    M, N, K = wl.M, wl.N, wl.K
+    c = wl.cfg
+    x = S.normal_bf16((M, K), c["a_std"], c["seed"] + 30, outlier_frac=c["outlier_frac"], outlier_mult=c["outlier_mult"])
+    w = S.normal_bf16((N, K), c["w_std"], c["seed"] + 31, outlier_frac=c["outlier_frac"], outlier_mult=c["outlier_mult"])
+    xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    Wc, sW, gW = bsq.quantize_mxfp6(torch.from_numpy(w.view(np.int16)).to(dev).view(torch.bfloat16), "e3m2")
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    sg = torch.empty(1, dtype=torch.float32, device=dev)
+    wsq = torch.empty(bsq.gemm_quant_a_workspace_bytes(), dtype=torch.uint8, device=dev)
+    codes = torch.empty((M, 3 * K // 4), dtype=torch.uint8, device=dev)
+    scales = torch.empty(bsq.scale_bytes(M, K // 32), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(16, bsq.quantize_workspace_bytes(M, K)), dtype=torch.uint8, device=dev)
+    fused = graph_call_us(lambda s: bsq.gemm_mxfp6_quant_a_(xd, 0, Wc, 0, sW, gW, Y, sg, wsq, M, N, K, s),
+                          stream, flush, flush_b, flush_sink, args)
+
+    def two(s):
+        bsq.quantize_mxfp6_(xd, 0, codes, scales, sg, ws, s)
+        bsq.gemm_mxfp6_(codes, 0, scales, sg, Wc, 0, sW, gW, Y, M, N, K, s)
+    two_us = graph_call_us(two, stream, flush, flush_b, flush_sink, args)
+    return {"M": M, "N": N, "K": K, "format": "bf16 x -> e3m2 in the GEMM, e3m2 W", "fused_us": round(fused, 2),
+            "quantize_then_gemm_us": round(two_us, 2),
+            "TFLOP/s": round(2 * M * N * K / (fused * 1e-6) / 1e12, 1)}
 
 
 def grouped_moe_us(wl, dev, stream, flush, flush_b, flush_sink, args, pk):
@@ -690,6 +722,8 @@ def main():
         line["byte_container_quantizer"] = r["containers"]
     if r["grouped"] is not None:
         line["grouped_moe"] = r["grouped"]
+    if r["quant_a"] is not None:
+        line["gemm_with_fused_activation_quantizer"] = r["quant_a"]
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

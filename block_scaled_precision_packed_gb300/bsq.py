@@ -70,6 +70,8 @@ def load(path: str | None = None):
             "bsq_quantize_nvfp4_batch": (i32, [vp, i32, vp, sz, vp]),
             "bsq_gemm_nvfp4": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, vp]),
             "bsq_gemm_mxfp6": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, vp, i32, i64, i64, i64, vp]),
+            "bsq_gemm_quant_a_workspace_bytes": (sz, []),
+            "bsq_gemm_mxfp6_quant_a": (i32, [vp, i32, vp, i32, vp, vp, vp, i32, vp, i64, i64, i64, vp, sz, vp]),
             "bsq_gemv_nvfp4": (i32, [vp, vp, vp, vp, vp, i32, i64, i64, i64, vp]),
             "bsq_gemv_mxfp6": (i32, [vp, vp, i32, vp, vp, vp, i32, i64, i64, i64, vp]),
             "bsq_dequant_nvfp4": (i32, [vp, vp, vp, vp, i64, i64, vp]),
@@ -208,6 +210,20 @@ def gemm_mxfp6_(A, fa, sA, gA, W, fw, sW, gW, Y, M, N, K, stream=None):
         _p(A), fa, _p(sA), _p(gA), _p(W), fw, _p(sW), _p(gW), _p(Y), out, M, N, K, _stream(stream)))
 
 
+def gemm_quant_a_workspace_bytes() -> int:
+    return load().bsq_gemm_quant_a_workspace_bytes()
+
+
+def gemm_mxfp6_quant_a_(x, fa, W, fw, sW, gW, Y, s_global_a, workspace, M, N, K, stream=None):
+    """Y = gA*gW * quantize(x) W^T with x bf16 [M, K] quantized to fa inside the
+    GEMM; s_global_a (device float, or None) receives A's global factor."""
+    out = OUT_BF16 if Y.dtype == torch.bfloat16 else OUT_F32
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("bsq_gemm_mxfp6_quant_a", load().bsq_gemm_mxfp6_quant_a(
+        _p(x), fa, _p(W), fw, _p(sW), _p(gW), _p(Y), out, _p(s_global_a), M, N, K, _p(workspace), ws_bytes,
+        _stream(stream)))
+
+
 def gemv_nvfp4_(x, W, sW, gW, y, N, K, stream=None):
     M = x.shape[0]
     out = OUT_BF16 if y.dtype == torch.bfloat16 else OUT_F32
@@ -314,6 +330,19 @@ def gemm_mxfp6(A, fa, sA, gA, W, fw, sW, gW, K, out_dtype=torch.bfloat16):
     Y = torch.empty((M, N), dtype=out_dtype, device=A.device)
     gemm_mxfp6_(A, fa, sA, gA, W, fw, sW, gW, Y, M, N, K)
     return Y
+
+
+def gemm_mxfp6_quant_a(x, fa, W, fw, sW, gW, K, out_dtype=torch.bfloat16):
+    """(Y, s_global_a): the MX product with the activation quantizer in the GEMM."""
+    fa = FMT_IDS[fa] if isinstance(fa, str) else fa
+    fw = FMT_IDS[fw] if isinstance(fw, str) else fw
+    x = _bf16_bits(x)
+    M, N = x.shape[0], W.shape[0]
+    Y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    sg = torch.empty(1, dtype=torch.float32, device=x.device)
+    ws = torch.empty(gemm_quant_a_workspace_bytes(), dtype=torch.uint8, device=x.device)
+    gemm_mxfp6_quant_a_(x, fa, W, fw, sW, gW, Y, sg, ws, M, N, K)
+    return Y, sg
 
 
 def gemv_nvfp4(x, W, sW, gW, K, out_dtype=torch.bfloat16):

@@ -232,6 +232,23 @@ bsq_status bsq_gemm_mxfp6(const uint8_t* A, bsq_mxfmt fa, const uint8_t* sA, con
     return gemm_launch(A, fa, sA, gA, W, fw, sW, gW, Y, out, M, N, K, false, stream);
 }
 
+size_t bsq_gemm_quant_a_workspace_bytes(void) { return kAmaxPartialsBytes; }
+
+bsq_status bsq_gemm_mxfp6_quant_a(const uint16_t* x, bsq_mxfmt fa, const uint8_t* W, bsq_mxfmt fw,
+                                  const uint8_t* sW, const float* gW, void* Y, bsq_outtype out, float* s_global_a,
+                                  int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+    if (!x || !W || !sW || !Y || !valid_out(out) || !valid_mx(fa) || !valid_mx(fw)) return BSQ_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 128 || K % 128 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+        return BSQ_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kAmaxPartialsBytes) return BSQ_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(sW) || !aligned16(Y) || !aligned16(workspace)) return BSQ_ERR_MISALIGNED;
+    if (s_global_a && (reinterpret_cast<uintptr_t>(s_global_a) & 3u)) return BSQ_ERR_MISALIGNED;
+    if (!(fw == BSQ_E4M3 ? aligned16(W) : aligned32(W))) return BSQ_ERR_MISALIGNED;
+    return gemm_quant_a_launch(x, fa, W, fw, sW, gW, Y, out, s_global_a, M, N, K, static_cast<uint32_t*>(workspace),
+                               stream);
+}
+
 bsq_status bsq_gemv_nvfp4(const uint16_t* x, const uint32_t* W, const uint8_t* sW, const float* gW, void* y,
                           bsq_outtype out, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     if (!x || !W || !sW || !y || !valid_out(out)) return BSQ_ERR_INVALID_ARG;

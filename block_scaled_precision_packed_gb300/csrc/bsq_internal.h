@@ -61,6 +61,10 @@ bsq_status quantize_grouped_mx_launch(const uint16_t* x, int64_t G, int64_t R, i
 bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32_t* codes, uint8_t* scales,
                                  float* s_global, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t quantize_workspace_bytes(int64_t M, int64_t K);
+// The amax pass alone: per-CTA maxima of |x| (bf16 magnitude bits) over x [n]
+// into partial (at most kAmaxPartialsBytes); returns how many, or -1.
+constexpr size_t kAmaxPartialsBytes = 2048 * sizeof(uint32_t);
+int amax_partials_launch(const uint16_t* x, int64_t n, uint32_t* partial, cudaStream_t s);
 size_t quantize_batch_workspace_bytes();
 // fmt: a bsq_mxfmt, or kNvfp4
 bsq_status quantize_batch_launch(const QTensor* ts, int n, int fmt, void* ws, size_t ws_bytes, cudaStream_t s);
@@ -68,6 +72,12 @@ bsq_status quantize_batch_launch(const QTensor* ts, int n, int fmt, void* ws, si
 bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA, const void* W, int fw,
                        const uint8_t* sW, const float* gW, void* Y, int out, int64_t M, int64_t N,
                        int64_t K, bool nvfp4, cudaStream_t s);
+
+// GEMM whose bf16 activations are MX-quantized in the kernel (the amax pass,
+// then the GEMM); partial: kAmaxPartialsBytes of device scratch.
+bsq_status gemm_quant_a_launch(const uint16_t* x, int fa, const void* W, int fw, const uint8_t* sW, const float* gW,
+                               void* Y, int out, float* s_global_a, int64_t M, int64_t N, int64_t K, uint32_t* partial,
+                               cudaStream_t s);
 
 bsq_status gemm_grouped_launch(const void* A, int fa, const uint8_t* sA, const float* gA, const void* W, int fw,
                                const uint8_t* sW, const float* gW, const int32_t* row_counts, void* Y, int out,

@@ -53,6 +53,7 @@
 
 #include "bsq_device.cuh"
 #include "bsq_internal.h"
+#include "mx_encode.cuh"
 
 namespace bsq {
 namespace {
@@ -82,10 +83,10 @@ struct Cfg {
     static constexpr int kSfbCols = kRowTilesB * kAtomsPerStage * 4;
     static constexpr int kSfColsPerStage = kSfaCols + kSfbCols;
     static_assert(BN + kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM budget");
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-    // barriers: full, empty, sf_full, sf_land per stage; acc_full, acc_empty,
-    // drain; the TMEM base and abort flag (one slot)
-    static_assert((4 * kStages + 4) * 8 <= 256, "barrier slots");
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/;
+    // barriers: full, empty, sf_full, sf_land, a_ready per stage; acc_full,
+    // acc_empty, drain; the TMEM base and abort flag (one slot)
+    static_assert((5 * kStages + 4) * 8 <= 512, "barrier slots");
 };
 
 constexpr int kMaxGroups = 256;
@@ -103,8 +104,14 @@ struct GemmArgs {
     int64_t cpd4;          // scale atoms along K per 128-row tile (pad4(blocks)/4)
     int out_bf16;
     uint32_t idesc;        // instruction descriptor without the scale-id fields
-    uint32_t tx_ab;        // TMA transaction bytes of one stage's A and W tiles
+    uint32_t tx_ab;        // TMA transaction bytes of one stage's A and W tiles (W only when A is quantized here)
     uint32_t* err;
+    // A quantized in the kernel (QA >= 0): bf16 activations [M, K], the amax
+    // pass's partial maxima, and where to put A's s_global (may be null)
+    const uint16_t* qx;
+    const uint32_t* qpartial;
+    int qn_partial;
+    float* qs_global;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -126,6 +133,12 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
     return remote;
 }
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" :: "r"(addr), "h"(v) : "memory");
+}
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -138,7 +151,7 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
 //            runs K stages [r*S/SPLIT, (r+1)*S/SPLIT), and the fp32 partial
 //            tiles are summed (rank order, deterministic) through distributed
 //            shared memory -- no workspace, no atomics.
-template <bool NVF4, int BN, int SPLIT, bool GROUPED = false>
+template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const GemmArgs args) {
     using C = Cfg<NVF4, BN>;
@@ -158,6 +171,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
     uint64_t* sf_full = acc_full + 4;                 // [kStages]: scales in TMEM and operands landed
     uint64_t* sf_land = sf_full + C::kStages;         // [kStages]: the stage's scale atoms are in smem
+    uint64_t* a_ready = sf_land + C::kStages;         // [kStages] (QA): the stage's A tile and SFA atom are made
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t M = args.M, N = args.N, K = args.K;
@@ -170,6 +184,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int64_t tile_first = SPLIT > 1 ? (int64_t)(blockIdx.x / SPLIT) : (int64_t)blockIdx.x;
     const int64_t tile_step = SPLIT > 1 ? num_tiles : (int64_t)gridDim.x;
     static_assert(!GROUPED || SPLIT == 1, "grouped products are persistent, not split-K");
+    static_assert(QA < 0 || (!NVF4 && BN == 128 && !GROUPED), "in-kernel A quantization: MX, 128-wide tiles");
+    __shared__ uint32_t qa_red[QA >= 0 ? kThreads / 32 : 1];
     // grouped: mb_first[g] = row blocks of the groups before g (prefix sums)
     __shared__ int32_t mb_first[GROUPED ? kMaxGroups + 1 : 1];
     int64_t n_units = num_tiles, n_mt = num_mb;      // units: tiles; row-block count of the unit space
@@ -182,6 +198,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(sf_full + s), 4);
             mbar_init(smem_u32(sf_land + s), 1);
+            mbar_init(smem_u32(a_ready + s), kEpiThreads / 32);
         }
         mbar_init(smem_u32(acc_full), 1);
         mbar_init(smem_u32(acc_empty), kEpiThreads);
@@ -216,6 +233,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         __syncthreads();
         n_mt = mb_first[args.G];
         n_units = n_mt * num_nb;
+    }
+    // A quantized here: the tensor amax from the amax pass's partial maxima (every
+    // thread), then gs = 448 * fmt_max / amax and s_global = fl(1/gs), exactly as
+    // the quantizer computes them.
+    float gs_a = 0.0f, sg_a = 0.0f;
+    if constexpr (QA >= 0) {
+        uint32_t m = 0;
+        for (int i = threadIdx.x; i < args.qn_partial; i += kThreads) m = max(m, args.qpartial[i]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) qa_red[warp] = m;
+        __syncthreads();
+        m = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) m = max(m, qa_red[w]);
+        const float amax = bf16_bits_to_f32(m);
+        gs_a = amax > 0.0f ? __fdiv_rn(gs_numerator(QA), amax) : 0.0f;
+        sg_a = gs_a != 0.0f ? __fdiv_rn(1.0f, gs_a) : 0.0f;
+        if (blockIdx.x == 0 && threadIdx.x == 0 && args.qs_global) *args.qs_global = sg_a;
     }
     // unit -> (group, row block within the group, column block)
     auto unit_at = [&](int64_t u, int64_t& g, int64_t& mb, int64_t& nb) {
@@ -259,9 +295,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     // scale-factor warps move them into TMEM while the
                     // operand tiles are still in flight.
                     const uint32_t lb = smem_u32(sf_land + stage);
-                    mbar_arrive_expect_tx(lb, (uint32_t)natoms * kAtom * (1 + C::kRowTilesB));
-                    bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), sa_base + (mb * args.cpd4 + kg) * kAtom,
-                              natoms * kAtom, lb);
+                    mbar_arrive_expect_tx(lb, (uint32_t)natoms * kAtom * ((QA >= 0 ? 0 : 1) + C::kRowTilesB));
+                    if constexpr (QA < 0)          // else the epilogue warps make A and its scale atom
+                        bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), sa_base + (mb * args.cpd4 + kg) * kAtom,
+                                  natoms * kAtom, lb);
 #pragma unroll
                     for (int rt = 0; rt < C::kRowTilesB; ++rt) {
                         int64_t wrt = nb * C::kRowTilesB + rt;
@@ -272,7 +309,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t fb = smem_u32(full + stage);
                     mbar_arrive_expect_tx(fb, args.tx_ab);
                     const int32_t kx = (int32_t)(ks * (NVF4 ? 128 : C::kStageK));   // bytes (nvfp4) / elements
-                    tma_load_2d(smem_u32(sA_st + stage * C::kABytes), &tmA, fb, kx, (int32_t)a_row0);
+                    if constexpr (QA < 0)
+                        tma_load_2d(smem_u32(sA_st + stage * C::kABytes), &tmA, fb, kx, (int32_t)a_row0);
                     tma_load_2d(smem_u32(sB_st + stage * C::kBBytes), &tmW, fb, kx, (int32_t)w_row0);
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     issued_any |= 1u << stage;
@@ -359,7 +397,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         bool ok = true;
         for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
             for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
-                if (!mbar_wait(smem_u32(sf_land + stage), phase, args.err, abort_flag, kErrGemmMma)) {
+                if (!mbar_wait(smem_u32(sf_land + stage), phase, args.err, abort_flag, kErrGemmMma) ||
+                    (QA >= 0 && !mbar_wait(smem_u32(a_ready + stage), phase, args.err, abort_flag, kErrGemmMma))) {
                     ok = false;
                     break;
                 }
@@ -396,10 +435,85 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
     } else {
         // ------------------------------------------------------- epilogue --
+        if constexpr (QA >= 0) {
+            // First the A operand: each stage's 128 x 128 tile of A quantized from
+            // bf16 (the quantizer's block scale and encode) straight into the layout
+            // the tensor map would have produced -- row r's 16-code chunk c at
+            // (c ^ (r & 7)) * 16 (128-byte swizzle), an fp6 chunk as its 12 packed
+            // bytes and 4 zero bytes, an e4m3 chunk as 16 bytes -- and its UE8M0
+            // bytes into the stage's scale atom.  Thread (r, h) takes values
+            // [64h, 64h + 64) of row r of the stage: blocks 2h and 2h + 1.  Rows >= M
+            // and blocks past K get zero codes and zero scales, as the quantizer
+            // writes them.  One tile per CTA (the host launches no persistence).
+            const int et = (int)threadIdx.x - 64;
+            const int qr = et >> 1, qh = et & 1;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
+                int64_t grp, mb, nb;
+                unit_at(tile, grp, mb, nb);
+                const int64_t grow = mb * kBM + qr;
+                const uint16_t* xrow = args.qx + (grow < M ? grow : 0) * K;
+                // this thread's 64 values of stage ks (two blocks), zeros past M or K
+                auto load_x = [&](int64_t ks, uint4 (&v)[2][4]) {
+#pragma unroll
+                    for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int64_t k = ks * C::kStageK + 64 * qh + 32 * bl + 8 * j;
+                            v[bl][j] = grow < M && k < K ? __ldg(reinterpret_cast<const uint4*>(xrow + k))
+                                                         : make_uint4(0, 0, 0, 0);
+                        }
+                };
+                uint4 xv[2][4];
+                if (ks_begin < ks_end) load_x(ks_begin, xv);
+                for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
+                    // the next stage's x is in flight while this one is encoded
+                    uint4 xn[2][4];
+                    if (ks + 1 < ks_end) load_x(ks + 1, xn);
+                    // the stage's buffers are free once the MMAs that read them completed
+                    if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, args.err, abort_flag, kErrGemmEpilogue)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a_row = smem_u32(sA_st + stage * C::kABytes) + (uint32_t)qr * 128u;
+                    uint32_t ue2 = 0;
+#pragma unroll
+                    for (int bl = 0; bl < 2; ++bl) {
+                        uint32_t ue, w[8];
+                        float inv;
+                        mx_block_scale<QA>(absmax32_bits(xv[bl]), gs_a, ue, inv);
+                        mx_encode_words<QA>(xv[bl], inv, w);
+                        ue2 |= ue << (8 * bl);
+                        const uint32_t c = (uint32_t)(4 * qh + 2 * bl);       // first 16-code chunk of the block
+                        const uint32_t p0 = a_row + ((c ^ (uint32_t)(qr & 7)) << 4);
+                        const uint32_t p1 = a_row + (((c + 1) ^ (uint32_t)(qr & 7)) << 4);
+                        if constexpr (QA == kE4M3) {
+                            sts_v4(p0, w[0], w[1], w[2], w[3]);
+                            sts_v4(p1, w[4], w[5], w[6], w[7]);
+                        } else {
+                            sts_v4(p0, w[0], w[1], w[2], 0u);
+                            sts_v4(p1, w[3], w[4], w[5], 0u);
+                        }
+                    }
+                    sts_u16(smem_u32(sSfa + stage * C::kSfaBytes) + (uint32_t)((qr & 31) * 16 + ((qr >> 5) & 3) * 4 + 2 * qh),
+                            (uint16_t)ue2);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMA reads A via the async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(a_ready + stage));
+#pragma unroll
+                    for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) xv[bl][j] = xn[bl][j];
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const int half = (warp - 2) >> 2;             // which half of the tile's columns
         constexpr int kHalf = BN / 2;
-        const float f = __fmul_rn(args.gA ? __ldg(args.gA) : 1.0f, args.gW ? __ldg(args.gW) : 1.0f);
+        const float f = __fmul_rn(QA >= 0 ? sg_a : (args.gA ? __ldg(args.gA) : 1.0f), args.gW ? __ldg(args.gW) : 1.0f);
         uint32_t acc_phase = 0;
         const bool vec = args.out_bf16 ? (N % 8 == 0) : (N % 4 == 0);
         // Each thread writes one output row: 32-byte stores (whole sectors)
@@ -568,7 +682,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int64_t mb = tile % num_mb, nb = tile / num_mb;
         constexpr int kPitch = BN + 4;
         constexpr int kRows = kBM / SPLIT;
-        const float f = __fmul_rn(args.gA ? __ldg(args.gA) : 1.0f, args.gW ? __ldg(args.gW) : 1.0f);
+        const float f = __fmul_rn(QA >= 0 ? sg_a : (args.gA ? __ldg(args.gA) : 1.0f), args.gW ? __ldg(args.gW) : 1.0f);
         // Each thread owns up to kPer float4 groups of this rank's rows; every
         // rank's copy of all of them is requested before the first sum, so the
         // distributed-shared-memory latency is paid once.
@@ -668,7 +782,7 @@ bool operand_map(CUtensorMap* map, const void* p, int fmt, bool nvf4, int64_t ro
                       (uint64_t)(3 * K / 4), 128, box_rows);
 }
 
-template <bool NVF4, int BN, int SPLIT, bool GROUPED = false>
+template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1>
 bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a,
                        cudaStream_t s) {
     using C = Cfg<NVF4, BN>;
@@ -677,7 +791,7 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
     std::call_once(flags[dev], [&] {
-        ok_dev[dev] = cudaFuncSetAttribute(gemm_kernel<NVF4, BN, SPLIT, GROUPED>,
+        ok_dev[dev] = cudaFuncSetAttribute(gemm_kernel<NVF4, BN, SPLIT, GROUPED, QA>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) == cudaSuccess;
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
@@ -696,7 +810,8 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
         // the tile count depends on the device row counts: one persistent CTA per SM
         cfg.gridDim = dim3((unsigned)imin64(a.G * tiles, info->num_sms), 1, 1);
     } else if constexpr (SPLIT == 1) {
-        cfg.gridDim = dim3((unsigned)imin64(tiles, info->num_sms), 1, 1);
+        // in-kernel A quantization runs one tile per CTA (no persistence)
+        cfg.gridDim = dim3((unsigned)(QA >= 0 ? tiles : imin64(tiles, info->num_sms)), 1, 1);
     } else {
         cfg.gridDim = dim3((unsigned)(tiles * SPLIT), 1, 1);
         attr[na].id = cudaLaunchAttributeClusterDimension;
@@ -707,7 +822,7 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    if (cudaLaunchKernelEx(&cfg, gemm_kernel<NVF4, BN, SPLIT, GROUPED>, ta, tw, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, gemm_kernel<NVF4, BN, SPLIT, GROUPED, QA>, ta, tw, a) != cudaSuccess) {
         (void)cudaGetLastError();
         return BSQ_ERR_CUDA;
     }
@@ -739,6 +854,7 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
     a.sA = sA; a.sW = sW; a.gA = gA; a.gW = gW; a.Y = Y;
     a.M = M; a.N = N; a.K = K;
     a.row_counts = nullptr; a.G = 1; a.sa_group = 0; a.sw_group = 0;
+    a.qx = nullptr; a.qpartial = nullptr; a.qn_partial = 0; a.qs_global = nullptr;
     a.cpd4 = pad_to(K / (nvf4 ? 16 : 32), 4) / 4;
     a.out_bf16 = out == BSQ_OUT_BF16;
     a.idesc = make_idesc(nvf4, fa, fw, bn);
@@ -783,6 +899,7 @@ bsq_status gemm_grouped_launch(const void* A, int fa, const uint8_t* sA, const f
     a.sA = sA; a.sW = sW; a.gA = gA; a.gW = gW; a.Y = Y;
     a.M = R; a.N = N; a.K = K;
     a.row_counts = row_counts; a.G = G;
+    a.qx = nullptr; a.qpartial = nullptr; a.qn_partial = 0; a.qs_global = nullptr;
     a.sa_group = pad_to(R, 128) * pad_to(nblk, 4);
     a.sw_group = pad_to(N, 128) * pad_to(nblk, 4);
     a.cpd4 = pad_to(nblk, 4) / 4;
@@ -795,6 +912,50 @@ bsq_status gemm_grouped_launch(const void* A, int fa, const uint8_t* sA, const f
     if (nvf4) r = bn == 256 ? launch_gemm<true, 256, 1, true>(info, ta, tw, a, s) : launch_gemm<true, 128, 1, true>(info, ta, tw, a, s);
     else r = bn == 256 ? launch_gemm<false, 256, 1, true>(info, ta, tw, a, s) : launch_gemm<false, 128, 1, true>(info, ta, tw, a, s);
     count_launch(nvf4 ? BSQ_KERNEL_GEMM_NVFP4 : BSQ_KERNEL_GEMM_MX);
+    return r;
+}
+
+
+bsq_status gemm_quant_a_launch(const uint16_t* x, int fa, const void* W, int fw, const uint8_t* sW, const float* gW,
+                               void* Y, int out, float* s_global_a, int64_t M, int64_t N, int64_t K, uint32_t* partial,
+                               cudaStream_t s) {
+    bsq_status st;
+    const DeviceInfo* info = device_info(&st);
+    if (!info) return st;
+    // the amax pass over x, then the GEMM (a programmatic dependent launch that
+    // reduces the partial maxima before it quantizes A)
+    const int n_partial = amax_partials_launch(x, M * K, partial, s);
+    if (n_partial < 0) return BSQ_ERR_CUDA;
+    const int64_t tiles128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
+    const int64_t nks = (K + 127) / 128;
+    int split = 1;
+    for (int sp = 8; sp >= 2; sp /= 2)
+        if (tiles128 * sp <= info->num_sms && nks >= sp) { split = sp; break; }
+    CUtensorMap tw;
+    if (!operand_map(&tw, W, fw, false, N, K, 128u)) return BSQ_ERR_CUDA;
+    GemmArgs a;
+    a.sA = nullptr; a.sW = sW; a.gA = nullptr; a.gW = gW; a.Y = Y;
+    a.M = M; a.N = N; a.K = K;
+    a.row_counts = nullptr; a.G = 1; a.sa_group = 0; a.sw_group = 0;
+    a.qx = x; a.qpartial = partial; a.qn_partial = n_partial; a.qs_global = s_global_a;
+    a.cpd4 = pad_to(K / 32, 4) / 4;
+    a.out_bf16 = out == BSQ_OUT_BF16;
+    a.idesc = make_idesc(false, fa, fw, 128);
+    a.err = info->err;
+    a.tx_ab = 128u * (fw == kE4M3 ? 128u : 96u);          // the W tile only
+    bsq_status r;
+#define BSQ_QA_SPLITS(F)                                                            \
+    if (split == 8) r = launch_gemm<false, 128, 8, false, F>(info, tw, tw, a, s);   \
+    else if (split == 4) r = launch_gemm<false, 128, 4, false, F>(info, tw, tw, a, s); \
+    else if (split == 2) r = launch_gemm<false, 128, 2, false, F>(info, tw, tw, a, s); \
+    else r = launch_gemm<false, 128, 1, false, F>(info, tw, tw, a, s);
+    switch (fa) {
+    case kE3M2: BSQ_QA_SPLITS(kE3M2); break;
+    case kE2M3: BSQ_QA_SPLITS(kE2M3); break;
+    default: BSQ_QA_SPLITS(kE4M3); break;
+    }
+#undef BSQ_QA_SPLITS
+    count_launch(BSQ_KERNEL_GEMM_MX);
     return r;
 }
 

@@ -290,6 +290,32 @@ BSQ_API bsq_status bsq_gemm_mxfp6(const uint8_t* A, bsq_mxfmt fa, const uint8_t*
                           cudaStream_t stream);
 
 /*
+ * bsq_gemm_mxfp6_quant_a -- the MX product with the activation quantizer fused
+ * into the GEMM (b12x fp6.py, the _containers quantize-then-MMA variants:
+ * bf16 activations quantized in the kernel straight into the operand layout).
+ * Two launches on `stream`: an amax pass over x (per-CTA maxima into the
+ * workspace), then the GEMM, which reduces those maxima to A's global scale
+ * gs = 448 * fmt_max / amax and, per 128 x 128 stage of A, computes the UE8M0
+ * block scales and codes exactly as bsq_quantize_mxfp6 does and writes them
+ * into shared memory for the tensor cores; A's codes never reach global memory.
+ * Y equals, bit for bit, bsq_quantize_mxfp6(x, fa) followed by bsq_gemm_mxfp6
+ * whenever that GEMM also runs 128-wide tiles (M*N small enough that 256-wide
+ * tiles would not give every SM one).
+ *   x          [M, K] bf16 activations, 16-byte aligned; fa e3m2, e2m3 or e4m3.
+ *   W, fw, sW, gW  as for bsq_gemm_mxfp6.
+ *   s_global_a device float receiving A's s_global = 1/gs (NULL: not stored).
+ *   workspace  >= bsq_gemm_quant_a_workspace_bytes() bytes, 16-byte aligned,
+ *              caller-owned scratch (contents on entry do not matter).
+ *   K % 128 == 0; M, N >= 1.  Errors: BSQ_ERR_INVALID_ARG, BSQ_ERR_MISALIGNED,
+ *   BSQ_ERR_WORKSPACE, BSQ_ERR_CUDA.
+ */
+BSQ_API size_t bsq_gemm_quant_a_workspace_bytes(void);
+BSQ_API bsq_status bsq_gemm_mxfp6_quant_a(const uint16_t* x, bsq_mxfmt fa, const uint8_t* W, bsq_mxfmt fw,
+                          const uint8_t* sW, const float* gW, void* Y, bsq_outtype out, float* s_global_a,
+                          int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+/*
  * bsq_gemv_nvfp4 -- decode product y = gW * x W^T with bf16 activations and an
  * nvfp4 weight (cubecl-tile packed.rs, packed_one_row_product: one activation
  * row, or a few, against packed weights streamed from HBM).

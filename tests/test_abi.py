@@ -45,6 +45,7 @@ def test_host_helpers(lib):
     assert bsq.quantize_workspace_bytes(16, 4096) == 0
     assert bsq.quantize_workspace_bytes(4096, 4096) >= 1024
     assert bsq.quantize_batch_workspace_bytes() >= 4 * (1 + 1024)   # counter + a partial per CTA
+    assert bsq.gemm_quant_a_workspace_bytes() >= 4 * 2048          # the amax pass's partial maxima
 
 
 def test_oracle_and_library_share_nothing():

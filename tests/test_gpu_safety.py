@@ -140,6 +140,15 @@ def test_bad_arguments_return_status_and_launch_nothing(bsq):
                                     2, 2, 4, 64, st) == 1                                            # K % 128
     assert L.bsq_gemm_grouped_mxfp6(p(c), 0, p(s), p(g), p(c), 0, p(s), p(g), p(rc), p(g), 0,
                                     300, 2, 4, 128, st) == 1                                         # G > 256
+    xa = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(bsq.gemm_quant_a_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    wsb = ws.numel()
+    assert L.bsq_gemm_mxfp6_quant_a(null, 0, p(c), 0, p(s), null, p(g), 1, null, 4, 4, 128, p(ws), wsb, st) == 1  # null x
+    assert L.bsq_gemm_mxfp6_quant_a(p(xa), 0, p(c), 0, p(s), null, p(g), 1, null, 4, 4, 64, p(ws), wsb, st) == 1  # K % 128
+    assert L.bsq_gemm_mxfp6_quant_a(p(xa), 0, p(c), 0, p(s), null, p(g), 1, null, 4, 4, 128, p(ws), 64, st) == 4  # small ws
+    assert L.bsq_gemm_mxfp6_quant_a(p(xa), 0, p(c), 0, p(s), null, p(g), 1, null, 4, 4, 128, null, wsb, st) == 4  # no ws
+    assert L.bsq_gemm_mxfp6_quant_a(ctypes.c_void_p(xa.data_ptr() + 2), 0, p(c), 0, p(s), null, p(g), 1, null,
+                                    4, 4, 128, p(ws), wsb, st) == 3                                               # x misaligned
     assert sum(bsq.launch_count(k) for k in bsq.KERNEL_IDS) == 0
 
 
