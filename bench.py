@@ -215,7 +215,8 @@ class Workload:
             w = S.normal_bf16((N, K), cfg["w_std"], cfg["seed"] + 2)
             self.ca, self.sa, self.ga = bsq.quantize_nvfp4(t(a).view(torch.bfloat16))
             self.cw, self.sw, self.gw = bsq.quantize_nvfp4(t(w).view(torch.bfloat16))
-            self.host_in = {}
+            # end to end: the quantized operands (codes, scales, global factors) come from the host
+            self.host_in = operand_host_copies(self, ("ca", "sa", "ga", "cw", "sw", "gw"))
             self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             self.flops = 2.0 * M * N * K
             by = (M + N) * K // 2 + bsq.scale_bytes(M, K // 16) + bsq.scale_bytes(N, K // 16) + M * N * 2
@@ -230,7 +231,7 @@ class Workload:
             w = S.normal_bf16((N, K), cfg["w_std"], cfg["seed"] + 2)
             self.ca, self.sa, self.ga = bsq.quantize_mxfp6(t(a).view(torch.bfloat16), "e4m3")
             self.cw, self.sw, self.gw = bsq.quantize_mxfp6(t(w).view(torch.bfloat16), "e2m3")
-            self.host_in = {}
+            self.host_in = operand_host_copies(self, ("ca", "sa", "ga", "cw", "sw", "gw"))
             self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             self.flops = 2.0 * M * N * K
             by = M * K + N * 3 * K // 4 + bsq.scale_bytes(M, K // 32) + bsq.scale_bytes(N, K // 32) + M * N * 2
@@ -247,6 +248,12 @@ class Workload:
     def step(self, stream):
         for _, fn, *_ in self._ops:
             fn(stream)
+
+
+def operand_host_copies(wl, names):
+    """Host copies of a product workload's device operands (raw bytes), for
+    the end-to-end arm, which copies them in from pinned host memory every step."""
+    return {n: getattr(wl, n).contiguous().view(-1).cpu().numpy().view(np.uint8) for n in names}
 
 
 def max_over_ranks(ms, dist, device):
@@ -373,8 +380,10 @@ def run_bsq(args, rank, world, dev_index):
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if wl.host_in:
-        pinned = {k: torch.from_numpy(v.view(np.int16)).pin_memory() for k, v in wl.host_in.items()}
-        dst = {k: getattr(wl, k).view(torch.int16) for k in pinned}
+        # flat 16-bit views of both sides (any operand dtype of even byte size)
+        pinned = {k: torch.from_numpy(np.ascontiguousarray(v).reshape(-1).view(np.int16)).pin_memory()
+                  for k, v in wl.host_in.items()}
+        dst = {k: getattr(wl, k).reshape(-1).view(torch.int16) for k in pinned}
         yh = torch.empty(wl.y.shape, dtype=wl.y.dtype).pin_memory()
         h2d = sum(v.numel() * 2 for v in pinned.values())
         d2h = wl.y.numel() * wl.y.element_size()
