@@ -67,9 +67,10 @@ constexpr uint32_t kTmemCols = 512;
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
-template <bool NVF4, int BN>
+template <bool NVF4, int BN, bool QX = false>
 struct Cfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
+    // QX: the stage also holds A's bf16 tile (128 x 128), quantized in the CTA
+    static constexpr int kStages = QX ? 3 : BN == 256 ? 4 : 6;
     static constexpr int kStageK = NVF4 ? 256 : 128;             // elements of K per stage
     static constexpr int kAtomsPerStage = NVF4 ? 4 : 1;          // scale atoms along K per 128 rows
     static constexpr int kRowTilesB = BN / 128;
@@ -77,7 +78,8 @@ struct Cfg {
     static constexpr int kBBytes = BN * 128;
     static constexpr int kSfaBytes = kAtomsPerStage * kAtom;
     static constexpr int kSfbBytes = kRowTilesB * kAtomsPerStage * kAtom;
-    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    static constexpr int kXBytes = QX ? kBM * 128 * 2 : 0;         // two {64, 128} bf16 boxes
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes + kXBytes;
     // TMEM: accumulator columns [0, BN), then per stage SFA then SFB columns.
     static constexpr int kSfaCols = kAtomsPerStage * 4;
     static constexpr int kSfbCols = kRowTilesB * kAtomsPerStage * 4;
@@ -136,6 +138,11 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank)
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" :: "r"(addr), "h"(v) : "memory");
 }
@@ -154,14 +161,15 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
 template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const GemmArgs args) {
-    using C = Cfg<NVF4, BN>;
+    using C = Cfg<NVF4, BN, (QA >= 0)>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA_st = smem;
     uint8_t* sB_st = sA_st + C::kStages * C::kABytes;
     uint8_t* sSfa = sB_st + C::kStages * C::kBBytes;
     uint8_t* sSfb = sSfa + C::kStages * C::kSfaBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sSfb + C::kStages * C::kSfbBytes);
+    uint8_t* sX = sSfb + C::kStages * C::kSfbBytes;                // QA: [kStages] bf16 A tiles
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sX + C::kStages * C::kXBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::kStages;
     uint64_t* acc_full = bars + 2 * C::kStages;
@@ -309,8 +317,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t fb = smem_u32(full + stage);
                     mbar_arrive_expect_tx(fb, args.tx_ab);
                     const int32_t kx = (int32_t)(ks * (NVF4 ? 128 : C::kStageK));   // bytes (nvfp4) / elements
-                    if constexpr (QA < 0)
+                    if constexpr (QA < 0) {
                         tma_load_2d(smem_u32(sA_st + stage * C::kABytes), &tmA, fb, kx, (int32_t)a_row0);
+                    } else {                   // tmA maps the bf16 activations: two 64-value boxes
+                        tma_load_2d(smem_u32(sX + stage * C::kXBytes), &tmA, fb, kx, (int32_t)a_row0);
+                        tma_load_2d(smem_u32(sX + stage * C::kXBytes + C::kXBytes / 2), &tmA, fb, kx + 64,
+                                    (int32_t)a_row0);
+                    }
                     tma_load_2d(smem_u32(sB_st + stage * C::kBBytes), &tmW, fb, kx, (int32_t)w_row0);
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     issued_any |= 1u << stage;
@@ -436,15 +449,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else {
         // ------------------------------------------------------- epilogue --
         if constexpr (QA >= 0) {
-            // First the A operand: each stage's 128 x 128 tile of A quantized from
-            // bf16 (the quantizer's block scale and encode) straight into the layout
-            // the tensor map would have produced -- row r's 16-code chunk c at
-            // (c ^ (r & 7)) * 16 (128-byte swizzle), an fp6 chunk as its 12 packed
-            // bytes and 4 zero bytes, an e4m3 chunk as 16 bytes -- and its UE8M0
-            // bytes into the stage's scale atom.  Thread (r, h) takes values
-            // [64h, 64h + 64) of row r of the stage: blocks 2h and 2h + 1.  Rows >= M
-            // and blocks past K get zero codes and zero scales, as the quantizer
-            // writes them.  One tile per CTA (the host launches no persistence).
+            // First the A operand: the producer loads each stage's 128 x 128 bf16
+            // tile of A beside the W tile (two {64, 128} boxes, 128-byte swizzle,
+            // zeros past M and K); these warps quantize it (the quantizer's block
+            // scale and encode) straight into the layout the tensor map would have
+            // produced for the codes -- row r's 16-code chunk c at (c ^ (r & 7)) *
+            // 16, an fp6 chunk as its 12 packed bytes and 4 zero bytes, an e4m3
+            // chunk as 16 bytes -- and its UE8M0 bytes into the stage's scale
+            // atom.  Thread (r, h) takes values [64h, 64h + 64) of row r of the
+            // stage: blocks 2h and 2h + 1.  Zero values give zero codes and zero
+            // scales, as the quantizer writes them.  One tile per CTA (the host
+            // launches no persistence).
             const int et = (int)threadIdx.x - 64;
             const int qr = et >> 1, qh = et & 1;
             int stage = 0;
@@ -453,30 +468,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
                 int64_t grp, mb, nb;
                 unit_at(tile, grp, mb, nb);
-                const int64_t grow = mb * kBM + qr;
-                const uint16_t* xrow = args.qx + (grow < M ? grow : 0) * K;
-                // this thread's 64 values of stage ks (two blocks), zeros past M or K
-                auto load_x = [&](int64_t ks, uint4 (&v)[2][4]) {
-#pragma unroll
-                    for (int bl = 0; bl < 2; ++bl)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int64_t k = ks * C::kStageK + 64 * qh + 32 * bl + 8 * j;
-                            v[bl][j] = grow < M && k < K ? __ldg(reinterpret_cast<const uint4*>(xrow + k))
-                                                         : make_uint4(0, 0, 0, 0);
-                        }
-                };
-                uint4 xv[2][4];
-                if (ks_begin < ks_end) load_x(ks_begin, xv);
+                (void)mb;
                 for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
-                    // the next stage's x is in flight while this one is encoded
-                    uint4 xn[2][4];
-                    if (ks + 1 < ks_end) load_x(ks + 1, xn);
-                    // the stage's buffers are free once the MMAs that read them completed
-                    if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, args.err, abort_flag, kErrGemmEpilogue)) {
+                    // the stage's W tile and bf16 A tile have landed (the producer refilled
+                    // the stage only after the MMAs that read it before completed)
+                    if (!mbar_wait(smem_u32(full + stage), phase, args.err, abort_flag, kErrGemmEpilogue)) {
                         ok = false;
                         break;
                     }
+                    // this thread's 64 values: box qh, row qr (128-byte swizzle: 16-byte
+                    // piece c at (c ^ (qr & 7)) * 16); rows >= M and values past K are zero
+                    uint4 xv[2][4];
+                    const uint32_t xb = smem_u32(sX + stage * C::kXBytes + qh * (C::kXBytes / 2)) + (uint32_t)qr * 128u;
+#pragma unroll
+                    for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            xv[bl][j] = lds_v4(xb + ((((uint32_t)(4 * bl + j)) ^ (uint32_t)(qr & 7)) << 4));
                     const uint32_t a_row = smem_u32(sA_st + stage * C::kABytes) + (uint32_t)qr * 128u;
                     uint32_t ue2 = 0;
 #pragma unroll
@@ -502,10 +510,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMA reads A via the async proxy
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(a_ready + stage));
-#pragma unroll
-                    for (int bl = 0; bl < 2; ++bl)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) xv[bl][j] = xn[bl][j];
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
                 }
             }
@@ -785,7 +789,7 @@ bool operand_map(CUtensorMap* map, const void* p, int fmt, bool nvf4, int64_t ro
 template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1>
 bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a,
                        cudaStream_t s) {
-    using C = Cfg<NVF4, BN>;
+    using C = Cfg<NVF4, BN, (QA >= 0)>;
     static std::once_flag flags[64];
     static bool ok_dev[64];
     int dev = 0;
@@ -931,8 +935,11 @@ bsq_status gemm_quant_a_launch(const uint16_t* x, int fa, const void* W, int fw,
     int split = 1;
     for (int sp = 8; sp >= 2; sp /= 2)
         if (tiles128 * sp <= info->num_sms && nks >= sp) { split = sp; break; }
-    CUtensorMap tw;
+    CUtensorMap tw, tx;
     if (!operand_map(&tw, W, fw, false, N, K, 128u)) return BSQ_ERR_CUDA;
+    // x [M, K] bf16 as 64-value boxes of 128 rows (128-byte swizzle, zeros past M and K)
+    if (!encode_map(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)(K * 2), 64, 128))
+        return BSQ_ERR_CUDA;
     GemmArgs a;
     a.sA = nullptr; a.sW = sW; a.gA = nullptr; a.gW = gW; a.Y = Y;
     a.M = M; a.N = N; a.K = K;
@@ -942,13 +949,13 @@ bsq_status gemm_quant_a_launch(const uint16_t* x, int fa, const void* W, int fw,
     a.out_bf16 = out == BSQ_OUT_BF16;
     a.idesc = make_idesc(false, fa, fw, 128);
     a.err = info->err;
-    a.tx_ab = 128u * (fw == kE4M3 ? 128u : 96u);          // the W tile only
+    a.tx_ab = 128u * (fw == kE4M3 ? 128u : 96u) + (uint32_t)(kBM * 128 * 2);   // the W tile and A's bf16 tile
     bsq_status r;
 #define BSQ_QA_SPLITS(F)                                                            \
-    if (split == 8) r = launch_gemm<false, 128, 8, false, F>(info, tw, tw, a, s);   \
-    else if (split == 4) r = launch_gemm<false, 128, 4, false, F>(info, tw, tw, a, s); \
-    else if (split == 2) r = launch_gemm<false, 128, 2, false, F>(info, tw, tw, a, s); \
-    else r = launch_gemm<false, 128, 1, false, F>(info, tw, tw, a, s);
+    if (split == 8) r = launch_gemm<false, 128, 8, false, F>(info, tx, tw, a, s);   \
+    else if (split == 4) r = launch_gemm<false, 128, 4, false, F>(info, tx, tw, a, s); \
+    else if (split == 2) r = launch_gemm<false, 128, 2, false, F>(info, tx, tw, a, s); \
+    else r = launch_gemm<false, 128, 1, false, F>(info, tx, tw, a, s);
     switch (fa) {
     case kE3M2: BSQ_QA_SPLITS(kE3M2); break;
     case kE2M3: BSQ_QA_SPLITS(kE2M3); break;
