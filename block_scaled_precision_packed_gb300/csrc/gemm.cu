@@ -369,12 +369,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t sf_col = (uint32_t)(BN + stage * C::kSfColsPerStage);
                     const uint64_t a_st = dA0 + (uint64_t)(stage * (C::kABytes >> 4));
                     const uint64_t b_st = dB0 + (uint64_t)(stage * (C::kBBytes >> 4));
-                    const int n_mma = NVF4 ? (int)imin64(4, (K - ks * C::kStageK) / 64) : 4;
                     // MX: the stage's one atom per operand serves all 4 K steps;
                     // nvfp4: K step kk reads atom kk
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if (kk >= n_mma) break;
+                    auto issue = [&](int kk) {
                         const uint64_t ad = a_st + (uint64_t)(2 * kk);          // +32 bytes per K step
                         const uint64_t bd = b_st + (uint64_t)(2 * kk);
                         const uint32_t acc = (ks > ks_begin || kk > 0) ? 1u : 0u;
@@ -385,6 +382,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             const uint32_t id = args.idesc | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
                             tc_mma_mxf8f6f4(tmem, ad, bd, id, tmem + sf_col, tmem + sf_col + C::kSfaCols, acc);
                         }
+                    };
+                    // A whole stage issues its four MMAs back to back, with no branch
+                    // between them; only an nvfp4 stage cut by K (K % 256 != 0) checks.
+                    if (!NVF4 || (ks + 1) * C::kStageK <= K) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) issue(kk);
+                    } else {
+                        const int n_mma = (int)((K - ks * C::kStageK) / 64);
+                        for (int kk = 0; kk < n_mma; ++kk) issue(kk);
                     }
                     tc_commit(smem_u32(empty + stage));
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
