@@ -46,8 +46,12 @@ enum ErrorSite : uint32_t {
     kErrQuantBarrier = 0x302,
 };
 
-// Wall-clock bound of every spin-wait in these kernels (ns).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Wall-clock bound of every spin-wait in these kernels (ns).  A test build
+// may set a shorter one (BSQ_WAIT_LIMIT_NS) to make a wait run out quickly.
+#ifndef BSQ_WAIT_LIMIT_NS
+#define BSQ_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = BSQ_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
@@ -224,6 +228,51 @@ __device__ __forceinline__ void tc_mma_mxf4nvf4(uint32_t d, uint64_t adesc, uint
                  "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p; }"
                  :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
 }
+// ---- CTA pair (cta_group::2): the two CTAs of a cluster whose ranks differ in
+// bit 0.  Established on GB300 against a CPU product: the allocation is
+// collective (one warp of each CTA issues it and both receive the same
+// columns); rank 0 issues the MMA, which reads A's 128 rows and B's N half
+// from each CTA's shared memory at the same offsets and writes each CTA's
+// 128 accumulator rows into its own TMEM; each CTA's TMEM holds A's scale
+// factors for its own rows and B's for all N rows of the MMA.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+// Arrive on the barrier at the same offset in both CTAs of the pair once this
+// thread's earlier pair MMAs have completed.
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(bar), "h"((uint16_t)3) : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf8f6f4_pair(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                     uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p; }"
+                 :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf4nvf4_pair(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                     uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p; }"
+                 :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+}
+// Arrive on a barrier given by its shared::cluster address, e.g. the peer
+// CTA's copy of a barrier (mapa).  Default semantics (release at CTA scope):
+// a cluster-scope release would make the arriving warp wait for the SM's
+// outstanding memory operations, serializing a pipeline's relay.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Registers r[0..N) -> TMEM columns [col, col + N) of the warp's 32 lanes

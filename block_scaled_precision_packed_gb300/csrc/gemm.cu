@@ -67,15 +67,19 @@ constexpr uint32_t kTmemCols = 512;
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
-template <bool NVF4, int BN, bool QX = false>
+template <bool NVF4, int BN, bool QX = false, bool PAIR = false>
 struct Cfg {
-    // QX: the stage also holds A's bf16 tile (128 x 128), quantized in the CTA
-    static constexpr int kStages = QX ? 3 : BN == 256 ? 4 : 6;
+    // QX: the stage also holds A's bf16 tile (128 x 128), quantized in the CTA.
+    // PAIR: a CTA pair computes a 256 x BN tile; each CTA stages its own 128 A
+    // rows and its own BN/2 W rows, and B's scale atoms for all BN rows.
+    static constexpr int kStages = QX ? 3 : PAIR ? (NVF4 ? 5 : 6) : BN == 256 ? 4 : 6;
     static constexpr int kStageK = NVF4 ? 256 : 128;             // elements of K per stage
     static constexpr int kAtomsPerStage = NVF4 ? 4 : 1;          // scale atoms along K per 128 rows
     static constexpr int kRowTilesB = BN / 128;
+    static constexpr int kRowsB = PAIR ? BN / 2 : BN;            // W rows in this CTA's B tile
+    static constexpr int kTileM = PAIR ? 2 * kBM : kBM;          // output rows per tile
     static constexpr int kABytes = kBM * 128;
-    static constexpr int kBBytes = BN * 128;
+    static constexpr int kBBytes = kRowsB * 128;
     static constexpr int kSfaBytes = kAtomsPerStage * kAtom;
     static constexpr int kSfbBytes = kRowTilesB * kAtomsPerStage * kAtom;
     static constexpr int kXBytes = QX ? kBM * 128 * 2 : 0;         // two {64, 128} bf16 boxes
@@ -85,7 +89,9 @@ struct Cfg {
     static constexpr int kSfbCols = kRowTilesB * kAtomsPerStage * 4;
     static constexpr int kSfColsPerStage = kSfaCols + kSfbCols;
     static_assert(BN + kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM budget");
+    static_assert(!PAIR || (BN == 256 && !QX), "pair tiles: 256 x 256, operands from memory");
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     // barriers: full, empty, sf_full, sf_land, a_ready per stage; acc_full,
     // acc_empty, drain; the TMEM base and abort flag (one slot)
     static_assert((5 * kStages + 4) * 8 <= 512, "barrier slots");
@@ -158,10 +164,10 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
 //            runs K stages [r*S/SPLIT, (r+1)*S/SPLIT), and the fp32 partial
 //            tiles are summed (rank order, deterministic) through distributed
 //            shared memory -- no workspace, no atomics.
-template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1>
+template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const GemmArgs args) {
-    using C = Cfg<NVF4, BN, (QA >= 0)>;
+    using C = Cfg<NVF4, BN, (QA >= 0), PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA_st = smem;
@@ -183,15 +189,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t M = args.M, N = args.N, K = args.K;
-    const int64_t num_mb = (M + kBM - 1) / kBM, num_nb = (N + BN - 1) / BN;
+    const int64_t num_mb = (M + C::kTileM - 1) / C::kTileM, num_nb = (N + BN - 1) / BN;
     const int64_t num_tiles = num_mb * num_nb;
     const int64_t nks_all = (K + C::kStageK - 1) / C::kStageK;
     const int64_t rt_total = pad_to(N, 128) / 128;   // 128-row scale tiles of W
+    const int64_t rt_total_a = pad_to(M, 128) / 128; // ... and of A
     const uint32_t krank = SPLIT > 1 ? cluster_rank() : 0u;
+    // PAIR: rank 0 of the pair issues the MMAs; rank 1 stages the other half
+    const uint32_t prank = PAIR ? cluster_rank() : 0u;
     const int64_t ks_begin = nks_all * krank / SPLIT, ks_end = nks_all * (krank + 1) / SPLIT;
-    const int64_t tile_first = SPLIT > 1 ? (int64_t)(blockIdx.x / SPLIT) : (int64_t)blockIdx.x;
-    const int64_t tile_step = SPLIT > 1 ? num_tiles : (int64_t)gridDim.x;
+    const int64_t tile_first = PAIR ? (int64_t)(blockIdx.x / 2)
+                                    : SPLIT > 1 ? (int64_t)(blockIdx.x / SPLIT) : (int64_t)blockIdx.x;
+    const int64_t tile_step = PAIR ? (int64_t)(gridDim.x / 2) : SPLIT > 1 ? num_tiles : (int64_t)gridDim.x;
     static_assert(!GROUPED || SPLIT == 1, "grouped products are persistent, not split-K");
+    static_assert(!PAIR || (SPLIT == 1 && !GROUPED && QA < 0), "pair tiles: persistent, ungrouped, quantized operands");
     static_assert(QA < 0 || (!NVF4 && BN == 128 && !GROUPED), "in-kernel A quantization: MX, 128-wide tiles");
     __shared__ uint32_t qa_red[QA >= 0 ? kThreads / 32 : 1];
     // grouped: mb_first[g] = row blocks of the groups before g (prefix sums)
@@ -204,12 +215,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(smem_u32(empty + s), 1);
         }
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(sf_full + s), 4);
+            mbar_init(smem_u32(sf_full + s), PAIR ? 8 : 4);     // PAIR: both CTAs' scale-factor warps
             mbar_init(smem_u32(sf_land + s), 1);
             mbar_init(smem_u32(a_ready + s), kEpiThreads / 32);
         }
         mbar_init(smem_u32(acc_full), 1);
-        mbar_init(smem_u32(acc_empty), kEpiThreads);
+        mbar_init(smem_u32(acc_empty), PAIR ? 2 * (kEpiThreads / 32) : kEpiThreads);   // PAIR: one per warp
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -217,11 +228,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         prefetch_tmap(&tmW);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_base_s), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_base_s), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before either signals the other's
     tc_fence_after();
     const uint32_t tmem = *tmem_base_s;
     // the setup above overlaps the previous kernel; its outputs (A, W, their
@@ -289,7 +306,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
                 int64_t grp, mb, nb;
                 unit_at(tile, grp, mb, nb);
-                const int64_t a_row0 = grp * M + mb * kBM, w_row0 = grp * N + nb * BN;
+                const int64_t a_row0 = grp * M + mb * C::kTileM + prank * kBM;
+                const int64_t w_row0 = grp * N + nb * BN + prank * C::kRowsB;
+                // this CTA's 128-row scale tile of A (rows past M: any finite scales)
+                int64_t a_rt = mb * (C::kTileM / kBM) + prank;
+                if (a_rt >= rt_total_a) a_rt = mb * (C::kTileM / kBM);
                 const uint8_t* sa_base = args.sA + grp * args.sa_group;
                 const uint8_t* sw_base = args.sW + grp * args.sw_group;
                 for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
@@ -305,7 +326,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t lb = smem_u32(sf_land + stage);
                     mbar_arrive_expect_tx(lb, (uint32_t)natoms * kAtom * ((QA >= 0 ? 0 : 1) + C::kRowTilesB));
                     if constexpr (QA < 0)          // else the epilogue warps make A and its scale atom
-                        bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), sa_base + (mb * args.cpd4 + kg) * kAtom,
+                        bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), sa_base + (a_rt * args.cpd4 + kg) * kAtom,
                                   natoms * kAtom, lb);
 #pragma unroll
                     for (int rt = 0; rt < C::kRowTilesB; ++rt) {
@@ -344,7 +365,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && prank == 0) {
             // --------------------------------------------------- MMA issue --
             // Descriptors of stage 0's tiles; a stage or K step is an offset in
             // the 16-byte-unit address field (smem < 256 KB), so the single
@@ -355,7 +376,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t tile = tile_first; tile < n_units && ok; tile += tile_step) {
-                if (!mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, args.err, abort_flag, kErrGemmMma)) break;
+                if (!mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, args.err, abort_flag, kErrGemmMma))
+                    break;
                 tc_fence_after();
                 for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
                     // the stage's operands have landed and its scales are in TMEM
@@ -375,12 +397,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         const uint64_t ad = a_st + (uint64_t)(2 * kk);          // +32 bytes per K step
                         const uint64_t bd = b_st + (uint64_t)(2 * kk);
                         const uint32_t acc = (ks > ks_begin || kk > 0) ? 1u : 0u;
-                        if constexpr (NVF4) {
+                        if constexpr (NVF4 && PAIR) {
+                            tc_mma_mxf4nvf4_pair(tmem, ad, bd, args.idesc, tmem + sf_col + 4 * kk,
+                                                 tmem + sf_col + C::kSfaCols + kk * C::kRowTilesB * 4, acc);
+                        } else if constexpr (NVF4) {
                             tc_mma_mxf4nvf4(tmem, ad, bd, args.idesc, tmem + sf_col + 4 * kk,
                                             tmem + sf_col + C::kSfaCols + kk * C::kRowTilesB * 4, acc);
                         } else {
                             const uint32_t id = args.idesc | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
-                            tc_mma_mxf8f6f4(tmem, ad, bd, id, tmem + sf_col, tmem + sf_col + C::kSfaCols, acc);
+                            if constexpr (PAIR)
+                                tc_mma_mxf8f6f4_pair(tmem, ad, bd, id, tmem + sf_col, tmem + sf_col + C::kSfaCols, acc);
+                            else
+                                tc_mma_mxf8f6f4(tmem, ad, bd, id, tmem + sf_col, tmem + sf_col + C::kSfaCols, acc);
                         }
                     };
                     // A whole stage issues its four MMAs back to back, with no branch
@@ -392,15 +420,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         const int n_mma = (int)((K - ks * C::kStageK) / 64);
                         for (int kk = 0; kk < n_mma; ++kk) issue(kk);
                     }
-                    tc_commit(smem_u32(empty + stage));
+                    // the stage is free again in both CTAs of a pair once these MMAs complete
+                    if constexpr (PAIR) tc_commit_pair_both(smem_u32(empty + stage));
+                    else tc_commit(smem_u32(empty + stage));
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(acc_full));
+                if constexpr (PAIR) tc_commit_pair_both(smem_u32(acc_full));
+                else tc_commit(smem_u32(acc_full));
                 acc_phase ^= 1;
             }
             // every MMA issued has completed before TMEM is released
-            tc_commit(smem_u32(drain));
+            if constexpr (PAIR) tc_commit_pair_local(smem_u32(drain));
+            else tc_commit(smem_u32(drain));
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(smem_u32(drain), 0)) {
                 if (globaltimer() - t0 > kWaitLimitNs) { atomicCAS(args.err, 0u, (uint32_t)kErrGemmDrain); break; }
@@ -448,7 +480,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     break;
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(sf_full + stage));
+                if (lane == 0) {
+                    // a pair's MMA thread (rank 0) waits for both CTAs' warps
+                    if (PAIR && prank != 0) mbar_arrive_cluster(map_rank(smem_u32(sf_full + stage), 0));
+                    else mbar_arrive(smem_u32(sf_full + stage));
+                }
                 if (++stage == C::kStages) { stage = 0; phase ^= 1; }
             }
         }
@@ -525,6 +561,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         constexpr int kHalf = BN / 2;
         const float f = __fmul_rn(QA >= 0 ? sg_a : (args.gA ? __ldg(args.gA) : 1.0f), args.gW ? __ldg(args.gW) : 1.0f);
         uint32_t acc_phase = 0;
+        // hand the accumulator back to the MMA thread: every thread (count 256),
+        // or for a pair one arrival per warp of either CTA on rank 0's barrier
+        auto release_acc = [&]() {
+            if constexpr (PAIR) {
+                __syncwarp();
+                if (lane == 0) {
+                    if (prank != 0) mbar_arrive_cluster(map_rank(smem_u32(acc_empty), 0));
+                    else mbar_arrive(smem_u32(acc_empty));
+                }
+            } else {
+                mbar_arrive(smem_u32(acc_empty));
+            }
+        };
         const bool vec = args.out_bf16 ? (N % 8 == 0) : (N % 4 == 0);
         // Each thread writes one output row: 32-byte stores (whole sectors)
         // halve the memory requests of 16-byte ones.
@@ -556,9 +605,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         for (int64_t tile = tile_first; tile < n_units && SPLIT == 1; tile += tile_step) {
             int64_t grp, mb, nb;
             unit_at(tile, grp, mb, nb);
-            if (!mbar_wait(smem_u32(acc_full), acc_phase, args.err, abort_flag, kErrGemmEpilogue)) break;
+            if (!mbar_wait(smem_u32(acc_full), acc_phase, args.err, abort_flag, kErrGemmEpilogue))
+                break;
             tc_fence_after();
-            const int64_t lrow = mb * kBM + 32 * q + lane;              // row within the group
+            const int64_t row_base = mb * C::kTileM + prank * kBM;     // this CTA's first row of the tile
+            const int64_t lrow = row_base + 32 * q + lane;              // row within the group
             int64_t rows_valid = M;
             float fg = f;
             if constexpr (GROUPED) {
@@ -586,7 +637,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                                                 __fmul_rn(__uint_as_float(r0[2 * e + 1]), fg));
                 }
                 tc_fence_before();
-                mbar_arrive(smem_u32(acc_empty));
+                release_acc();
                 acc_phase ^= 1;
                 if (vec32) {
                     // Whole 128-byte lines: within each group of four lanes
@@ -595,7 +646,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     // of the group holds chunk i of 64 columns of each of the
                     // four rows; one store then writes 8 rows x 128 bytes.
                     const int gi = lane & 3;
-                    const int64_t lrow0 = mb * kBM + 32 * q + (lane & ~3);  // the group's first row (within the group)
+                    const int64_t lrow0 = row_base + 32 * q + (lane & ~3);  // the group's first row (within the group)
                     uint16_t* ybase = static_cast<uint16_t*>(args.Y) + (grp * M + lrow0) * N + nb * BN + kHalf * half;
 #pragma unroll
                     for (int h = 0; h < kHalf / 64; ++h) {
@@ -680,7 +731,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(acc_empty));
+            release_acc();
             acc_phase ^= 1;
         }
     }
@@ -742,16 +793,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
     pdl_launch_dependents();
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) {
+        // neither CTA releases TMEM or its shared memory before the pair's
+        // last MMA (which reads both) has completed: rank 0's MMA thread waited
+        // for it above
+        __syncwarp();
+        cluster_sync();
+    } else {
+        __syncthreads();
+    }
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) {
+        if constexpr (PAIR) tmem_dealloc_pair(tmem, kTmemCols);
+        else tmem_dealloc(tmem, kTmemCols);
+    }
 }
 
 // ------------------------------------------------------------------ host ----
 // Instruction descriptor (kind::mxf8f6f4 / kind::mxf4nvf4, dense, K-major):
 // bits 7-9 A format, 10-12 B format, 17-22 N>>3, 23 scale type (1 = UE8M0),
 // 24-28 M>>4; the scale-factor ids (bits 4-5 B, 29-30 A) are set per MMA.
-uint32_t make_idesc(bool nvf4, int fa, int fw, int bn) {
+uint32_t make_idesc(bool nvf4, int fa, int fw, int bn, int bm = kBM) {
     auto code = [](int f) -> uint32_t { return f == kE4M3 ? 0u : f == kE2M3 ? 3u : 4u; };
     uint32_t d = 0;
     if (nvf4) {
@@ -763,7 +825,7 @@ uint32_t make_idesc(bool nvf4, int fa, int fw, int bn) {
         d |= 1u << 23;           // UE8M0 scales
     }
     d |= (uint32_t)(bn >> 3) << 17;
-    d |= (uint32_t)(kBM >> 4) << 24;
+    d |= (uint32_t)(bm >> 4) << 24;        // a pair's MMA spans both CTAs' rows: M = 256
     return d;
 }
 
@@ -792,20 +854,38 @@ bool operand_map(CUtensorMap* map, const void* p, int fmt, bool nvf4, int64_t ro
                       (uint64_t)(3 * K / 4), 128, box_rows);
 }
 
-template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1>
+template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1, bool PAIR = false>
 bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a,
                        cudaStream_t s) {
-    using C = Cfg<NVF4, BN, (QA >= 0)>;
+    using C = Cfg<NVF4, BN, (QA >= 0), PAIR>;
+    auto kernel = gemm_kernel<NVF4, BN, SPLIT, GROUPED, QA, PAIR>;
     static std::once_flag flags[64];
     static bool ok_dev[64];
+    static int pairs_dev[64];          // PAIR: how many CTA pairs fit on the device at once
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSQ_ERR_CUDA;
     std::call_once(flags[dev], [&] {
-        ok_dev[dev] = cudaFuncSetAttribute(gemm_kernel<NVF4, BN, SPLIT, GROUPED, QA>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) == cudaSuccess;
+        ok_dev[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) ==
+                      cudaSuccess;
+        if (PAIR && ok_dev[dev]) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3((unsigned)(2 * (info->num_sms / 2)), 1, 1);
+            q.blockDim = dim3(kThreads, 1, 1);
+            q.dynamicSmemBytes = C::kSmemBytes;
+            cudaLaunchAttribute ca;
+            ca.id = cudaLaunchAttributeClusterDimension;
+            ca.val.clusterDim.x = 2;
+            ca.val.clusterDim.y = 1;
+            ca.val.clusterDim.z = 1;
+            q.attrs = &ca;
+            q.numAttrs = 1;
+            int n = 0;
+            ok_dev[dev] = cudaOccupancyMaxActiveClusters(&n, kernel, &q) == cudaSuccess && n > 0;
+            pairs_dev[dev] = n;
+        }
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
-    const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
+    const int64_t tiles = ((a.M + C::kTileM - 1) / C::kTileM) * ((a.N + BN - 1) / BN);
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
@@ -816,7 +896,16 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if constexpr (GROUPED) {
+    if constexpr (PAIR) {
+        // persistent CTA pairs, no more than can be resident together (a pair
+        // that had to wait for another to finish would serialize its tiles)
+        cfg.gridDim = dim3((unsigned)(2 * imin64(tiles, pairs_dev[dev])), 1, 1);
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    } else if constexpr (GROUPED) {
         // the tile count depends on the device row counts: one persistent CTA per SM
         cfg.gridDim = dim3((unsigned)imin64(a.G * tiles, info->num_sms), 1, 1);
     } else if constexpr (SPLIT == 1) {
@@ -832,7 +921,7 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    if (cudaLaunchKernelEx(&cfg, gemm_kernel<NVF4, BN, SPLIT, GROUPED, QA>, ta, tw, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tw, a) != cudaSuccess) {
         (void)cudaGetLastError();
         return BSQ_ERR_CUDA;
     }
@@ -851,14 +940,20 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
     // 128-wide tiles leave most SMs idle, split K across a cluster.
     const int64_t tiles256 = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
     const int64_t tiles128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
+    const int64_t pair_tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + 255) / 256);
     const int bn = tiles256 >= info->num_sms ? 256 : 128;
+    // 256 x 256 tiles on CTA pairs when A has more than one 128-row block and
+    // the pair tiles still give every pair of SMs one: each SM then stages half
+    // of B, halving the shared-memory traffic of the B operand per MMA
+    const bool pair = bn == 256 && M > kBM && pair_tiles >= info->num_sms / 2;
     const int64_t nks = (K + (nvf4 ? 255 : 127)) / (nvf4 ? 256 : 128);
     int split = 1;
     if (bn == 128)
         for (int sp = 8; sp >= 2; sp /= 2)
             if (tiles128 * sp <= info->num_sms && nks >= sp) { split = sp; break; }
+    const uint32_t rows_b = pair ? 128u : (uint32_t)bn;     // W rows one CTA stages per tile
     CUtensorMap ta, tw;
-    if (!operand_map(&ta, A, fa, nvf4, M, K, kBM) || !operand_map(&tw, W, fw, nvf4, N, K, (uint32_t)bn))
+    if (!operand_map(&ta, A, fa, nvf4, M, K, kBM) || !operand_map(&tw, W, fw, nvf4, N, K, rows_b))
         return BSQ_ERR_CUDA;
     GemmArgs a;
     a.sA = sA; a.sW = sW; a.gA = gA; a.gW = gW; a.Y = Y;
@@ -867,14 +962,17 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
     a.qx = nullptr; a.qpartial = nullptr; a.qn_partial = 0; a.qs_global = nullptr;
     a.cpd4 = pad_to(K / (nvf4 ? 16 : 32), 4) / 4;
     a.out_bf16 = out == BSQ_OUT_BF16;
-    a.idesc = make_idesc(nvf4, fa, fw, bn);
+    a.idesc = make_idesc(nvf4, fa, fw, bn, pair ? 2 * kBM : kBM);
     a.err = info->err;
     // A 16U6_ALIGN16B load lands 128 bytes per 128-code row in shared memory but
     // counts the 96 packed bytes it read toward the transaction.
     auto row_tx = [&](int f) { return (uint32_t)(nvf4 || f == kE4M3 ? 128 : 96); };
-    a.tx_ab = kBM * row_tx(fa) + (uint32_t)bn * row_tx(fw);
+    a.tx_ab = kBM * row_tx(fa) + rows_b * row_tx(fw);
     bsq_status r;
-    if (nvf4) {
+    if (pair) {
+        if (nvf4) r = launch_gemm<true, 256, 1, false, -1, true>(info, ta, tw, a, s);
+        else r = launch_gemm<false, 256, 1, false, -1, true>(info, ta, tw, a, s);
+    } else if (nvf4) {
         if (bn == 256) r = launch_gemm<true, 256, 1>(info, ta, tw, a, s);
         else if (split == 8) r = launch_gemm<true, 128, 8>(info, ta, tw, a, s);
         else if (split == 4) r = launch_gemm<true, 128, 4>(info, ta, tw, a, s);

@@ -11,21 +11,19 @@
 //  * MX formats (gemv_kernel, here): a CTA owns 128 weight rows (8 warps x 16
 //    rows) and walks all of K; the weight is dequantized in registers, never
 //    staged: each thread loads its rows' packed bytes straight from global
-//    memory (16-byte loads, prefetched a 256-element chunk ahead) and turns
-//    them into bf16 pairs.  Products run on the tensor cores as mma.sync
-//    m16n8k16 bf16 -> f32, weight rows as the A operand (16 rows), activation
-//    rows as B (8 per n-tile).
+//    memory (prefetched a 256-element chunk ahead) and turns them into bf16
+//    pairs.  Products run on the tensor cores as mma.sync m16n8k16 bf16 -> f32,
+//    weight rows as the A operand (16 rows), activation rows as B (8 per
+//    n-tile).
 //  * Exact decode ("placed" bf16): a code's bits are dropped into the low
 //    bf16 exponent/mantissa fields and its sign into the sign bit, which is
-//    the code's value times a fixed power of two (bf16 subnormals included).
-//    One bf16x2 multiply by (block scale * 2^c) then yields value*scale*2^c'
-//    exactly: every fp6*2^k and e2m1*ue4m3 product fits bf16's 8-bit
-//    significand.  The fixed power is undone in fp32 at the end.  No rounding
-//    happens before the tensor-core accumulate.
-//  * In the MX kernel K inside a 32-element thread range is permuted
-//    consistently for both operands (pairs (j, j+4) of each 8-code group share
-//    a bf16x2 register); the activation chunk is staged in shared memory in
-//    that order with a bank-conflict-free layout.
+//    the code's value times a fixed power of two (bf16 subnormals included);
+//    one bf16x2 multiply by a constant power of two makes it the code's value
+//    (at most 4 significant bits: exact).  No rounding happens before the
+//    tensor-core accumulate.
+//  * MX block scales are applied in fp32 to per-block partial sums: the two
+//    MMAs of a K slice cover exactly one 32-code block (each thread of a quad
+//    holds 8 of its codes), so any UE8M0 byte scales its block exactly.
 #include <climits>
 #include <mutex>
 #include <type_traits>
@@ -41,43 +39,50 @@ constexpr int kRowsPerCta = 128;         // 16 rows per warp
 constexpr int kChunk = 256;              // K elements staged per step (2 sub-chunks of 128)
 constexpr int kPitch = kChunk / 8 + 4;   // 16-byte units per staged x row (== 4 mod 8)
 
-template <int WFMT>
-struct WTraits;
-template <>
-struct WTraits<kE3M2> { static constexpr int kRegs = 6; static constexpr int kBlock = 32; };
-template <>
-struct WTraits<kE2M3> { static constexpr int kRegs = 6; static constexpr int kBlock = 32; };
-template <>
-struct WTraits<kE4M3> { static constexpr int kRegs = 8; static constexpr int kBlock = 32; };
-
-// Raw packed bytes of one thread's 32-code range of one row, plus its scales.
+// Raw packed bytes of one thread's share of one row's 128-element sub-chunk:
+// codes 8t..8t+7 of each of the sub-chunk's four MX blocks (thread t of the
+// quad), plus the four blocks' UE8M0 bytes.
 template <int WFMT>
 struct RowRaw {
-    uint32_t w[WTraits<WFMT>::kRegs];
-    uint32_t s;   // nvfp4: two ue4m3 bytes (blocks 2t', 2t'+1); MX: one UE8M0 byte
+    uint32_t w[8];   // block b: w[2b] codes 0..3 of the thread's eight, w[2b+1] codes 4..7 (packed bits)
+    uint32_t s;      // the sub-chunk's four UE8M0 bytes, block b in byte b
 };
 
 template <int WFMT>
 __device__ __forceinline__ void load_row(RowRaw<WFMT>& rr, const uint8_t* __restrict__ W, const uint8_t* __restrict__ sW,
-                                         int64_t row, int64_t k, bool valid, int64_t K, int64_t cpd4) {
+                                         int64_t row, int64_t k, int t, bool valid, int64_t K, int64_t cpd4) {
     if (!valid) {
 #pragma unroll
-        for (int i = 0; i < WTraits<WFMT>::kRegs; ++i) rr.w[i] = 0;
+        for (int i = 0; i < 8; ++i) rr.w[i] = 0;
         rr.s = 0;
         return;
     }
     if constexpr (WFMT == kE4M3) {
-        const uint4* p = reinterpret_cast<const uint4*>(W + row * K + k);
-        const uint4 a = __ldg(p), b = __ldg(p + 1);
-        rr.w[0] = a.x; rr.w[1] = a.y; rr.w[2] = a.z; rr.w[3] = a.w;
-        rr.w[4] = b.x; rr.w[5] = b.y; rr.w[6] = b.z; rr.w[7] = b.w;
-        rr.s = __ldg(sW + swz_offset(row, k / 32, cpd4));
+        // block b's codes 8t..8t+7: bytes 32b + 8t .. +8 of the sub-chunk
+        const uint8_t* base = W + row * K + k + 8 * t;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(base + 32 * b));
+            rr.w[2 * b] = v.x;
+            rr.w[2 * b + 1] = v.y;
+        }
     } else {
-        const uint2* p = reinterpret_cast<const uint2*>(W + row * (3 * K / 4) + (3 * k) / 4);
-        const uint2 a = __ldg(p), b = __ldg(p + 1), c = __ldg(p + 2);
-        rr.w[0] = a.x; rr.w[1] = a.y; rr.w[2] = b.x; rr.w[3] = b.y; rr.w[4] = c.x; rr.w[5] = c.y;
-        rr.s = __ldg(sW + swz_offset(row, k / 32, cpd4));
+        // block b's codes 8t..8t+7: 6 bytes at 24b + 6t, read as the two aligned
+        // words that hold them (rows of 3K/4 bytes, K % 128 == 0: 4-byte aligned)
+        const uint8_t* rowp = W + row * (3 * K / 4) + (3 * k) / 4;
+        const int off = 6 * t;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp + 24 * b + (off & ~3));
+            const uint32_t lo = __ldg(wp), hi = __ldg(wp + 1);
+            const uint32_t b0 = (off & 2) ? __funnelshift_r(lo, hi, 16) : lo;     // bits 0..31 of the 48
+            const uint32_t b1 = (off & 2) ? (hi >> 16) : (hi & 0xFFFFu);         // bits 32..47
+            rr.w[2 * b] = b0 & 0xFFFFFFu;                                         // codes 0..3
+            rr.w[2 * b + 1] = (b0 >> 24) | (b1 << 8);                             // codes 4..7
+        }
     }
+    // the four blocks' scale bytes are consecutive in the swizzled buffer
+    rr.s = __ldg(reinterpret_cast<const uint32_t*>(sW + swz_offset(row, k / 32, cpd4)));
 }
 
 // Four fp6 codes of a 24-bit little-endian lane -> four byte containers.
@@ -100,41 +105,37 @@ __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
     return r;
 }
 
-// bf16x2 scale multiplier for one MX block: 2^(ue-11), so the product is
-// value*2^(ue-127)*2^(116-P).
+// 2^P in both bf16 halves: a placed code times this is the code's value
+// (an exact bf16: at most 4 significant bits, inside the normal range).
 template <int WFMT>
-__device__ __forceinline__ uint32_t scale_mult(uint32_t code) {
-    const uint32_t b = ((code & 0xFF) + 116u) << 7;
-    return b | (b << 16);
+__device__ __forceinline__ constexpr uint32_t unplace_mult() {
+    constexpr uint32_t p = WFMT == kE3M2 ? 124u : WFMT == kE2M3 ? 126u : 120u;
+    return ((p + 127u) << 7) | (((p + 127u) << 7) << 16);
 }
 
-// The weight operand of one thread for one 128-element sub-chunk of one row:
-// P[q][j] holds codes (8q+j, 8q+j+4) of its 32-code range, scaled.
+// The UE8M0 byte's value 2^(ue-127) as an fp32, built from its bits (byte 0 is
+// the subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_value(uint32_t ue) {
+    return ue == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(ue << 23);
+}
+
+// One row's sub-chunk as MMA A-operand registers: V[b][j] holds codes
+// (8t+2j, 8t+2j+1) of block b as exact bf16 values; sc[b] the block scale.
 template <int WFMT>
-__device__ __forceinline__ void decode_row(const RowRaw<WFMT>& rr, uint32_t (&P)[4][4]) {
-    {
-        const uint32_t sm = scale_mult<WFMT>(rr.s);
-        uint32_t C[8];   // byte containers of the 32 codes, 4 per word
-        if constexpr (WFMT == kE4M3) {
+__device__ __forceinline__ void decode_row(const RowRaw<WFMT>& rr, uint32_t (&V)[4][4], float (&sc)[4]) {
+    constexpr uint32_t kUnplace = unplace_mult<WFMT>();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) C[i] = rr.w[i];
-        } else {
-            // 24 bytes = 8 lanes of 3 bytes; w[] holds them little-endian.
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const int byte = 3 * g, wi = byte >> 2, sh = (byte & 3) * 8;
-                uint32_t bits = rr.w[wi] >> sh;
-                if (sh > 8) bits |= rr.w[wi + 1] << (32 - sh);
-                C[g] = fp6_to_containers(bits & 0xFFFFFFu);
-            }
+    for (int b = 0; b < 4; ++b) {
+        uint32_t c0 = rr.w[2 * b], c1 = rr.w[2 * b + 1];     // byte containers of codes 0..3 / 4..7
+        if constexpr (WFMT != kE4M3) {
+            c0 = fp6_to_containers(c0);
+            c1 = fp6_to_containers(c1);
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t u = __byte_perm(C[2 * q], C[2 * q + 1], (uint32_t)(j | ((4 + j) << 8)));
-                P[q][j] = bmul2(place_pair<WFMT>(u), sm);
-            }
+        V[b][0] = bmul2(place_pair<WFMT>(__byte_perm(c0, 0, 0x4140)), kUnplace);
+        V[b][1] = bmul2(place_pair<WFMT>(__byte_perm(c0, 0, 0x4342)), kUnplace);
+        V[b][2] = bmul2(place_pair<WFMT>(__byte_perm(c1, 0, 0x4140)), kUnplace);
+        V[b][3] = bmul2(place_pair<WFMT>(__byte_perm(c1, 0, 0x4342)), kUnplace);
+        sc[b] = ue8m0_value((rr.s >> (8 * b)) & 0xFFu);
     }
 }
 
@@ -145,6 +146,14 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The MX kernel.  Each quad of a warp (rows g and g + 8) walks K in 128-element
+// sub-chunks = four MX blocks; thread t holds codes 8t..8t+7 of every block, so
+// the two m16n8k16 MMAs of a block (MMA s: K slots 2t, 2t+1 <- codes 8t+4s,
+// +1; slots 2t+8, 2t+9 <- codes 8t+4s+2, +3) sum that block alone.  Each
+// block's sum starts from zero and is added to the fp32 accumulator times the
+// block's scale 2^(ue-127): every UE8M0 byte is applied exactly in fp32, and
+// the operands are the codes' exact values.  x is staged in its natural order
+// (16 bytes = x[8t .. 8t+8) of a block per thread and activation row).
 template <int NT, int WFMT>
 __global__ void __launch_bounds__(kThreads)
 gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const uint8_t* __restrict__ sW,
@@ -155,10 +164,10 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int64_t row0 = (int64_t)blockIdx.x * kRowsPerCta + warp * 16 + g;
     const int64_t row1 = row0 + 8;
-    const int64_t cpd4 = pad_to(K / WTraits<WFMT>::kBlock, 4) / 4;
+    const int64_t cpd4 = pad_to(K / 32, 4) / 4;
     const int64_t nck = (K + kChunk - 1) / kChunk;
 
-    // ---- activation staging: 16-byte group u of row r of a chunk ----
+    // ---- activation staging: 16-byte group u of row r of a chunk, natural order ----
     auto stage_load = [&](int64_t ck, uint4 (&xr)[NT]) {
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
@@ -167,27 +176,23 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
             const int64_t k = ck * kChunk + u * 8;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (r < M && k < K) v = __ldg(reinterpret_cast<const uint4*>(x + r * K + k));
-            // [x0..x7] -> [(x0,x4), (x1,x5), (x2,x6), (x3,x7)]
-            xr[i] = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
-                               __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+            xr[i] = v;
         }
     };
     auto stage_store = [&](int buf, const uint4 (&xr)[NT]) {
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
             const int idx = threadIdx.x + i * kThreads;
-            const int r = idx >> 5, u = idx & 31;
-            const int h = u >> 4, tt = (u >> 2) & 3, q = u & 3;
-            xs[buf][r * kPitch + 16 * h + 4 * q + tt] = xr[i];
+            xs[buf][(idx >> 5) * kPitch + (idx & 31)] = xr[i];
         }
     };
     auto load_w = [&](int64_t ck, RowRaw<WFMT> (&rr)[2][2]) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int64_t k = ck * kChunk + 128 * h + 32 * t;
+            const int64_t k = ck * kChunk + 128 * h;
             const bool kv = ck < nck && k < K;
-            load_row<WFMT>(rr[h][0], W, sW, row0, k, kv && row0 < N, K, cpd4);
-            load_row<WFMT>(rr[h][1], W, sW, row1, k, kv && row1 < N, K, cpd4);
+            load_row<WFMT>(rr[h][0], W, sW, row0, k, t, kv && row0 < N, K, cpd4);
+            load_row<WFMT>(rr[h][1], W, sW, row1, k, t, kv && row1 < N, K, cpd4);
         }
     };
 
@@ -211,24 +216,24 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
         load_w(ck + 1, wnext);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            uint32_t P0[4][4], P1[4][4];
-            decode_row<WFMT>(wcur[h][0], P0);
-            decode_row<WFMT>(wcur[h][1], P1);
+            uint32_t V0[4][4], V1[4][4];
+            float s0[4], s1[4];
+            decode_row<WFMT>(wcur[h][0], V0, s0);
+            decode_row<WFMT>(wcur[h][1], V1, s1);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 xb[NT];
+            for (int b = 0; b < 4; ++b) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[nt] = xs[buf][(8 * nt + g) * kPitch + 16 * h + 4 * q + t];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int j0 = 2 * half;
-                    const uint32_t a[4] = {P0[q][j0], P1[q][j0], P0[q][j0 + 1], P1[q][j0 + 1]};
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const uint32_t b0 = half ? xb[nt].z : xb[nt].x;
-                        const uint32_t b1 = half ? xb[nt].w : xb[nt].y;
-                        mma_bf16(acc[nt], a, b0, b1);
-                    }
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint4 xb = xs[buf][(8 * nt + g) * kPitch + 16 * h + 4 * b + t];
+                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    const uint32_t a0[4] = {V0[b][0], V1[b][0], V0[b][1], V1[b][1]};
+                    const uint32_t a1[4] = {V0[b][2], V1[b][2], V0[b][3], V1[b][3]};
+                    mma_bf16(d, a0, xb.x, xb.y);
+                    mma_bf16(d, a1, xb.z, xb.w);
+                    acc[nt][0] = __fmaf_rn(d[0], s0[b], acc[nt][0]);
+                    acc[nt][1] = __fmaf_rn(d[1], s0[b], acc[nt][1]);
+                    acc[nt][2] = __fmaf_rn(d[2], s1[b], acc[nt][2]);
+                    acc[nt][3] = __fmaf_rn(d[3], s1[b], acc[nt][3]);
                 }
             }
         }
@@ -238,9 +243,8 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
         for (int h = 0; h < 2; ++h) { wcur[h][0] = wnext[h][0]; wcur[h][1] = wnext[h][1]; }
     }
 
-    // ---- epilogue: undo the fixed power of two, apply gW, store y[m, n] ----
-    constexpr float kLift = WFMT == kE3M2 ? 0x1p8f : WFMT == kE2M3 ? 0x1p10f : 0x1p4f;
-    const float f = __fmul_rn(kLift, gW ? __ldg(gW) : 1.0f);
+    // ---- epilogue: apply gW, store y[m, n] ----
+    const float f = gW ? __ldg(gW) : 1.0f;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll

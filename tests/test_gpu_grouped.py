@@ -70,7 +70,7 @@ def run_grouped_gemm(bsq, G, R, N, K, rc, fa, fw, out, seed):
     return Y, (oA, osA, ogA, oW, osW, ogW)
 
 
-@pytest.mark.parametrize("fa,fw", [("e3m2", "e2m3"), ("e4m3", "e3m2")])
+@pytest.mark.parametrize("fa,fw", [("e3m2", "e2m3"), ("e4m3", "e3m2"), ("e2m3", "e2m3")])
 def test_grouped_gemm_matches_oracle(bsq, fa, fw):
     G, R, N, K = 3, 200, 320, 256
     rc = [200, 1, 131]

@@ -101,6 +101,42 @@ def test_gemv_mx(bsq, fmt, M, N, K):
         check_products(y, want, s, f"gemv_{fmt} M{M} N{N} K{K}")
 
 
+def swizzle_plain(plain):
+    """Row-major [rows, blocks] scale bytes -> the swizzled buffer (the oracle's offset rule)."""
+    rows, blocks = plain.shape
+    buf = np.zeros(O.scale_bytes(rows, blocks), dtype=np.uint8)
+    for r in range(rows):
+        for b in range(blocks):
+            buf[O.swz_offset(r, b, blocks)] = plain[r, b]
+    return buf
+
+
+@pytest.mark.parametrize("fmt", ["e3m2", "e2m3", "e4m3"])
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_gemv_mx_every_ue8m0_byte(bsq, fmt, M):
+    """Block scales covering every UE8M0 byte 0..254 (2^-127 .. 2^127; byte 0
+    read as 2^-127).  Two bands keep every output finite in fp32: bytes 0..140
+    with N(0,1) activations, bytes 115..254 with activations scaled by 2^-24;
+    within a row the blocks' scales are mixed across the whole band."""
+    N, K = 300, 512
+    nb = K // 32
+    g = np.random.default_rng(2000 + M)
+    rb = K if fmt == "e4m3" else 3 * K // 4
+    codes = g.integers(0, 256, size=(N, rb), dtype=np.uint8)
+    if fmt == "e4m3":
+        codes[(codes & 0x7F) == 0x7F] &= 0xFE            # no NaN codes
+    for lo, hi, xstd in ((0, 140, 1.0), (115, 254, 2.0 ** -24)):
+        plain = g.integers(lo, hi + 1, size=(N, nb)).astype(np.uint8)
+        plain.ravel()[:hi - lo + 1] = np.arange(lo, hi + 1, dtype=np.uint8)   # every byte of the band occurs
+        sc = swizzle_plain(plain)
+        x = S.normal_bf16((M, K), xstd, 2100 + M + lo)
+        want, s = O.gemv_mx(x, codes, MX[fmt], sc, 1.0, M, N, K)
+        assert np.isfinite(want).all()
+        for out in (torch.float32, torch.bfloat16):
+            y = bsq.gemv_mxfp6(dev_tensor(x), dev_tensor(codes), fmt, dev_tensor(sc), None, K, out_dtype=out)
+            check_products(y, want, s, f"gemv_{fmt} M{M} UE8M0 bytes {lo}..{hi}")
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (200, 333, 320), (1, 256, 64), (256, 512, 1024),
                                    (384, 1024, 512), (130, 4096, 256), (200, 336, 256)])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
@@ -114,8 +150,7 @@ def test_gemm_nvfp4(bsq, M, N, K, out):
     check_products(y, want, s, f"gemm_nvfp4 {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("fa,fw", [("e3m2", "e3m2"), ("e4m3", "e2m3"), ("e2m3", "e3m2"), ("e4m3", "e4m3"),
-                                   ("e3m2", "e4m3")])
+@pytest.mark.parametrize("fa,fw", [(a, w) for a in ("e3m2", "e2m3", "e4m3") for w in ("e3m2", "e2m3", "e4m3")])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 333, 384), (256, 1024, 1024), (1, 300, 256)])
 def test_gemm_mx(bsq, fa, fw, M, N, K):
     A, sA, gA = mx_operand(M, K, fa, 71 + M)
@@ -129,9 +164,9 @@ def test_gemm_mx(bsq, fa, fw, M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(1100, 4315, 256), (1024, 9728, 128), (1100, 4400, 128)])
 def test_gemm_nvfp4_many_tiles(bsq, M, N, K):
-    """At least one 256-wide tile per SM (the persistent 128 x 256 path) with
-    several row blocks, an odd row-block count with a ragged last block, and a
-    ragged N edge; every output checked."""
+    """More 256 x 256 tiles than pairs of SMs (the persistent CTA-pair path)
+    with several row blocks, an odd row-block count with a ragged last block,
+    and a ragged N edge; every output checked."""
     A, sA = nvfp4_operand(M, K, 91 + M)
     W, sW = nvfp4_operand(N, K, 93 + N)
     gA = torch.tensor([0.5], device="cuda")
@@ -142,11 +177,48 @@ def test_gemm_nvfp4_many_tiles(bsq, M, N, K):
     check_products(y, want, s, f"gemm_nvfp4 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 9800, 320), (2048, 4864, 512)])
+def test_gemm_nvfp4_pair_tiles(bsq, M, N, K):
+    """256 x 256 tiles on CTA pairs: rank 0 issues MMAs over both CTAs' A rows
+    and W halves.  300 rows leave the second pair tile's rank 1 entirely past M
+    (zero-filled rows, clamped scale tile) and rank 0 ragged; N = 9800 leaves the
+    last W tile's second half past N; K = 320 ends in a one-MMA stage."""
+    A, sA = nvfp4_operand(M, K, 101 + M)
+    W, sW = nvfp4_operand(N, K, 103 + N)
+    gA = torch.tensor([0.5], device="cuda")
+    gW = torch.tensor([1.5], device="cuda")
+    want, s = O.gemm_nvfp4(A, sA, 0.5, W, sW, 1.5, M, N, K)
+    for out in (torch.float32, torch.bfloat16):
+        y = bsq.gemm_nvfp4(dev_tensor(A), dev_tensor(sA), gA, dev_tensor(W), dev_tensor(sW), gW, K, out_dtype=out)
+        check_products(y, want, s, f"gemm_nvfp4 pair {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("kind", ["nvfp4", "e4m3xe2m3"])
+def test_gemm_single_cta_256_wide(bsq, kind):
+    """One 128-row block of A and more 256-wide W tiles than SMs: the product
+    stays on single-CTA 128 x 256 tiles (a CTA pair would idle its second half)."""
+    M, N, K = 100, 152 * 256 + 40, 128
+    if kind == "nvfp4":
+        A, sA = nvfp4_operand(M, K, 105)
+        W, sW = nvfp4_operand(N, K, 106)
+        y = bsq.gemm_nvfp4(dev_tensor(A), dev_tensor(sA), None, dev_tensor(W), dev_tensor(sW), None, K,
+                           out_dtype=torch.bfloat16)
+        want, s = O.gemm_nvfp4(A, sA, 1.0, W, sW, 1.0, M, N, K)
+    else:
+        A, sA, gA = mx_operand(M, K, "e4m3", 107)
+        W, sW, gW = mx_operand(N, K, "e2m3", 108)
+        y = bsq.gemm_mxfp6(dev_tensor(A), "e4m3", dev_tensor(sA), torch.tensor([gA], device="cuda"),
+                           dev_tensor(W), "e2m3", dev_tensor(sW), torch.tensor([gW], device="cuda"), K,
+                           out_dtype=torch.bfloat16)
+        want, s = O.gemm_mx(A, O.E4M3, sA, gA, W, O.E2M3, sW, gW, M, N, K)
+    check_products(y, want, s, f"gemm {kind} {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("fa,fw,N,out", [("e4m3", "e2m3", 4315, torch.float32), ("e3m2", "e3m2", 4315, torch.float32),
                                          ("e4m3", "e2m3", 4400, torch.bfloat16), ("e3m2", "e3m2", 4315, torch.bfloat16)])
 def test_gemm_mx_many_tiles(bsq, fa, fw, N, out):
-    """The persistent 128 x 256 path for MX operands (fp6 W included) on a
-    ragged shape with more tiles than SMs; every output checked.  N = 4400 (a
+    """The persistent 256 x 256 CTA-pair path for MX operands (fp6 W included)
+    on a ragged shape with more tiles than pairs of SMs; every output checked.  N = 4400 (a
     multiple of 16, not of the tile) takes the whole-line bf16 stores up to a
     ragged column edge."""
     M, K = 1100, 256
