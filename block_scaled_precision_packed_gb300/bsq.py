@@ -76,7 +76,7 @@ def load(path: str | None = None):
             "bsq_gemv_mxfp6": (i32, [vp, vp, i32, vp, vp, vp, i32, i64, i64, i64, vp]),
             "bsq_dequant_nvfp4": (i32, [vp, vp, vp, vp, i64, i64, vp]),
             "bsq_dequant_mxfp6": (i32, [vp, i32, vp, vp, vp, i64, i64, vp]),
-            "bsq_get_device_error": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
+            "bsq_get_device_error": (i32, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
             "bsq_launch_count": (ctypes.c_uint64, [i32]),
             "bsq_reset_launch_counts": (None, []),
         }
@@ -248,9 +248,11 @@ def dequant_mxfp6_(codes, fmt, scales, g, out, R, K, stream=None):
         _p(codes), fmt, _p(scales), _p(g), _p(out), R, K, _stream(stream)))
 
 
-def device_error() -> tuple[int, int]:
+def device_error(stream=None) -> tuple[int, int]:
+    """(status, site) of the device error word after the work on `stream` (torch's
+    current stream by default) has finished; the word is cleared when set."""
     code = ctypes.c_uint32(0)
-    st = load().bsq_get_device_error(ctypes.byref(code))
+    st = load().bsq_get_device_error(_stream(stream), ctypes.byref(code))
     return st, code.value
 
 

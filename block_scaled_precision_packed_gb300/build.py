@@ -71,6 +71,38 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     return LIB
 
 
+def build_variant(name: str, defines, rebuilt=("bsq_api.cu", "quantize.cu")) -> str:
+    """A separately named copy of the library (lib<name>.so in _build_<name>/)
+    whose `rebuilt` translation units are compiled with extra preprocessor
+    defines; the others are the regular build's objects.  Used by tests for
+    compile-time test hooks (a short wait limit, a skipped barrier arrival),
+    never by the product path."""
+    build()
+    out_dir = os.path.join(PKG, f"_build_{name}")
+    os.makedirs(out_dir, exist_ok=True)
+    cc = nvcc()
+    flags = [f"-D{d}" for d in defines]
+    objs, jobs = [], []
+    for src in SOURCES:
+        if src in rebuilt:
+            o = os.path.join(out_dir, src.replace(".cu", ".o"))
+            jobs.append([cc, *NVCC_FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", o])
+        else:
+            o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        objs.append(o)
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        for r in ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), jobs):
+            if r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+                raise RuntimeError("nvcc failed for variant " + name)
+    lib = os.path.join(out_dir, f"lib{name}.so")
+    r = subprocess.run([cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", lib, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write(r.stdout + r.stderr)
+        raise RuntimeError("link failed for variant " + name)
+    return lib
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv,
           extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else [])

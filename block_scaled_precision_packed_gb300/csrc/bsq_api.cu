@@ -270,23 +270,39 @@ bsq_status bsq_gemv_mxfp6(const uint16_t* x, const uint8_t* W, bsq_mxfmt fw, con
 bsq_status bsq_dequant_nvfp4(const uint32_t* codes, const uint8_t* scales, const float* g, float* out, int64_t R,
                              int64_t K, cudaStream_t stream) {
     if (!codes || !scales || !out || R < 1 || K < 16 || K % 16) return BSQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(codes) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u) ||
+        (g && (reinterpret_cast<uintptr_t>(g) & 3u)))
+        return BSQ_ERR_MISALIGNED;
     return dequant_launch(codes, kNvfp4, scales, g, out, R, K, true, stream);
 }
 
 bsq_status bsq_dequant_mxfp6(const uint8_t* codes, bsq_mxfmt fmt, const uint8_t* scales, const float* g, float* out,
                              int64_t R, int64_t K, cudaStream_t stream) {
     if (!codes || !scales || !out || !valid_mx(fmt) || R < 1 || K < 32 || K % 32) return BSQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) || (g && (reinterpret_cast<uintptr_t>(g) & 3u)))
+        return BSQ_ERR_MISALIGNED;
     return dequant_launch(codes, fmt, scales, g, out, R, K, false, stream);
 }
 
-bsq_status bsq_get_device_error(uint32_t* code_out) {
+bsq_status bsq_get_device_error(cudaStream_t stream, uint32_t* code_out) {
     if (!code_out) return BSQ_ERR_INVALID_ARG;
     bsq_status st;
     if (!device_info(&st)) return st;
-    if (cudaDeviceSynchronize() != cudaSuccess) return BSQ_ERR_CUDA;
-    uint32_t v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return BSQ_ERR_CUDA;
-    if (v != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return BSQ_ERR_CUDA;
+    // the work enqueued on `stream` has finished, then the word is read (and
+    // cleared if set) in stream order; other streams are not waited for
+    uint32_t v = 0;
+    static const uint32_t zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_device_error, sizeof v, 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return BSQ_ERR_CUDA;
+    }
+    if (v != 0 && (cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream) !=
+                       cudaSuccess ||
+                   cudaStreamSynchronize(stream) != cudaSuccess)) {
+        (void)cudaGetLastError();
+        return BSQ_ERR_CUDA;
+    }
     *code_out = v;
     if (v == 0) return BSQ_OK;
     return (v & 0xF00u) ? BSQ_ERR_TIMEOUT : BSQ_ERR_DEVICE_CHECK;

@@ -21,6 +21,7 @@
 // consecutive values (one MX block, or two nvfp4 blocks) = 64 contiguous bytes,
 // so the block amax and scale math run once per 32 values without shuffles.
 #include <cstdio>
+#include <atomic>
 #include <mutex>
 
 #include "bsq_device.cuh"
@@ -526,6 +527,11 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
     if (threadIdx.x == 0) {
         uint32_t* ctl = args.ws + kCtlWord;
         args.ws[1 + blockIdx.x] = m;
+#ifdef BSQ_TEST_BARRIER_SKIP_LAST_CTA
+        // test build only: the grid's last CTA never counts itself in, so every
+        // CTA's bounded wait below runs out (no copy or TMEM is in flight here)
+        if (blockIdx.x + 1 != gridDim.x)
+#endif
         red_release_add_u32(ctl + 2, 1u);
         if (ld_acquire_u32(ctl + 2) < G) {
             const uint64_t t0 = globaltimer();
@@ -1212,19 +1218,29 @@ namespace {
 static __device__ __align__(256) uint32_t g_noalloc_partials[kMaxPartials];
 
 constexpr int kNoallocMaxDevices = 64;
-std::once_flag g_noalloc_once[kNoallocMaxDevices];
-uint32_t* g_noalloc_ptr[kNoallocMaxDevices];
+std::mutex g_noalloc_mutex;
+std::atomic<uint32_t*> g_noalloc_ptr[kNoallocMaxDevices];
 
 // Device address of the scratch array on the current device (nullptr on error).
+// Only a successful lookup is kept: a lookup that failed (for instance one
+// attempted during a stream capture) is tried again by the next call.
 uint32_t* noalloc_scratch() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) return nullptr;
-    std::call_once(g_noalloc_once[dev], [dev] {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_partials) == cudaSuccess) g_noalloc_ptr[dev] = static_cast<uint32_t*>(p);
-        else (void)cudaGetLastError();
-    });
-    return g_noalloc_ptr[dev];
+    uint32_t* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    p = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_noalloc_partials) == cudaSuccess) {
+            p = static_cast<uint32_t*>(q);
+            g_noalloc_ptr[dev].store(p, std::memory_order_release);
+        } else {
+            (void)cudaGetLastError();
+        }
+    }
+    return p;
 }
 
 }  // namespace

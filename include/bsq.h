@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define BSQ_ABI_VERSION 1
+#define BSQ_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define BSQ_API __attribute__((visibility("default")))
@@ -207,8 +207,9 @@ BSQ_API bsq_status bsq_quantize_mxfp6_act(const uint16_t* x, int64_t M, int64_t 
  * the amax pass never launches more CTAs than that, so every size the checks
  * above accept fits, and a call that would need more returns
  * BSQ_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
- * address (make it before any stream capture).  Calls share the array: two
- * calls whose kernels overlap on the GPU race on it.  Calls no allocator.
+ * address (make it before any stream capture); a lookup that fails returns
+ * BSQ_ERR_CUDA and is tried again by the next call.  Calls share the array:
+ * two calls whose kernels overlap on the GPU race on it.  Calls no allocator.
  */
 BSQ_API bsq_status bsq_quantize_mxfp6_noalloc(const uint16_t* x, int64_t M, int64_t K, bsq_mxfmt fmt,
                                       uint8_t* codes, uint8_t* scales, float* s_global,
@@ -328,7 +329,11 @@ BSQ_API bsq_status bsq_gemv_nvfp4(const uint16_t* x, const uint32_t* W, const ui
 
 /*
  * bsq_gemv_mxfp6 -- the same decode product with an MX weight (e3m2 / e2m3
- * 4-in-3 packed, or e4m3).  K % 128 == 0; 1 <= M <= 32.
+ * 4-in-3 packed, or e4m3).  K % 128 == 0; 1 <= M <= 32.  Every UE8M0 byte
+ * 0..254 is applied exactly (byte 0 as 2^-127): each 32-code block's products
+ * are summed in fp32 and scaled by the block's power of two before they are
+ * added up.  |y - y_exact| <= 1e-5 * sum_k |x_k w_k| (fp32 out) while the
+ * result and the fp32 partial sums stay in fp32's normal range.
  */
 BSQ_API bsq_status bsq_gemv_mxfp6(const uint16_t* x, const uint8_t* W, bsq_mxfmt fw, const uint8_t* sW,
                           const float* gW, void* y, bsq_outtype out, int64_t M, int64_t N, int64_t K,
@@ -339,6 +344,7 @@ BSQ_API bsq_status bsq_gemv_mxfp6(const uint16_t* x, const uint8_t* W, bsq_mxfmt
  * packed_scaled_copy, b12x _lib/fp6.py dequant_mxfp6_torch):
  *   out[r, k] = decode(code) * scale(r, k/blk) * g   (fp32, [R, K])
  * g: device float (NULL = 1).  UE8M0 byte 0 decodes as 2^-127.
+ * nvfp4 codes, out and g must be 4-byte aligned (BSQ_ERR_MISALIGNED).
  */
 BSQ_API bsq_status bsq_dequant_nvfp4(const uint32_t* codes, const uint8_t* scales, const float* g,
                              float* out, int64_t R, int64_t K, cudaStream_t stream);
@@ -347,11 +353,15 @@ BSQ_API bsq_status bsq_dequant_mxfp6(const uint8_t* codes, bsq_mxfmt fmt, const 
 
 /*
  * Reads and clears the device error word of the current device (a bounded
- * wait that timed out, or a device-side check).  Synchronizes the device.
+ * wait that timed out, or a device-side check).  Waits for the work enqueued
+ * on `stream` (0 = the legacy default stream) to finish, then reads the word
+ * and, if it is set, clears it, in stream order; work on other streams is not
+ * waited for (the word is shared by every stream of the device).
  * *code_out = 0 when nothing was recorded; otherwise a site id (nonzero).
- * Returns BSQ_ERR_TIMEOUT / BSQ_ERR_DEVICE_CHECK when a code was recorded.
+ * Returns BSQ_ERR_TIMEOUT / BSQ_ERR_DEVICE_CHECK when a code was recorded,
+ * BSQ_ERR_CUDA if the stream reported an error.
  */
-BSQ_API bsq_status bsq_get_device_error(uint32_t* code_out);
+BSQ_API bsq_status bsq_get_device_error(cudaStream_t stream, uint32_t* code_out);
 
 /* Launch counters (host side), one per kernel family, for dispatch tests and
  * for counting launches in a timed region.  ids: see BSQ_KERNEL_*. */

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_host_helpers(lib):
     from block_scaled_precision_packed_gb300 import bsq
     import oracle as O
-    assert lib.bsq_abi_version() == 1
+    assert lib.bsq_abi_version() == 2
     assert bsq.status_string(0) == "BSQ_OK"
     assert bsq.status_string(3) == "BSQ_ERR_MISALIGNED"
     for rows, blocks in ((1, 1), (128, 4), (300, 257), (28672, 512)):
