@@ -81,6 +81,7 @@ def _declare(L):
         "bsqo_quantize_mx_act": (i, [p, i64, i64, i, i, p, p, p, p]),
         "bsqo_f32_to_bf16": (ctypes.c_uint16, [f]),
         "bsqo_double_to_bf16": (ctypes.c_uint16, [d]),
+        "bsqo_double_to_bf16_n": (None, [p, i64, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -140,9 +141,10 @@ def double_to_bf16(v: float) -> int:
 
 
 def double_to_bf16_array(y: np.ndarray) -> np.ndarray:
-    f = lib().bsqo_double_to_bf16
-    return np.array([f(float(v)) for v in np.asarray(y, dtype=np.float64).ravel()],
-                    dtype=np.uint16).reshape(np.shape(y))
+    v = np.ascontiguousarray(y, dtype=np.float64).ravel()
+    out = np.empty(v.size, dtype=np.uint16)
+    lib().bsqo_double_to_bf16_n(_ptr(v), v.size, _ptr(out))
+    return out.reshape(np.shape(y))
 
 
 # ---------------------------------------------------------------- packing ----

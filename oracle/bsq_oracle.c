@@ -599,7 +599,9 @@ static void product_at(const operand* a, const operand* w, int64_t K,
                        const int64_t* mi, const int64_t* ni, int64_t cnt,
                        double* y, double* s, int nthreads) {
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
+    /* nthreads <= 0: every processor (set explicitly: an earlier call's count
+     * would otherwise persist) */
+    omp_set_num_threads(nthreads > 0 ? nthreads : omp_get_num_procs());
 #pragma omp parallel for schedule(dynamic, 16) if (nthreads != 1)
 #endif
     for (int64_t i = 0; i < cnt; ++i) {
@@ -736,4 +738,9 @@ BSQO_API uint16_t bsqo_double_to_bf16(double v) {
     if (r >= 0x1p128) return sign | 0x7F80;  /* rounded past the largest bf16 */
     float rf = (float)r;                     /* exact: r has <= 8 significant bits */
     return sign | (uint16_t)(bits_of_f32(rf) >> 16);
+}
+
+/* bsqo_double_to_bf16 over an array (no arithmetic of its own). */
+BSQO_API void bsqo_double_to_bf16_n(const double* v, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = bsqo_double_to_bf16(v[i]);
 }

@@ -3,11 +3,11 @@
 Tolerances (the acceptance bar of the path):
   * quantizer codes, scales, packed bytes and s_global: bit-exact;
   * fp32 products: |got - y| <= 1e-5 * S with S = |gA gW| sum_k |a_k w_k|;
-  * bf16 products: within 1 bf16 ulp of round_bf16(y); an output whose exact
-    value y sits so close to zero that fp32 accumulation alone moves it by more
-    than an ulp passes if |got - y| <= 1e-5 * S + ulp(got)/2 (the fp32 bound
-    plus the final rounding) -- the reading of the bf16 rule for outputs with
-    heavy cancellation.
+  * bf16 products: within 1 bf16 ulp of round_bf16(y).  Only an output whose
+    exact value is so small that the fp32 accumulation bound alone exceeds half
+    a bf16 ulp of it -- |y| < 2^8 * 1e-5 * S, heavy cancellation -- may instead
+    pass with |got - y| <= 1e-5 * S + ulp(got)/2 (the fp32 bound plus the final
+    rounding); every other output is held to the 1-ulp rule.
 """
 import numpy as np
 import torch
@@ -50,7 +50,8 @@ def check_products(got: torch.Tensor, want: np.ndarray, S: np.ndarray, what: str
         ok = np.abs(bf16_ordinal(bits) - bf16_ordinal(rb)) <= 1
         val = bf16_value(bits)
         ulp = np.abs(bf16_value((bits & 0x7FFF) | 1) - bf16_value(bits & 0x7FFF)) + 2.0 ** -133
-        ok |= np.abs(val - want) <= REL * S + ulp / 2
+        cancelled = np.abs(want) < 256.0 * REL * S
+        ok |= cancelled & (np.abs(val - want) <= REL * S + ulp / 2)
     else:
         val = got.detach().cpu().contiguous().numpy().astype(np.float64).ravel()
         ok = np.abs(val - want) <= REL * S + 1e-300
@@ -59,6 +60,21 @@ def check_products(got: torch.Tensor, want: np.ndarray, S: np.ndarray, what: str
         i = np.flatnonzero(~ok)[:8]
         raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} outputs out of tolerance; "
                              f"first idx {i.tolist()} got {val[i].tolist()} want {want[i].tolist()} S {S[i].tolist()}")
+
+
+def boundary_index(R, tile=128):
+    """Every index on either side of a tile boundary: 0, 127, 128, 255, 256, ...
+    up to R - 1."""
+    b = {0, R - 1}
+    for t in range(tile, R, tile):
+        b.update((t - 1, t))
+    return np.array(sorted(b), dtype=np.int64)
+
+
+def products_by_blocks(dec_a, dec_w, g):
+    """y = g * dec_a @ dec_w^T and S = |g| * |dec_a| @ |dec_w|^T in float64 (a
+    library matmul over operands the oracle decoded exactly)."""
+    return g * (dec_a @ dec_w.T), abs(g) * (np.abs(dec_a) @ np.abs(dec_w).T)
 
 
 def sample_pairs(M, N, n, seed, edges=True):
