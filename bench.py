@@ -1,29 +1,31 @@
 #!/usr/bin/env python
 """Benchmark of the block-scaled packed-precision hot path on GB300.
 
-Default workload (the one the headline metric is quoted on): MX-FP6 e3m2 W6A6,
-A bf16 [128, 4096] and W bf16 [4096, 4096] ~ N(0, 0.02) with 1% outliers x20.
-One step = quantize A and W (one batched launch; each tensor its own amax
-global scale, exact ceil UE8M0, RNE encode, 4-in-3 packing) + the tcgen05
-block-scaled GEMM (fp32 accumulate, bf16 out) -- every row of the hot path
-this workload exercises.
+Headline workload (the largest single-GPU configuration): nvfp4 prefill GEMM
+M = N = K = 8192, both operands e2m1 with ue4m3 scales per 16 and an fp32
+tensor factor, quantized beforehand from bf16 N(0, 1) (A) and N(0, 0.02) (W);
+one step = the tcgen05 block-scaled GEMM (fp32 accumulate, bf16 out).
 
-  value       GEMM TFLOP/s of the whole step (2*M*N*K / step time), summed over
-              ranks (each rank runs its own independent replica: weak scaling).
-  roofline    the step's dominant op (largest device time), achieved vs the
-              measured peak in MEASURED_PEAKS.json.
+  value       GEMM TFLOP/s of the step (2*M*N*K / step time), summed over ranks
+              (each rank runs its own independent replica: weak scaling).
+  roofline    the step's kernel, achieved vs the dense fp4 tensor peak (the
+              measured bf16 peak in MEASURED_PEAKS.json times the nominal ratio).
   e2e         the same metric through the public API with host buffers: the
-              step's bf16 inputs copied from pinned host memory, the bf16 output
-              copied back, inside the timed region.
-  cpu_baseline  the CPU oracle on a bounded sample of the same step, extrapolated.
+              step's quantized operands copied from pinned host memory, the bf16
+              output copied back, inside the timed region.
+  configs     every other configuration, each with its own time and roofline:
+              the decode GEMV at M = 1, 8, 32 (HBM GB/s), the W6A8 GEMM (fp8/fp6
+              tensor peak) with the small-M e2m3 quantizer, the one-row GEMV and
+              the W6A6 step (batched quantize + GEMM); L2 flushed and warm.
+  cpu_baseline  the CPU oracle on a bounded sample of the step, at 1 core and at
+              every host core, extrapolated to the step.
 
-Other workloads (--workload) measure the decode GEMV, the nvfp4 prefill GEMM
-and the W6A8 GEMM the same way.  L2 is flushed before every timed step (a
-256 MiB write, then a 256 MiB read of another buffer so no dirty lines remain).
-The step is captured once as a CUDA graph with event nodes at its two ends and
-replayed (device time).  A second capture with an event node after every op,
-replayed after the timed steps, gives the per-op split and the dominant op's
-duration for the roofline.
+--workload selects a single workload (its line alone).  L2 is flushed before
+every timed step (a 256 MiB write, then a 256 MiB read of another buffer so no
+dirty lines remain); the warm figures replay without the flush.  Each step is
+captured once as a CUDA graph with event nodes at its two ends and replayed
+(device time).  A second capture with an event node after every op gives the
+per-op split and the dominant op's duration for the roofline.
 """
 from __future__ import annotations
 
@@ -33,6 +35,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -40,8 +43,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ("mxfp6_e3m2_w6a6_128x4096x4096", "nvfp4_decode_gemv_Mx28672x8192", "nvfp4_prefill_gemm_8192",
-             "w6a8_e4m3xe2m3_4096x14336x4096", "nvfp4_gemv_1x256x256")
+WORKLOADS = ("nvfp4_prefill_gemm_8192", "nvfp4_decode_gemv_Mx28672x8192", "w6a8_e4m3xe2m3_4096x14336x4096",
+             "mxfp6_e3m2_w6a6_128x4096x4096", "nvfp4_gemv_1x256x256")
+HEADLINE = WORKLOADS[0]
 METRIC = "block-scaled GEMM TFLOP/s & decode GEMV HBM GB/s, as fraction of GB300 roofline"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -90,10 +94,10 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"bsq_clocks_gpu{gpu_index}_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
         q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
@@ -112,12 +116,19 @@ class ClockSampler:
             self.proc.terminate()
             self.proc.wait()
             self.f.close()
+        self.rows = self._read()
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
 
-    def summary(self):
-        if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _read(self):
         rows = []
-        for line in open(self.path):
+        try:
+            lines = open(self.path).read().splitlines()
+        except OSError:
+            return rows
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -125,6 +136,12 @@ class ClockSampler:
                 rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
             except ValueError:
                 continue
+        return rows
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = self.rows
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [r[0] for r in rows]
@@ -139,7 +156,7 @@ class Workload:
     """Holds device inputs/outputs; step() runs the hot path once on `stream`;
     ops() lists (name, launch fn, algorithmic bytes, flops, bound, peak kind)."""
 
-    def __init__(self, name, dev, gemv_m=32):
+    def __init__(self, name, dev, gemv_m=32, cache=None):
         import torch
         from block_scaled_precision_packed_gb300 import bsq, synthetic as S
         self.name, self.dev, self.bsq, self.torch = name, dev, bsq, torch
@@ -180,10 +197,13 @@ class Workload:
             N, K = cfg["N"], cfg["K"]
             M = gemv_m
             self.M, self.N, self.K = M, N, K
-            w = S.normal_bf16((N, K), cfg["w_std"], cfg["seed"] + 1)
-            wd = t(w).view(torch.bfloat16)
-            self.cw, self.sw, self.gw = bsq.quantize_nvfp4(wd)
-            del wd
+            cache = {} if cache is None else cache
+            if "decode_w" not in cache:     # one quantized weight serves every M
+                w = S.normal_bf16((N, K), cfg["w_std"], cfg["seed"] + 1)
+                wd = t(w).view(torch.bfloat16)
+                cache["decode_w"] = bsq.quantize_nvfp4(wd)
+                del wd, w
+            self.cw, self.sw, self.gw = cache["decode_w"]
             x = S.normal_bf16((M, K), cfg["x_std"], cfg["seed"] + 2 + M)
             self.host_in = {"x": x}
             self.x = t(x).view(torch.bfloat16)
@@ -272,6 +292,124 @@ def job_throughput(units_per_step, world, ms):
     return units_per_step * world / (ms / 1e3)
 
 
+class Timer:
+    """Device timing of a workload's step: the step captured as a CUDA graph
+    (event nodes at its ends) and replayed, L2 flushed before each replay (cold)
+    or not (warm); a second capture with an event node after every op gives the
+    per-op split (its event nodes add a little time per op)."""
+
+    def __init__(self, dev, stream, args, dist):
+        import torch
+        self.torch, self.dev, self.stream, self.args, self.dist = torch, dev, stream, args, dist
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        # after the write, a read of a second buffer of the same size leaves L2
+        # holding clean lines, so the step does not pay for the flush's write-backs
+        self.flush_b = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def capture(self, ops, per_op):
+        torch, stream = self.torch, self.stream
+        n = len(ops)
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n + 1)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            evs[0].record(stream)
+            for j, (_, fn, *_r) in enumerate(ops):
+                fn(stream)
+                if per_op or j == n - 1:
+                    evs[j + 1].record(stream)
+        return graph, evs
+
+    def replay(self, g, i, cold=True):
+        torch, stream = self.torch, self.stream
+        with torch.cuda.stream(stream):
+            if cold:
+                self.flush.fill_(i + 1000)
+                torch.sum(self.flush_b, dim=0, dtype=torch.int64, out=self.flush_sink)
+            g.replay()
+        stream.synchronize()
+
+    def run(self, wl, clock=None):
+        """{cold_ms, warm_ms, op_ms [per op, cold], launches_per_step}; the
+        cold timed region is the K steps between a barrier and a synchronize,
+        its mean taken as the slowest rank's."""
+        from block_scaled_precision_packed_gb300 import bsq
+        torch, stream, args, dist = self.torch, self.stream, self.args, self.dist
+        ops = wl.ops()
+        n = len(ops)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                wl.step(stream)                     # loads kernels before capture
+        torch.cuda.synchronize()
+        bsq.reset_launch_counts()
+        graph, evs = self.capture(ops, False)
+        launches = sum(bsq.launch_count(k) for k in bsq.KERNEL_IDS)
+        graph_ops, evs_ops = self.capture(ops, True)
+        for i in range(args.warmup):
+            self.replay(graph, i)
+            self.replay(graph_ops, i)
+        cold = np.zeros(args.steps)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with clock if clock is not None else _NoClock():
+            for i in range(args.steps):
+                self.replay(graph, i)
+                cold[i] = evs[0].elapsed_time(evs[n])
+            torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        op_ms = np.zeros((args.steps, n))
+        for i in range(args.steps):
+            self.replay(graph_ops, i)
+            for j in range(n):
+                op_ms[i, j] = evs_ops[j].elapsed_time(evs_ops[j + 1])
+        warm = np.zeros(args.steps)
+        for i in range(args.warmup + args.steps):
+            self.replay(graph, i, cold=False)
+            if i >= args.warmup:
+                warm[i - args.warmup] = evs[0].elapsed_time(evs[n])
+        cold_ms = max_over_ranks(float(cold.mean()), dist, self.dev)
+        warm_ms = max_over_ranks(float(warm.mean()), dist, self.dev)
+        return {"cold_ms": cold_ms, "warm_ms": warm_ms, "op_ms": op_ms.mean(axis=0), "launches_per_step": launches}
+
+
+class _NoClock:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def roofline(wl, op_ms, pk, workload, gemv_m=None):
+    """The dominant op's achieved rate against its peak: algorithmic bytes (HBM
+    bound) or flops (tensor bound) per launch over its mean duration."""
+    ops = wl.ops()
+    d = int(np.argmax(op_ms))
+    name, _, by, fl, bound, pkind = ops[d]
+    dur_s = op_ms[d] / 1e3
+    if bound == "hbm":
+        achieved, peak, ru = by / dur_s / 1e9, pk["hbm"], "GB/s"
+    else:
+        achieved, peak, ru = fl / dur_s / 1e12, tensor_peak(pkind, pk), "TFLOP/s"
+    return {"bound": bound, "kernel": name, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": ru,
+            "frac": round(achieved / peak, 4), "peak_source": pk["src"] + (" (burst)" if bound == "tensor" else ""),
+            "algorithmic": by if bound == "hbm" else fl,
+            "traffic": traffic_for(name, workload, gemv_m if workload == "nvfp4_decode_gemv_Mx28672x8192" else None),
+            "ms": round(float(op_ms[d]), 5)}
+
+
+def config_entry(wl, t, pk, workload, gemv_m=None):
+    """One configuration's figures for the line: its step time (L2 flushed and
+    warm), throughput in its unit, per-op split and roofline."""
+    unit, per_step = wl.units
+    return {"us": round(t["cold_ms"] * 1e3, 2), "us_warm_l2": round(t["warm_ms"] * 1e3, 2),
+            "value": round(per_step / (t["cold_ms"] / 1e3), 2), "unit": unit,
+            "per_op_us": {wl.ops()[j][0]: round(float(t["op_ms"][j]) * 1e3, 2) for j in range(len(wl.ops()))},
+            "roofline": roofline(wl, t["op_ms"], pk, workload, gemv_m)}
+
+
 def run_bsq(args, rank, world, dev_index):
     import torch
     from block_scaled_precision_packed_gb300 import bsq
@@ -279,140 +417,97 @@ def run_bsq(args, rank, world, dev_index):
     dev = torch.device("cuda", dev_index)
     bsq.load()
     pk = peaks()
-    wl = Workload(args.workload, dev, gemv_m=args.gemv_m)
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    # after the write, a read of a second buffer of the same size leaves L2
-    # holding clean lines, so the step does not pay for the flush's write-backs
-    flush_b = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
     dist = None
     if world > 1:
         import torch.distributed as dist
-    ops = wl.ops()
-
-    # The step is captured once as a CUDA graph and replayed: the timed region
-    # measures device time, not the host's launch rate.  The timed graph has
-    # event nodes only at its two ends; a second capture with an event node
-    # after every op, replayed for the same number of steps after the timed
-    # region, gives the per-op split (its event nodes add a little time per op,
-    # so the split slightly overstates each op).  The L2 flush runs outside the
-    # graphs, before every step.
-    n_ops = len(ops)
-    with torch.cuda.stream(stream):
-        for i in range(2):
-            wl.step(stream)                     # loads kernels before capture
-    torch.cuda.synchronize()
-
-    def capture(per_op):
-        # external events become event-record nodes inside the captured graph
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ops + 1)]
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            evs[0].record(stream)
-            for j, (_, fn, *_r) in enumerate(ops):
-                fn(stream)
-                if per_op or j == n_ops - 1:
-                    evs[j + 1].record(stream)
-        return graph, evs
-
-    bsq.reset_launch_counts()
-    graph, evs = capture(False)
-    launches_per_step = sum(bsq.launch_count(k) for k in bsq.KERNEL_IDS)
-    graph_ops, evs_ops = capture(True)
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            for g in (graph, graph_ops):
-                flush.fill_(i)
-                g.replay()
-    torch.cuda.synchronize()
-
-    def flushed_replay(g, i):
-        with torch.cuda.stream(stream):
-            flush.fill_(i + 1000)
-            torch.sum(flush_b, dim=0, dtype=torch.int64, out=flush_sink)
-            g.replay()
-        stream.synchronize()
-
-    # ---- timed region: K steps, L2 flushed before each ----
-    step_ms_all = np.zeros(args.steps)
-    op_ms = np.zeros((args.steps, n_ops))
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
+    timer = Timer(dev, stream, args, dist)
+    cache = {}
+    wl = Workload(args.workload, dev, gemv_m=args.gemv_m, cache=cache)
     with ClockSampler(dev_index) as clk:
-        for i in range(args.steps):
-            flushed_replay(graph, i)
-            step_ms_all[i] = evs[0].elapsed_time(evs[n_ops])
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        # per-op split (same flush, the instrumented capture)
-        for i in range(args.steps):
-            flushed_replay(graph_ops, i)
-            for j in range(n_ops):
-                op_ms[i, j] = evs_ops[j].elapsed_time(evs_ops[j + 1])
-        torch.cuda.synchronize()
-    launches = launches_per_step * args.steps
-    if dist:
-        dist.barrier()
-    step_ms = max_over_ranks(float(step_ms_all.mean()), dist, dev)
+        t = timer.run(wl)
     unit, per_step = wl.units
+    step_ms = t["cold_ms"]
     value = job_throughput(per_step, world, step_ms)
+    roof = roofline(wl, t["op_ms"], pk, args.workload, args.gemv_m)
+    per_op = {wl.ops()[j][0]: round(float(t["op_ms"][j]) * 1e3, 2) for j in range(len(wl.ops()))}
+    launches = t["launches_per_step"] * args.steps
+    e2e = end_to_end(wl, timer, args, dist, dev, per_step, world)
+    flush, flush_b, flush_sink = timer.flush, timer.flush_b, timer.flush_sink
+    extras = {}
+    if args.workload == "w6a8_e4m3xe2m3_4096x14336x4096":
+        extras["quantizer_small_m_us"] = small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args)
+    if args.workload == "mxfp6_e3m2_w6a6_128x4096x4096":
+        extras.update(w6a6_next_rows(wl, dev, stream, timer, args, pk))
+    configs = None
+    if args.all_configs:
+        del wl
+        configs = {}
+        for M in (1, 8, 32):
+            w = Workload("nvfp4_decode_gemv_Mx28672x8192", dev, gemv_m=M, cache=cache)
+            configs.setdefault("nvfp4_decode_gemv_Mx28672x8192", {})[f"M={M}"] = \
+                config_entry(w, timer.run(w), pk, "nvfp4_decode_gemv_Mx28672x8192", M)
+            del w
+        cache.clear()
+        w = Workload("w6a8_e4m3xe2m3_4096x14336x4096", dev)
+        e = config_entry(w, timer.run(w), pk, "w6a8_e4m3xe2m3_4096x14336x4096")
+        e["quantizer_small_m_us"] = small_m_quantizer_us(w, dev, stream, flush, flush_b, flush_sink, args)
+        configs["w6a8_e4m3xe2m3_4096x14336x4096"] = e
+        del w
+        w = Workload("nvfp4_gemv_1x256x256", dev)
+        configs["nvfp4_gemv_1x256x256"] = config_entry(w, timer.run(w), pk, "nvfp4_gemv_1x256x256")
+        del w
+        w = Workload("mxfp6_e3m2_w6a6_128x4096x4096", dev)
+        e = config_entry(w, timer.run(w), pk, "mxfp6_e3m2_w6a6_128x4096x4096")
+        e["next"] = w6a6_next_rows(w, dev, stream, timer, args, pk)
+        configs["mxfp6_e3m2_w6a6_128x4096x4096"] = e
+        del w
+    return dict(value=value, unit=unit, step_ms=step_ms, warm_ms=t["warm_ms"], roofline=roof, per_op_us=per_op,
+                e2e=e2e, launches=launches, clocks=clk.summary(), extras=extras, configs=configs)
 
-    # dominant op and its roofline
-    mean_op = op_ms.mean(axis=0)
-    d = int(np.argmax(mean_op))
-    name, _, by, fl, bound, pkind = ops[d]
-    dur_s = mean_op[d] / 1e3
-    if bound == "hbm":
-        achieved, peak, ru = by / dur_s / 1e9, pk["hbm"], "GB/s"
-    else:
-        achieved, peak, ru = fl / dur_s / 1e12, tensor_peak(pkind, pk), "TFLOP/s"
-    roof = {"bound": bound, "kernel": name, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": ru,
-            "frac": round(achieved / peak, 4), "peak_source": pk["src"] + (" (burst)" if bound == "tensor" else ""),
-            "algorithmic": by if bound == "hbm" else fl,
-            "traffic": traffic_for(name, args.workload,
-                                   args.gemv_m if args.workload == "nvfp4_decode_gemv_Mx28672x8192" else None),
-            "ms": round(float(mean_op[d]), 5)}
-    per_op = {ops[j][0]: round(float(mean_op[j]) * 1e3, 2) for j in range(n_ops)}
 
-    # ---- end to end through the public API with host buffers ----
-    e2e = None
-    if wl.host_in:
-        # flat 16-bit views of both sides (any operand dtype of even byte size)
-        pinned = {k: torch.from_numpy(np.ascontiguousarray(v).reshape(-1).view(np.int16)).pin_memory()
-                  for k, v in wl.host_in.items()}
-        dst = {k: getattr(wl, k).reshape(-1).view(torch.int16) for k in pinned}
-        yh = torch.empty(wl.y.shape, dtype=wl.y.dtype).pin_memory()
-        h2d = sum(v.numel() * 2 for v in pinned.values())
-        d2h = wl.y.numel() * wl.y.element_size()
-        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup + args.steps):
-                flush.fill_(i)
-                if i >= args.warmup:
-                    e_ev[i - args.warmup][0].record(stream)
-                for k in pinned:
-                    dst[k].copy_(pinned[k], non_blocking=True)
-                wl.step(stream)
-                yh.copy_(wl.y, non_blocking=True)
-                if i >= args.warmup:
-                    e_ev[i - args.warmup][1].record(stream)
-        torch.cuda.synchronize()
-        e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in e_ev])), dist, dev)
-        e2e = {"value": round(job_throughput(per_step, world, e_ms), 3), "unit": unit, "ms_per_step": round(e_ms, 4),
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    small_m = small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) \
-        if args.workload == "w6a8_e4m3xe2m3_4096x14336x4096" else None
-    w6a6 = args.workload == "mxfp6_e3m2_w6a6_128x4096x4096"
-    fused_act = fused_act_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
-    containers = byte_container_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
-    grouped = grouped_moe_us(wl, dev, stream, flush, flush_b, flush_sink, args, peaks()) if w6a6 else None
-    quant_a = fused_quant_a_gemm_us(wl, dev, stream, flush, flush_b, flush_sink, args) if w6a6 else None
-    return dict(value=value, unit=unit, step_ms=step_ms, roofline=roof, per_op_us=per_op, e2e=e2e,
-                launches=launches, clocks=clk.summary(), wl=wl, small_m=small_m, fused_act=fused_act,
-                containers=containers, grouped=grouped, quant_a=quant_a)
+def end_to_end(wl, timer, args, dist, dev, per_step, world):
+    """The step through the public API with host buffers: every step copies
+    its inputs in from pinned host memory and its output back (L2 flushed
+    before each step as in the timed region)."""
+    import torch
+    if not wl.host_in:
+        return None
+    stream = timer.stream
+    # flat 16-bit views of both sides (any operand dtype of even byte size)
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v).reshape(-1).view(np.int16)).pin_memory()
+              for k, v in wl.host_in.items()}
+    dst = {k: getattr(wl, k).reshape(-1).view(torch.int16) for k in pinned}
+    yh = torch.empty(wl.y.shape, dtype=wl.y.dtype).pin_memory()
+    h2d = sum(v.numel() * 2 for v in pinned.values())
+    d2h = wl.y.numel() * wl.y.element_size()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            timer.flush.fill_(i)
+            if i >= args.warmup:
+                e_ev[i - args.warmup][0].record(stream)
+            for k in pinned:
+                dst[k].copy_(pinned[k], non_blocking=True)
+            wl.step(stream)
+            yh.copy_(wl.y, non_blocking=True)
+            if i >= args.warmup:
+                e_ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in e_ev])), dist, dev)
+    return {"value": round(job_throughput(per_step, world, e_ms), 3), "unit": wl.units[0],
+            "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def w6a6_next_rows(wl, dev, stream, timer, args, pk):
+    """The W6A6 layer's next rows of the path: the fused activation quantizer,
+    the byte-container quantizer, the grouped (MoE) layer and the GEMM with the
+    activation quantizer inside it."""
+    f, fb, fs = timer.flush, timer.flush_b, timer.flush_sink
+    return {"fused_activation_quantizer": fused_act_quantizer_us(wl, dev, stream, f, fb, fs, args),
+            "byte_container_quantizer": byte_container_quantizer_us(wl, dev, stream, f, fb, fs, args),
+            "grouped_moe": grouped_moe_us(wl, dev, stream, f, fb, fs, args, pk),
+            "gemm_with_fused_activation_quantizer": fused_quant_a_gemm_us(wl, dev, stream, f, fb, fs, args)}
 
 
 def graph_call_us(fn, stream, flush, flush_b, flush_sink, args):
@@ -593,95 +688,157 @@ def small_m_quantizer_us(wl, dev, stream, flush, flush_b, flush_sink, args):
 
 
 # ----------------------------------------------------------- CPU oracle arm ---
-def oracle_sample(workload, rows_w):
-    """Time the oracle on a bounded sample of one step; returns (seconds for a
-    full step, extrapolated; description)."""
-    import oracle as O
-    from block_scaled_precision_packed_gb300 import synthetic as S
-    cfg = S.WORKLOADS[workload]
-    if workload == "mxfp6_e3m2_w6a6_128x4096x4096":
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+# Output rows x weight rows of the product the oracle computes per sample: a
+# single-core sample (a few seconds of CPU work) and a 16x larger one for all
+# host cores, taken on the workload's own quantized operands.
+ORACLE_SAMPLE = {1: (16, 256), 0: (32, 2048)}
+
+
+class OracleSample:
+    """A bounded sample of one step of a workload for the CPU oracle: the
+    operands are the oracle's own quantization of the workload's bf16 inputs
+    (only the rows the sample needs; the tensor amax spans the whole tensor),
+    the product is a block of output rows x weight rows, and the step's time is
+    the sample's scaled by the step's outputs over the sample's."""
+
+    def __init__(self, workload, threads, gemv_m=32):
+        import oracle as O
+        from block_scaled_precision_packed_gb300 import synthetic as S
+        self.O, self.workload, self.threads = O, workload, threads
+        cfg = S.WORKLOADS[workload]
+        mr, nr = ORACLE_SAMPLE[1 if threads == 1 else 0]
+        if workload == "nvfp4_gemv_1x256x256":
+            M, N, K = cfg["M"], cfg["N"], cfg["K"]
+            self.x = S.normal_bf16((M, K), cfg["x_std"], cfg["seed"])
+            self.W = S.random_words((N, K // 8), cfg["seed"] + 1)
+            self.sw = S.choice_bytes(O.scale_bytes(N, K // 16), cfg["seed"] + 2, S.UE4M3_POW2_M4_TO_P4)
+            self.mr, self.nr, self.scale = M, N, 1.0
+            self.desc = f"the whole product [{M},{N}], K = {K}"
+            self.args = (M, N, K)
+            return
+        if workload == "nvfp4_decode_gemv_Mx28672x8192":
+            M, N, K = gemv_m, cfg["N"], cfg["K"]
+            w = S.normal_bf16((N, K), cfg["w_std"], cfg["seed"] + 1)
+            rows = np.arange(nr, dtype=np.int64)
+            self.W, sb, g = O.quantize_nvfp4_rows(w, rows)
+            self.sw = _swizzle(O, sb)
+            self.g = g
+            self.x = S.normal_bf16((M, K), cfg["x_std"], cfg["seed"] + 2 + M)
+            self.mr, self.nr, self.scale = M, nr, N / nr
+            self.desc = f"GEMV outputs [{M},{nr}] of [{M},{N}] (weight rows quantized by the oracle), scaled by {N}/{nr}"
+            self.args = (M, nr, K)
+            return
         M, N, K = cfg["M"], cfg["N"], cfg["K"]
-        a = S.normal_bf16((M, K), cfg["a_std"], cfg["seed"] + 1, cfg["outlier_frac"], cfg["outlier_mult"])
-        w = S.normal_bf16((N, K), cfg["w_std"], cfg["seed"] + 2, cfg["outlier_frac"], cfg["outlier_mult"])
-        rows = np.arange(rows_w, dtype=np.int64)
+        mr = min(mr, M)
+        a = S.normal_bf16((M, K), cfg["a_std"], cfg["seed"] + 1, cfg.get("outlier_frac", 0.0),
+                          cfg.get("outlier_mult", 20.0))
+        w = S.normal_bf16((N, K), cfg["w_std"], cfg["seed"] + 2, cfg.get("outlier_frac", 0.0),
+                          cfg.get("outlier_mult", 20.0))
+        ra, rw = np.arange(mr, dtype=np.int64), np.arange(nr, dtype=np.int64)
+        self.a, self.w, self.rw = a, w, rw
+        if workload == "nvfp4_prefill_gemm_8192":
+            self.A, sa, self.ga = O.quantize_nvfp4_rows(a, ra)
+            self.W, sw, self.gw = O.quantize_nvfp4_rows(w, rw)
+        else:
+            fa, fw = (O.E3M2, O.E3M2) if workload.startswith("mxfp6") else (O.E4M3, O.E2M3)
+            self.fa, self.fw = fa, fw
+            self.A, sa, self.ga = O.quantize_mx_rows(a, fa, ra)
+            self.W, sw, self.gw = O.quantize_mx_rows(w, fw, rw)
+        self.sa, self.sw = _swizzle(O, sa), _swizzle(O, sw)
+        self.mr, self.nr, self.scale = mr, nr, (M / mr) * (N / nr)
+        self.desc = (f"GEMM outputs [{mr},{nr}] of [{M},{N}] on the oracle's quantization of the workload's "
+                     f"operands, scaled by area" + (f"; plus quantize A whole and W rows 0..{nr - 1} (scaled by "
+                                                    f"{N}/{nr})" if workload.startswith("mxfp6") else ""))
+        self.args = (mr, nr, K)
+        self.NW = N
+
+    def step_seconds(self):
+        """One sample's time scaled to the full step."""
+        O, th = self.O, self.threads
         t0 = time.perf_counter()
-        ca, sa, ga = O.quantize_mx(a, O.E3M2)
-        t1 = time.perf_counter()
-        cw, uw, gw = O.quantize_mx_rows(w, O.E3M2, rows)
-        t2 = time.perf_counter()
-        sw = np.zeros(O.scale_bytes(rows_w, K // 32), np.uint8)
-        for r in range(rows_w):
-            for b in range(K // 32):
-                sw[O.swz_offset(r, b, K // 32)] = uw[r, b]
-        t3 = time.perf_counter()
-        O.gemm_mx(ca, O.E3M2, sa, ga, cw, O.E3M2, sw, gw, M, rows_w, K, threads=1)
-        t4 = time.perf_counter()
-        full = (t1 - t0) + (t2 - t1) * N / rows_w + (t4 - t3) * N / rows_w
-        return full, f"quantize A [{M},{K}] whole, W rows 0..{rows_w - 1} of {N} (tensor amax over all of W), " \
-                     f"GEMM outputs [{M},{rows_w}]; W quantize and GEMM scaled by {N}/{rows_w}"
-    if workload in ("nvfp4_decode_gemv_Mx28672x8192", "nvfp4_gemv_1x256x256"):
-        N, K = cfg["N"], cfg["K"]
-        M = 32 if "Ms" in cfg else cfg["M"]
-        rows_w = min(rows_w, N)
-        x = S.normal_bf16((M, K), cfg["x_std"], cfg["seed"] + 2)
-        W = S.random_words((rows_w, K // 8), cfg["seed"] + 1)
-        sc = S.choice_bytes(O.scale_bytes(rows_w, K // 16), cfg["seed"] + 2, list(range(0x20, 0x60)))
-        t0 = time.perf_counter()
-        O.gemv_nvfp4(x, W, sc, 1.0, M, rows_w, K, threads=1)
-        t1 = time.perf_counter()
-        return (t1 - t0) * N / rows_w, f"GEMV outputs [{M},{rows_w}] of [{M},{N}], scaled by {N}/{rows_w}"
-    # GEMM workloads: a block of output rows against a block of W rows
-    M, N, K = cfg["M"], cfg["N"], cfg["K"]
-    mr = 16
-    if workload == "nvfp4_prefill_gemm_8192":
-        A = S.random_words((mr, K // 8), 1)
-        W = S.random_words((rows_w, K // 8), 2)
-        sa = S.choice_bytes(O.scale_bytes(mr, K // 16), 3, list(range(0x20, 0x60)))
-        sw = S.choice_bytes(O.scale_bytes(rows_w, K // 16), 4, list(range(0x20, 0x60)))
-        t0 = time.perf_counter()
-        O.gemm_nvfp4(A, sa, 1.0, W, sw, 1.0, mr, rows_w, K, threads=1)
-    else:
-        A = S.random_bytes(mr * K, 1).reshape(mr, K) & 0x7E
-        W = S.random_bytes(rows_w * 3 * K // 4, 2).reshape(rows_w, 3 * K // 4)
-        sa = S.choice_bytes(O.scale_bytes(mr, K // 32), 3, list(range(120, 134)))
-        sw = S.choice_bytes(O.scale_bytes(rows_w, K // 32), 4, list(range(120, 134)))
-        t0 = time.perf_counter()
-        O.gemm_mx(A, O.E4M3, sa, 1.0, W, O.E2M3, sw, 1.0, mr, rows_w, K, threads=1)
-    t1 = time.perf_counter()
-    return (t1 - t0) * (M / mr) * (N / rows_w), f"GEMM outputs [{mr},{rows_w}] of [{M},{N}], scaled by area"
+        if self.workload == "nvfp4_gemv_1x256x256":
+            O.gemv_nvfp4(self.x, self.W, self.sw, 0.5, *self.args, threads=th)
+        elif self.workload == "nvfp4_decode_gemv_Mx28672x8192":
+            O.gemv_nvfp4(self.x, self.W, self.sw, self.g, *self.args, threads=th)
+        elif self.workload == "nvfp4_prefill_gemm_8192":
+            O.gemm_nvfp4(self.A, self.sa, self.ga, self.W, self.sw, self.gw, *self.args, threads=th)
+        else:
+            O.gemm_mx(self.A, self.fa, self.sa, self.ga, self.W, self.fw, self.sw, self.gw, *self.args, threads=th)
+        t = (time.perf_counter() - t0) * self.scale
+        if self.workload.startswith("mxfp6"):          # the W6A6 step quantizes both operands too
+            t0 = time.perf_counter()
+            O.quantize_mx(self.a, self.fa)
+            t1 = time.perf_counter()
+            O.quantize_mx_rows(self.w, self.fw, self.rw)
+            t += (t1 - t0) + (time.perf_counter() - t1) * self.NW / self.rw.size
+        return t
+
+
+def _swizzle(O, plain):
+    rows, blocks = plain.shape
+    buf = np.zeros(O.scale_bytes(rows, blocks), np.uint8)
+    for r in range(rows):
+        for b in range(blocks):
+            buf[O.swz_offset(r, b, blocks)] = plain[r, b]
+    return buf
+
+
+def cpu_baseline(workload, gemv_m, unit):
+    """The oracle as it stands on this host: one sample at 1 core, one (16x
+    larger) at every core; value = the step's units per extrapolated second."""
+    import oracle as O
+    O.build()
+    per_step = per_step_units(workload, gemv_m)
+    out = {"kind": "oracle", "unit": unit}
+    for threads, key in ((1, "one_core"), (0, "all_cores")):
+        smp = OracleSample(workload, threads, gemv_m)
+        t = smp.step_seconds()
+        out[key] = {"value": per_step / t, "cores": 1 if threads == 1 else host_cores(),
+                    "ms_per_step_extrapolated": round(t * 1e3, 1), "sample": smp.desc}
+    # the headline figure: all host cores
+    out.update(value=out["all_cores"]["value"], cores=out["all_cores"]["cores"], sample=out["all_cores"]["sample"],
+               host_cpu_count=os.cpu_count())
+    return out
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="bsq", choices=["bsq", "reference"])
-    ap.add_argument("--workload", default=WORKLOADS[0], choices=WORKLOADS)
+    ap.add_argument("--workload", default=None, choices=WORKLOADS,
+                    help=f"one workload alone (default: {HEADLINE} with every other configuration in 'configs')")
     ap.add_argument("--gemv-m", type=int, default=32, choices=[1, 8, 32])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    args.all_configs = args.workload is None
+    if args.workload is None:
+        args.workload = HEADLINE
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    wl_cfg = {"workload": args.workload}
-    if args.workload == "nvfp4_decode_gemv_Mx28672x8192":
-        wl_cfg["M"] = args.gemv_m
+    wl_cfg = workload_config(args.workload, args.gemv_m)
+    unit = "GB/s" if "gemv" in args.workload else "TFLOP/s"
 
     if args.impl == "reference":
-        # The CPU oracle as it stands, on this arm's workload and metric; rank 0 only.
+        # The CPU oracle as it stands, on this arm's workload, metric and sample
+        # (every host core); rank 0 only.
         if rank != 0:
             return
         import oracle as O
         O.build()
-        rows = 8
-        unit = "GB/s" if "gemv" in args.workload else "TFLOP/s"
-        times, desc = [], ""
+        smp = OracleSample(args.workload, 0, args.gemv_m)
+        times = []
         for i in range(args.warmup + args.steps):
-            t, desc = oracle_sample(args.workload, rows)
+            t = smp.step_seconds()
             if i >= args.warmup:
                 times.append(t)
         step_s = float(np.mean(times))
@@ -690,8 +847,9 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(args.workload),
-                "data": "synthetic", "config": wl_cfg,
-                "cpu_baseline": {"kind": "oracle", "value": v, "unit": unit, "cores": 1, "sample": desc},
+                "data": "synthetic (seeded; shapes and distributions of the workload)", "config": wl_cfg,
+                "cpu_baseline": {"kind": "oracle", "value": v, "unit": unit, "cores": host_cores(),
+                                 "sample": smp.desc + f"; extrapolated per step, {args.steps} steps timed"},
                 "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -705,38 +863,33 @@ def main():
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    cpu = None
-    if not args.no_cpu_baseline:
-        import oracle as O
-        O.build()
-        t, desc = oracle_sample(args.workload, 256 if args.workload.startswith("mxfp6") else 16)
-        per_step = per_step_units(args.workload, args.gemv_m)
-        cpu = {"kind": "oracle", "value": per_step / t, "unit": r["unit"], "cores": 1, "sample": desc,
-               "ms_per_step_extrapolated": round(t * 1e3, 1)}
+    cpu = None if args.no_cpu_baseline else cpu_baseline(args.workload, args.gemv_m, r["unit"])
     line = {"metric": METRIC, "value": round(r["value"], 3), "unit": r["unit"], "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["step_ms"], 5),
+            "ms_per_step_warm_l2": round(r["warm_ms"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(args.workload),
             "data": "synthetic (seeded; shapes and distributions of the workload)",
-            "config": dict(wl_cfg, l2="flushed before every timed step (256 MiB write, then a read pass)",
-                           timing="step captured as a CUDA graph (event nodes at its ends only) and replayed; "
-                                  "per-op split from a second capture with an event node after each op",
-                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "config": dict(wl_cfg, parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "roofline": r["roofline"], "per_op_us": r["per_op_us"], "e2e": r["e2e"],
             "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "cpu_baseline": cpu}
-    if r["small_m"] is not None:
-        line["quantizer_small_m_us"] = r["small_m"]
-    if r["fused_act"] is not None:
-        line["fused_activation_quantizer"] = r["fused_act"]
-    if r["containers"] is not None:
-        line["byte_container_quantizer"] = r["containers"]
-    if r["grouped"] is not None:
-        line["grouped_moe"] = r["grouped"]
-    if r["quant_a"] is not None:
-        line["gemm_with_fused_activation_quantizer"] = r["quant_a"]
+    line.update(r["extras"])
+    if r["configs"] is not None:
+        line["configs"] = r["configs"]
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def workload_config(workload, gemv_m):
+    c = {"workload": workload,
+         "l2": "flushed before every timed step (256 MiB write, then a read pass); warm-L2 figures replay "
+               "without the flush",
+         "timing": "step captured as a CUDA graph (event nodes at its ends only) and replayed; per-op split from "
+                   "a second capture with an event node after each op"}
+    if workload == "nvfp4_decode_gemv_Mx28672x8192":
+        c["M"] = gemv_m
+    return c
 
 
 def per_step_units(workload, gemv_m):

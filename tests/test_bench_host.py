@@ -36,8 +36,30 @@ def test_reference_arm_line_on_a_small_workload():
     assert r.returncode == 0, r.stderr[-2000:]
     line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == bench.host_cores()
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    # the same configuration object as this arm's line
+    assert line["config"] == bench.workload_config("nvfp4_gemv_1x256x256", 32)
+
+
+def test_default_workload_is_the_largest_configuration():
+    """The headline line is the nvfp4 prefill GEMM 8192^3 (the largest
+    single-GPU configuration); the others are reported under 'configs'."""
+    assert bench.HEADLINE == "nvfp4_prefill_gemm_8192" == bench.WORKLOADS[0]
+    from block_scaled_precision_packed_gb300 import synthetic as S
+    flops = {w: 2 * S.WORKLOADS[w]["M"] * S.WORKLOADS[w]["N"] * S.WORKLOADS[w]["K"]
+             for w in S.WORKLOADS if "M" in S.WORKLOADS[w]}
+    assert max(flops, key=flops.get) == bench.HEADLINE
+
+
+def test_oracle_sample_one_core_and_all_cores_share_the_product():
+    """The cpu_baseline legs and the reference arm time the same product on
+    the oracle's own quantization of the workload's inputs; the all-core sample
+    is the larger one."""
+    one = bench.OracleSample("nvfp4_gemv_1x256x256", 1)
+    every = bench.OracleSample("nvfp4_gemv_1x256x256", 0)
+    assert one.desc == every.desc and one.step_seconds() > 0 and every.step_seconds() > 0
+    assert bench.ORACLE_SAMPLE[0][0] * bench.ORACLE_SAMPLE[0][1] > bench.ORACLE_SAMPLE[1][0] * bench.ORACLE_SAMPLE[1][1]
 
 
 def test_traffic_counts_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
