@@ -100,16 +100,12 @@ struct Cfg {
 constexpr int kMaxGroups = 256;
 
 struct GemmArgs {
-    const uint8_t* sA;
-    const uint8_t* sW;
     const float* gA;           // grouped: [G]
     const float* gW;           // grouped: [G]
     void* Y;
     int64_t M, N, K;           // grouped: M = R, the rows per group of A
     const int32_t* row_counts; // grouped: [G] valid A rows per group
     int64_t G;                 // groups (1 when not grouped)
-    int64_t sa_group, sw_group;   // grouped: bytes of one group's scale buffer
-    int64_t cpd4;          // scale atoms along K per 128-row tile (pad4(blocks)/4)
     int out_bf16;
     uint32_t idesc;        // instruction descriptor without the scale-id fields
     uint32_t tx_ab;        // TMA transaction bytes of one stage's A and W tiles (W only when A is quantized here)
@@ -166,7 +162,8 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
 //            shared memory -- no workspace, no atomics.
 template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const GemmArgs args) {
+gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+            const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSW, const GemmArgs args) {
     using C = Cfg<NVF4, BN, (QA >= 0), PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -226,6 +223,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmW);
+        if constexpr (QA < 0) prefetch_tmap(&tmSA);
+        prefetch_tmap(&tmSW);
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -308,33 +307,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 unit_at(tile, grp, mb, nb);
                 const int64_t a_row0 = grp * M + mb * C::kTileM + prank * kBM;
                 const int64_t w_row0 = grp * N + nb * BN + prank * C::kRowsB;
-                // this CTA's 128-row scale tile of A (rows past M: any finite scales)
-                int64_t a_rt = mb * (C::kTileM / kBM) + prank;
-                if (a_rt >= rt_total_a) a_rt = mb * (C::kTileM / kBM);
-                const uint8_t* sa_base = args.sA + grp * args.sa_group;
-                const uint8_t* sw_base = args.sW + grp * args.sw_group;
+                // this CTA's 128-row scale tile of A (past M: zeros)
+                const int64_t a_rt = mb * (C::kTileM / kBM) + prank;
                 for (int64_t ks = ks_begin; ks < ks_end; ++ks) {
                     if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, args.err, abort_flag, kErrGemmProducer)) {
                         ok = false;
                         break;
                     }
                     const int64_t kg = ks * C::kAtomsPerStage;             // first scale atom along K
-                    const int natoms = (int)imin64(C::kAtomsPerStage, args.cpd4 - kg);
                     // The scale atoms go first, on their own barrier: the
                     // scale-factor warps move them into TMEM while the
-                    // operand tiles are still in flight.
+                    // operand tiles are still in flight.  One tensor-map load
+                    // per operand ({128 words, atoms, row tiles} of the
+                    // atom-contiguous scale buffer); atoms past K and row tiles
+                    // past the operand's rows read as zeros.
                     const uint32_t lb = smem_u32(sf_land + stage);
-                    mbar_arrive_expect_tx(lb, (uint32_t)natoms * kAtom * ((QA >= 0 ? 0 : 1) + C::kRowTilesB));
+                    mbar_arrive_expect_tx(lb, (uint32_t)((QA >= 0 ? 0 : C::kSfaBytes) + C::kSfbBytes));
                     if constexpr (QA < 0)          // else the epilogue warps make A and its scale atom
-                        bulk_load(smem_u32(sSfa + stage * C::kSfaBytes), sa_base + (a_rt * args.cpd4 + kg) * kAtom,
-                                  natoms * kAtom, lb);
-#pragma unroll
-                    for (int rt = 0; rt < C::kRowTilesB; ++rt) {
-                        int64_t wrt = nb * C::kRowTilesB + rt;
-                        if (wrt >= rt_total) wrt = nb * C::kRowTilesB;    // rows beyond N: any finite scales
-                        bulk_load(smem_u32(sSfb + stage * C::kSfbBytes + rt * C::kAtomsPerStage * kAtom),
-                                  sw_base + (wrt * args.cpd4 + kg) * kAtom, natoms * kAtom, lb);
-                    }
+                        tma_load_3d(smem_u32(sSfa + stage * C::kSfaBytes), &tmSA, lb, 0, (int32_t)kg,
+                                    (int32_t)(grp * rt_total_a + a_rt));
+                    tma_load_3d(smem_u32(sSfb + stage * C::kSfbBytes), &tmSW, lb, 0, (int32_t)kg,
+                                (int32_t)(grp * rt_total + nb * C::kRowTilesB));
                     const uint32_t fb = smem_u32(full + stage);
                     mbar_arrive_expect_tx(fb, args.tx_ab);
                     const int32_t kx = (int32_t)(ks * (NVF4 ? 128 : C::kStageK));   // bytes (nvfp4) / elements
@@ -843,6 +836,28 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint
     return r == CUDA_SUCCESS;
 }
 
+// Tensor map over a block-scale buffer as 32-bit words: {128 words of a
+// 512-byte atom, atoms along K (cpd4), 128-row tiles}; one load of box
+// {128, box_atoms, box_tiles} brings a stage's atoms of one or two row tiles
+// into shared memory in [tile][atom][512 B] order, zeros past either end.
+bool scale_map(CUtensorMap* map, const uint8_t* base, int64_t row_tiles, int64_t cpd4, uint32_t box_atoms,
+               uint32_t box_tiles) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)cpd4, (cuuint64_t)row_tiles};
+    const cuuint64_t strides[2] = {(cuuint64_t)kAtom, (cuuint64_t)(cpd4 * kAtom)};
+    const cuuint32_t box[3] = {128, box_atoms, box_tiles};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The four tensor maps of a launch: operands A and W, their scale buffers.
+struct Maps {
+    CUtensorMap a, w, sa, sw;
+};
+
 // Tensor map of one operand: nvfp4 as raw bytes (K/2 per row), fp6 through
 // the 16U6_ALIGN16B unpacking type (K codes per row), e4m3 as bytes.
 bool operand_map(CUtensorMap* map, const void* p, int fmt, bool nvf4, int64_t rows, int64_t K, uint32_t box_rows) {
@@ -855,8 +870,7 @@ bool operand_map(CUtensorMap* map, const void* p, int fmt, bool nvf4, int64_t ro
 }
 
 template <bool NVF4, int BN, int SPLIT, bool GROUPED = false, int QA = -1, bool PAIR = false>
-bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a,
-                       cudaStream_t s) {
+bsq_status launch_gemm(const DeviceInfo* info, const Maps& mp, const GemmArgs& a, cudaStream_t s) {
     using C = Cfg<NVF4, BN, (QA >= 0), PAIR>;
     auto kernel = gemm_kernel<NVF4, BN, SPLIT, GROUPED, QA, PAIR>;
     static std::once_flag flags[64];
@@ -921,7 +935,7 @@ bsq_status launch_gemm(const DeviceInfo* info, const CUtensorMap& ta, const CUte
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    if (cudaLaunchKernelEx(&cfg, kernel, ta, tw, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, mp.a, mp.w, mp.sa, mp.sw, a) != cudaSuccess) {
         (void)cudaGetLastError();
         return BSQ_ERR_CUDA;
     }
@@ -952,15 +966,18 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
         for (int sp = 8; sp >= 2; sp /= 2)
             if (tiles128 * sp <= info->num_sms && nks >= sp) { split = sp; break; }
     const uint32_t rows_b = pair ? 128u : (uint32_t)bn;     // W rows one CTA stages per tile
-    CUtensorMap ta, tw;
-    if (!operand_map(&ta, A, fa, nvf4, M, K, kBM) || !operand_map(&tw, W, fw, nvf4, N, K, rows_b))
+    const int64_t cpd4 = pad_to(K / (nvf4 ? 16 : 32), 4) / 4;
+    const uint32_t stage_atoms = nvf4 ? 4u : 1u;
+    Maps mp;
+    if (!operand_map(&mp.a, A, fa, nvf4, M, K, kBM) || !operand_map(&mp.w, W, fw, nvf4, N, K, rows_b) ||
+        !scale_map(&mp.sa, sA, pad_to(M, 128) / 128, cpd4, stage_atoms, 1) ||
+        !scale_map(&mp.sw, sW, pad_to(N, 128) / 128, cpd4, stage_atoms, (uint32_t)(bn / 128)))
         return BSQ_ERR_CUDA;
     GemmArgs a;
-    a.sA = sA; a.sW = sW; a.gA = gA; a.gW = gW; a.Y = Y;
+    a.gA = gA; a.gW = gW; a.Y = Y;
     a.M = M; a.N = N; a.K = K;
-    a.row_counts = nullptr; a.G = 1; a.sa_group = 0; a.sw_group = 0;
+    a.row_counts = nullptr; a.G = 1;
     a.qx = nullptr; a.qpartial = nullptr; a.qn_partial = 0; a.qs_global = nullptr;
-    a.cpd4 = pad_to(K / (nvf4 ? 16 : 32), 4) / 4;
     a.out_bf16 = out == BSQ_OUT_BF16;
     a.idesc = make_idesc(nvf4, fa, fw, bn, pair ? 2 * kBM : kBM);
     a.err = info->err;
@@ -970,20 +987,20 @@ bsq_status gemm_launch(const void* A, int fa, const uint8_t* sA, const float* gA
     a.tx_ab = kBM * row_tx(fa) + rows_b * row_tx(fw);
     bsq_status r;
     if (pair) {
-        if (nvf4) r = launch_gemm<true, 256, 1, false, -1, true>(info, ta, tw, a, s);
-        else r = launch_gemm<false, 256, 1, false, -1, true>(info, ta, tw, a, s);
+        if (nvf4) r = launch_gemm<true, 256, 1, false, -1, true>(info, mp, a, s);
+        else r = launch_gemm<false, 256, 1, false, -1, true>(info, mp, a, s);
     } else if (nvf4) {
-        if (bn == 256) r = launch_gemm<true, 256, 1>(info, ta, tw, a, s);
-        else if (split == 8) r = launch_gemm<true, 128, 8>(info, ta, tw, a, s);
-        else if (split == 4) r = launch_gemm<true, 128, 4>(info, ta, tw, a, s);
-        else if (split == 2) r = launch_gemm<true, 128, 2>(info, ta, tw, a, s);
-        else r = launch_gemm<true, 128, 1>(info, ta, tw, a, s);
+        if (bn == 256) r = launch_gemm<true, 256, 1>(info, mp, a, s);
+        else if (split == 8) r = launch_gemm<true, 128, 8>(info, mp, a, s);
+        else if (split == 4) r = launch_gemm<true, 128, 4>(info, mp, a, s);
+        else if (split == 2) r = launch_gemm<true, 128, 2>(info, mp, a, s);
+        else r = launch_gemm<true, 128, 1>(info, mp, a, s);
     } else {
-        if (bn == 256) r = launch_gemm<false, 256, 1>(info, ta, tw, a, s);
-        else if (split == 8) r = launch_gemm<false, 128, 8>(info, ta, tw, a, s);
-        else if (split == 4) r = launch_gemm<false, 128, 4>(info, ta, tw, a, s);
-        else if (split == 2) r = launch_gemm<false, 128, 2>(info, ta, tw, a, s);
-        else r = launch_gemm<false, 128, 1>(info, ta, tw, a, s);
+        if (bn == 256) r = launch_gemm<false, 256, 1>(info, mp, a, s);
+        else if (split == 8) r = launch_gemm<false, 128, 8>(info, mp, a, s);
+        else if (split == 4) r = launch_gemm<false, 128, 4>(info, mp, a, s);
+        else if (split == 2) r = launch_gemm<false, 128, 2>(info, mp, a, s);
+        else r = launch_gemm<false, 128, 1>(info, mp, a, s);
     }
     count_launch(nvf4 ? BSQ_KERNEL_GEMM_NVFP4 : BSQ_KERNEL_GEMM_MX);
     return r;
@@ -999,26 +1016,26 @@ bsq_status gemm_grouped_launch(const void* A, int fa, const uint8_t* sA, const f
     // 256-wide W tiles when the groups' full row blocks would still give every SM one
     const int64_t full256 = G * ((R + kBM - 1) / kBM) * ((N + 255) / 256);
     const int bn = full256 >= info->num_sms ? 256 : 128;
-    CUtensorMap ta, tw;
-    if (!operand_map(&ta, A, fa, nvf4, G * R, K, kBM) || !operand_map(&tw, W, fw, nvf4, G * N, K, (uint32_t)bn))
-        return BSQ_ERR_CUDA;
     const int64_t nblk = K / (nvf4 ? 16 : 32);
+    const int64_t cpd4 = pad_to(nblk, 4) / 4;
+    Maps mp;
+    if (!operand_map(&mp.a, A, fa, nvf4, G * R, K, kBM) || !operand_map(&mp.w, W, fw, nvf4, G * N, K, (uint32_t)bn) ||
+        !scale_map(&mp.sa, sA, G * (pad_to(R, 128) / 128), cpd4, nvf4 ? 4u : 1u, 1) ||
+        !scale_map(&mp.sw, sW, G * (pad_to(N, 128) / 128), cpd4, nvf4 ? 4u : 1u, (uint32_t)(bn / 128)))
+        return BSQ_ERR_CUDA;
     GemmArgs a;
-    a.sA = sA; a.sW = sW; a.gA = gA; a.gW = gW; a.Y = Y;
+    a.gA = gA; a.gW = gW; a.Y = Y;
     a.M = R; a.N = N; a.K = K;
     a.row_counts = row_counts; a.G = G;
     a.qx = nullptr; a.qpartial = nullptr; a.qn_partial = 0; a.qs_global = nullptr;
-    a.sa_group = pad_to(R, 128) * pad_to(nblk, 4);
-    a.sw_group = pad_to(N, 128) * pad_to(nblk, 4);
-    a.cpd4 = pad_to(nblk, 4) / 4;
     a.out_bf16 = out == BSQ_OUT_BF16;
     a.idesc = make_idesc(nvf4, fa, fw, bn);
     a.err = info->err;
     auto row_tx = [&](int f) { return (uint32_t)(nvf4 || f == kE4M3 ? 128 : 96); };
     a.tx_ab = kBM * row_tx(fa) + (uint32_t)bn * row_tx(fw);
     bsq_status r;
-    if (nvf4) r = bn == 256 ? launch_gemm<true, 256, 1, true>(info, ta, tw, a, s) : launch_gemm<true, 128, 1, true>(info, ta, tw, a, s);
-    else r = bn == 256 ? launch_gemm<false, 256, 1, true>(info, ta, tw, a, s) : launch_gemm<false, 128, 1, true>(info, ta, tw, a, s);
+    if (nvf4) r = bn == 256 ? launch_gemm<true, 256, 1, true>(info, mp, a, s) : launch_gemm<true, 128, 1, true>(info, mp, a, s);
+    else r = bn == 256 ? launch_gemm<false, 256, 1, true>(info, mp, a, s) : launch_gemm<false, 128, 1, true>(info, mp, a, s);
     count_launch(nvf4 ? BSQ_KERNEL_GEMM_NVFP4 : BSQ_KERNEL_GEMM_MX);
     return r;
 }
@@ -1039,27 +1056,29 @@ bsq_status gemm_quant_a_launch(const uint16_t* x, int fa, const void* W, int fw,
     int split = 1;
     for (int sp = 8; sp >= 2; sp /= 2)
         if (tiles128 * sp <= info->num_sms && nks >= sp) { split = sp; break; }
-    CUtensorMap tw, tx;
-    if (!operand_map(&tw, W, fw, false, N, K, 128u)) return BSQ_ERR_CUDA;
+    Maps mp;
+    if (!operand_map(&mp.w, W, fw, false, N, K, 128u) ||
+        !scale_map(&mp.sw, sW, pad_to(N, 128) / 128, pad_to(K / 32, 4) / 4, 1, 1))
+        return BSQ_ERR_CUDA;
+    mp.sa = mp.sw;        // A's scales are made in the kernel; this map is never read
     // x [M, K] bf16 as 64-value boxes of 128 rows (128-byte swizzle, zeros past M and K)
-    if (!encode_map(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)(K * 2), 64, 128))
+    if (!encode_map(&mp.a, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)(K * 2), 64, 128))
         return BSQ_ERR_CUDA;
     GemmArgs a;
-    a.sA = nullptr; a.sW = sW; a.gA = nullptr; a.gW = gW; a.Y = Y;
+    a.gA = nullptr; a.gW = gW; a.Y = Y;
     a.M = M; a.N = N; a.K = K;
-    a.row_counts = nullptr; a.G = 1; a.sa_group = 0; a.sw_group = 0;
+    a.row_counts = nullptr; a.G = 1;
     a.qx = x; a.qpartial = partial; a.qn_partial = n_partial; a.qs_global = s_global_a;
-    a.cpd4 = pad_to(K / 32, 4) / 4;
     a.out_bf16 = out == BSQ_OUT_BF16;
     a.idesc = make_idesc(false, fa, fw, 128);
     a.err = info->err;
     a.tx_ab = 128u * (fw == kE4M3 ? 128u : 96u) + (uint32_t)(kBM * 128 * 2);   // the W tile and A's bf16 tile
     bsq_status r;
 #define BSQ_QA_SPLITS(F)                                                            \
-    if (split == 8) r = launch_gemm<false, 128, 8, false, F>(info, tx, tw, a, s);   \
-    else if (split == 4) r = launch_gemm<false, 128, 4, false, F>(info, tx, tw, a, s); \
-    else if (split == 2) r = launch_gemm<false, 128, 2, false, F>(info, tx, tw, a, s); \
-    else r = launch_gemm<false, 128, 1, false, F>(info, tx, tw, a, s);
+    if (split == 8) r = launch_gemm<false, 128, 8, false, F>(info, mp, a, s);   \
+    else if (split == 4) r = launch_gemm<false, 128, 4, false, F>(info, mp, a, s); \
+    else if (split == 2) r = launch_gemm<false, 128, 2, false, F>(info, mp, a, s); \
+    else r = launch_gemm<false, 128, 1, false, F>(info, mp, a, s);
     switch (fa) {
     case kE3M2: BSQ_QA_SPLITS(kE3M2); break;
     case kE2M3: BSQ_QA_SPLITS(kE2M3); break;
