@@ -355,12 +355,31 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 // (bf16 exponent field 113..142; every such bf16 value is an f16 normal).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& ok) {
     const uint32_t lo_e = (w >> 7) & 0xFFu, hi_e = (w >> 23) & 0xFFu;
-    const bool lo_ok = (w & 0x7FFFu) == 0 || (lo_e >= 113 && lo_e <= 142);
-    const bool hi_ok = (w & 0x7FFF0000u) == 0 || (hi_e >= 113 && hi_e <= 142);
+    // exact in f16: zero, an f16 normal, or an f16 subnormal a bf16 value lands
+    // on exactly (exponent field 110..112: 8 significant bits at >= 2^-17)
+    const bool lo_ok = (w & 0x7FFFu) == 0 || (lo_e >= 110 && lo_e <= 142);
+    const bool hi_ok = (w & 0x7FFF0000u) == 0 || (hi_e >= 110 && hi_e <= 142);
     ok = lo_ok && hi_ok;
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
     return r;
+}
+
+// A stage's scale atoms of n_rb consecutive 128-row tiles from rb0: one load of
+// a 2-tile box per pair of tiles, a 1-tile box for an odd remainder, into
+// [tile][atom][512 B] at dst; tiles past the weight's rows and atoms past K
+// read as zeros (the maps are {128 words, atoms, tiles} of the scale buffer).
+__device__ __forceinline__ void load_scale_tiles(uint32_t dst, const CUtensorMap* tmS2, const CUtensorMap* tmS1,
+                                                 uint32_t bar, int i, int rb0, int n_rb) {
+    int j = 0;
+    for (; j + 2 <= n_rb; j += 2) tma_load_3d(dst + (uint32_t)j * 2048u, tmS2, bar, 0, 4 * i, rb0 + j);
+    if (j < n_rb) tma_load_3d(dst + (uint32_t)j * 2048u, tmS1, bar, 0, 4 * i, rb0 + j);
+}
+// Programmatic dependent launch: the prologue above overlaps the previous
+// kernel; nothing that kernel writes is read before this wait.
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 struct Args {
@@ -389,7 +408,8 @@ struct Plan {
 
 template <int NT, int CW>
 __global__ void __launch_bounds__((CW + 1) * 32, 1)
-gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
+gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS2,
+                 const __grid_constant__ CUtensorMap tmS1, const Args args) {
     constexpr int R = 16 * CW;
     constexpr int kCons = CW * 32;
     constexpr int kWBytes = R * 128;                        // one stage of codes
@@ -415,7 +435,6 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
     const int nst = (int)((K + 255) / 256);
     const int rb0 = (int)(row_base >> 7);
     const int rb1 = (int)((row_base + R - 1) >> 7);
-    const int64_t n_rb_total = (N + 127) / 128;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -426,27 +445,24 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait_then_release();
 
     if (warp == CW) {
         // ---------------- producer ----------------
         if (lane == 0) {
             prefetch_tmap(&tmW);
+            prefetch_tmap(&tmS2);
+            prefetch_tmap(&tmS1);
             int issued = 0;
             for (int i = 0; i < nst; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages &&
                     !mbar_wait(smem_u32(empty + s), ((i / kStages) - 1) & 1, args.err, abort_flag, kErrGemvProducer))
                     break;
-                const int64_t atoms_left = args.cpd4 - 4LL * i;
-                const uint32_t n_atoms = (uint32_t)(atoms_left < 4 ? atoms_left : 4);
-                uint32_t n_rb = 0;
-                for (int rb = rb0; rb <= rb1 && rb < n_rb_total; ++rb) ++n_rb;
-                mbar_arrive_expect_tx(smem_u32(full + s), kWBytes + n_rb * n_atoms * 512);
+                const int n_rb = rb1 - rb0 + 1;
+                mbar_arrive_expect_tx(smem_u32(full + s), kWBytes + (uint32_t)n_rb * 2048u);
                 tma_load_2d(smem_u32(sWst + s * kWBytes), &tmW, smem_u32(full + s), i * 128, (int32_t)row_base);
-                for (uint32_t j = 0; j < n_rb; ++j) {
-                    const uint8_t* src = args.sW + ((int64_t)(rb0 + j) * args.cpd4 + 4LL * i) * 512;
-                    bulk_load(smem_u32(sSst + s * kSBytes + j * 2048), src, n_atoms * 512, smem_u32(full + s));
-                }
+                load_scale_tiles(smem_u32(sSst + s * kSBytes), &tmS2, &tmS1, smem_u32(full + s), i, rb0, n_rb);
                 issued = i + 1;
             }
             if (*abort_flag) {
@@ -651,10 +667,12 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const Args args) {
 // conversions drop out of the stage loop.
 constexpr int kResMaxStages = 8;
 
-// both halves of a bf16x2 word zero or f16 normals (bf16 exponent field 113..142)
+// both halves of a bf16x2 word exactly representable in f16: zero, or bf16
+// exponent field 110..142 (f16 normals, and f16 subnormals: a bf16 value's 8
+// significant bits at 2^-17 or above are whole multiples of 2^-24)
 __device__ __forceinline__ bool f16_exact2(uint32_t w) {
     const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
-    return (lo == 0 || lo - (113u << 7) < (30u << 7)) && (hi == 0 || hi - (113u << 7) < (30u << 7));
+    return (lo == 0 || lo - (110u << 7) < (33u << 7)) && (hi == 0 || hi - (110u << 7) < (33u << 7));
 }
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_rn(uint32_t w) {
     bool unused;
@@ -675,7 +693,8 @@ __device__ __forceinline__ float ue4m3_bits_to_f32(uint32_t b) {
 
 template <int CW, bool SLOT>
 __global__ void __launch_bounds__((CW + 1) * 32, 1)
-gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, int n_stages, uint32_t x_pitch) {
+gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS2,
+                     const __grid_constant__ CUtensorMap tmS1, const Args args, int n_stages, uint32_t x_pitch) {
     constexpr int R = 16 * CW;
     constexpr int kCons = CW * 32;
     constexpr int kWBytes = R * 128;
@@ -688,14 +707,14 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, i
     uint8_t* sX = sSst + n_stages * kSBytes;                            // M rows x x_pitch bytes
     uint64_t* full = reinterpret_cast<uint64_t*>(sX + M * x_pitch);      // x_pitch % 16 == 0
     uint64_t* empty = full + kResMaxStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kResMaxStages);
+    uint64_t* xbar = empty + kResMaxStages;                              // x has landed in shared memory
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(xbar + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row_base = (int64_t)blockIdx.x * R;
     const int nst = (int)((K + 255) / 256);
     const int rb0 = (int)(row_base >> 7);
     const int rb1 = (int)((row_base + R - 1) >> 7);
-    const int64_t n_rb_total = (N + 127) / 128;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -703,30 +722,33 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, i
             mbar_init(smem_u32(full + st), 1);
             mbar_init(smem_u32(empty + st), CW);
         }
+        mbar_init(smem_u32(xbar), 1);
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait_then_release();
 
     if (warp == CW) {
         // ---------------- producer (as in gemv_nvf4_kernel) ----------------
         if (lane == 0) {
+            // x first, before the weight ring's traffic: each row one bulk copy
+            // of its K bf16 values into its shared-memory row
+            mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * K * 2));
+            for (int64_t r = 0; r < M; ++r)
+                bulk_load(smem_u32(sX + r * x_pitch), args.x + r * K, (uint32_t)(K * 2), smem_u32(xbar));
             prefetch_tmap(&tmW);
+            prefetch_tmap(&tmS2);
+            prefetch_tmap(&tmS1);
             int issued = 0;
             for (int i = 0; i < nst; ++i) {
                 const int st = i % n_stages;
                 if (i >= n_stages &&
                     !mbar_wait(smem_u32(empty + st), ((i / n_stages) - 1) & 1, args.err, abort_flag, kErrGemvProducer))
                     break;
-                const int64_t atoms_left = args.cpd4 - 4LL * i;
-                const uint32_t n_atoms = (uint32_t)(atoms_left < 4 ? atoms_left : 4);
-                uint32_t n_rb = 0;
-                for (int rb = rb0; rb <= rb1 && rb < n_rb_total; ++rb) ++n_rb;
-                mbar_arrive_expect_tx(smem_u32(full + st), kWBytes + n_rb * n_atoms * 512);
+                const int n_rb = rb1 - rb0 + 1;
+                mbar_arrive_expect_tx(smem_u32(full + st), kWBytes + (uint32_t)n_rb * 2048u);
                 tma_load_2d(smem_u32(sWst + st * kWBytes), &tmW, smem_u32(full + st), i * 128, (int32_t)row_base);
-                for (uint32_t j = 0; j < n_rb; ++j) {
-                    const uint8_t* src = args.sW + ((int64_t)(rb0 + j) * args.cpd4 + 4LL * i) * 512;
-                    bulk_load(smem_u32(sSst + st * kSBytes + j * 2048), src, n_atoms * 512, smem_u32(full + st));
-                }
+                load_scale_tiles(smem_u32(sSst + st * kSBytes), &tmS2, &tmS1, smem_u32(full + st), i, rb0, n_rb);
                 issued = i + 1;
             }
             if (*abort_flag) {
@@ -737,35 +759,44 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const Args args, i
                     }
                 }
             }
+            {   // the x copy too
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(smem_u32(xbar), 0) && globaltimer() - t0 < kWaitLimitNs) {
+                }
+            }
         }
         return;
     }
 
     // ---------------- consumers ----------------
-    // 1. x -> shared memory once: check every value (one AND over the consumer
-    //    threads), then store it as f16 or as raw bf16; x is re-read from L2.
-    //    A row holds nst * 256 values (the K tail zero, as the weight's TMA
-    //    fill there is zero) plus 64 bytes of padding.
-    const int64_t units = M * (K / 8);                                  // 16-byte units of x
-    bool ok = true;
-    for (int64_t u = threadIdx.x; u < units; u += kCons) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(args.x) + u);
-        ok = ok && f16_exact2(v.x) && f16_exact2(v.y) && f16_exact2(v.z) && f16_exact2(v.w);
-    }
-    const bool use_f16 = bar_and(1, kCons, ok);
+    // 1. x has been copied into shared memory (the producer's first transfer):
+    //    check every value (one AND over the consumer threads), then convert it
+    //    in place to f16 or leave it raw bf16.  A row holds nst * 256 values
+    //    (the K tail zero, as the weight's TMA fill there is zero) plus 64 bytes
+    //    of padding.
+    const bool x_ok = mbar_wait(smem_u32(xbar), 0, args.err, abort_flag, kErrGemvConsumer);
     const int64_t row_units = (int64_t)nst * 32;                        // 16-byte units per staged row
+    bool ok = true;
     for (int64_t u = threadIdx.x; u < M * row_units; u += kCons) {
         const int64_t r = u / row_units, c = u - r * row_units;
-        uint4 v = make_uint4(0, 0, 0, 0);
         if (c < K / 8) {
-            v = __ldg(reinterpret_cast<const uint4*>(args.x + r * K) + c);
-            if (use_f16)
-                v = make_uint4(bf16x2_to_f16x2_rn(v.x), bf16x2_to_f16x2_rn(v.y), bf16x2_to_f16x2_rn(v.z),
-                               bf16x2_to_f16x2_rn(v.w));
+            const uint4 v = *reinterpret_cast<const uint4*>(sX + r * x_pitch + 16 * c);
+            ok = ok && f16_exact2(v.x) && f16_exact2(v.y) && f16_exact2(v.z) && f16_exact2(v.w);
         }
-        *reinterpret_cast<uint4*>(sX + r * x_pitch + 16 * c) = v;
     }
-    bar_and(1, kCons, true);                                            // x staged for every warp
+    const bool use_f16 = bar_and(1, kCons, ok);
+    for (int64_t u = threadIdx.x; u < M * row_units; u += kCons) {
+        const int64_t r = u / row_units, c = u - r * row_units;
+        uint4* p = reinterpret_cast<uint4*>(sX + r * x_pitch + 16 * c);
+        if (c >= K / 8) {
+            *p = make_uint4(0, 0, 0, 0);
+        } else if (use_f16) {
+            const uint4 v = *p;
+            *p = make_uint4(bf16x2_to_f16x2_rn(v.x), bf16x2_to_f16x2_rn(v.y), bf16x2_to_f16x2_rn(v.z),
+                            bf16x2_to_f16x2_rn(v.w));
+        }
+    }
+    bar_and(1, kCons, x_ok);                                            // x staged for every warp
 
     const int g = lane >> 2, t = lane & 3;
     const int64_t row0 = row_base + warp * 16 + g, row1 = row0 + 8;
@@ -1004,7 +1035,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 2)
-gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Args args) {
+gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ CUtensorMap tmS1, const Args args) {
     using P = Plan<NP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1048,25 +1080,25 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_s;
+    pdl_wait_then_release();
 
     if (warp == 0) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
+            prefetch_tmap(&tmS1);
             int issued = 0;
             for (int i = 0; i < nst; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages &&
                     !mbar_wait(smem_u32(empty + s), ((i / kStages) - 1) & 1, args.err, abort_flag, kErrGemvProducer))
                     break;
-                const int64_t atoms_left = args.cpd4 - 4LL * i;
-                const uint32_t n_atoms = (uint32_t)(atoms_left < 4 ? atoms_left : 4);
                 uint8_t* st = smem + s * P::kStage;
                 const uint32_t fb = smem_u32(full + s);
-                mbar_arrive_expect_tx(fb, P::kW + n_atoms * 512 + P::kX);
+                mbar_arrive_expect_tx(fb, P::kW + P::kS + P::kX);
                 tma_load_2d(smem_u32(st), &tmW, fb, i * 128, (int32_t)row_base);
-                bulk_load(smem_u32(st + P::kW), args.sW + (rb * args.cpd4 + 4LL * i) * 512, n_atoms * 512, fb);
+                tma_load_3d(smem_u32(st + P::kW), &tmS1, fb, 0, 4 * i, (int32_t)rb);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     tma_load_2d(smem_u32(st + P::kW + P::kS + j * P::kXBox), &tmX, fb, i * 256 + 64 * j, 0);
@@ -1286,8 +1318,31 @@ int nvf4_warps(int64_t N, int sms) {
     return best;
 }
 
+// The weight's tensor map and its scale buffer's (2-tile and 1-tile boxes).
+struct NvfMaps {
+    CUtensorMap w, s2, s1;
+};
+
+// Programmatic dependent launch: the kernel's prologue may overlap the
+// previous kernel on the stream; the kernel waits (griddepcontrol.wait)
+// before reading anything that kernel wrote.
+template <typename KernelT, typename... Args>
+cudaError_t launch_pdl(KernelT kernel, dim3 grid, int threads, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int NT, int CW>
-bsq_status launch_nvf4_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+bsq_status launch_nvf4_cfg(const NvfMaps& mp, const nvf4::Args& a, cudaStream_t s) {
     constexpr int R = 16 * CW;
     constexpr size_t smem = nvf4::Plan<NT, CW>::kBytes;
     auto kern = nvf4::gemv_nvf4_kernel<NT, CW>;
@@ -1300,29 +1355,29 @@ bsq_status launch_nvf4_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStrea
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return BSQ_ERR_UNSUPPORTED; }
     const dim3 grid((unsigned)((a.N + R - 1) / R));
-    kern<<<grid, (CW + 1) * 32, smem, s>>>(tm, a);
+    if (launch_pdl(kern, grid, (CW + 1) * 32, smem, s, mp.w, mp.s2, mp.s1, a) != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
     return launch_status();
 }
 
 template <int NT>
-bsq_status launch_nvf4_nt(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+bsq_status launch_nvf4_nt(int cw, const NvfMaps& mp, const nvf4::Args& a, cudaStream_t s) {
     switch (cw) {
-    case 12: return launch_nvf4_cfg<NT, 12>(tm, a, s);
-    case 8: return launch_nvf4_cfg<NT, 8>(tm, a, s);
-    case 6: return launch_nvf4_cfg<NT, 6>(tm, a, s);
-    default: return launch_nvf4_cfg<NT, 4>(tm, a, s);
+    case 12: return launch_nvf4_cfg<NT, 12>(mp, a, s);
+    case 8: return launch_nvf4_cfg<NT, 8>(mp, a, s);
+    case 6: return launch_nvf4_cfg<NT, 6>(mp, a, s);
+    default: return launch_nvf4_cfg<NT, 4>(mp, a, s);
     }
 }
 
 // The resident-x kernel when x and a ring of >= 6 stages fit (M <= 2 at K = 8192);
 // returns -1 (nothing launched) when they do not.
 template <int CW, bool SLOT>
-int launch_nvf4_res_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+int launch_nvf4_res_cfg(const NvfMaps& mp, const nvf4::Args& a, cudaStream_t s) {
     constexpr int R = 16 * CW;
     constexpr int64_t kStage = R * 128 + nvf4::kMaxRowBlocks * 2048;
     // nst * 256 values per row (the K tail zero) + 64 bytes: == 64 mod 128, conflict-free B reads
     const int64_t pitch = (a.K + 255) / 256 * 512 + 64;
-    const int64_t fixed = 1024 + a.M * pitch + 2 * nvf4::kResMaxStages * 8 + 16;
+    const int64_t fixed = 1024 + a.M * pitch + (2 * nvf4::kResMaxStages + 1) * 8 + 16;
     int64_t stages = (nvf4::kSmemLimit - fixed) / kStage;
     if (stages > nvf4::kResMaxStages) stages = nvf4::kResMaxStages;
     if (stages < 6) return -1;                               // a shallower ring starves the consumers
@@ -1338,28 +1393,28 @@ int launch_nvf4_res_cfg(const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return -1; }
     const dim3 grid((unsigned)((a.N + R - 1) / R));
-    kern<<<grid, (CW + 1) * 32, smem, s>>>(tm, a, (int)stages, (uint32_t)pitch);
+    if (launch_pdl(kern, grid, (CW + 1) * 32, smem, s, mp.w, mp.s2, mp.s1, a, (int)stages, (uint32_t)pitch) != cudaSuccess) { (void)cudaGetLastError(); return (int)BSQ_ERR_CUDA; }
     return (int)launch_status();
 }
 
 template <bool SLOT>
-int launch_nvf4_res_slot(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
+int launch_nvf4_res_slot(int cw, const NvfMaps& mp, const nvf4::Args& a, cudaStream_t s) {
     switch (cw) {
-    case 12: return launch_nvf4_res_cfg<12, SLOT>(tm, a, s);
-    case 8: return launch_nvf4_res_cfg<8, SLOT>(tm, a, s);
-    case 6: return launch_nvf4_res_cfg<6, SLOT>(tm, a, s);
-    default: return launch_nvf4_res_cfg<4, SLOT>(tm, a, s);
+    case 12: return launch_nvf4_res_cfg<12, SLOT>(mp, a, s);
+    case 8: return launch_nvf4_res_cfg<8, SLOT>(mp, a, s);
+    case 6: return launch_nvf4_res_cfg<6, SLOT>(mp, a, s);
+    default: return launch_nvf4_res_cfg<4, SLOT>(mp, a, s);
     }
 }
 
-int launch_nvf4_res(int cw, const CUtensorMap& tm, const nvf4::Args& a, cudaStream_t s) {
-    return a.M == 1 ? launch_nvf4_res_slot<true>(cw, tm, a, s) : launch_nvf4_res_slot<false>(cw, tm, a, s);
+int launch_nvf4_res(int cw, const NvfMaps& mp, const nvf4::Args& a, cudaStream_t s) {
+    return a.M == 1 ? launch_nvf4_res_slot<true>(cw, mp, a, s) : launch_nvf4_res_slot<false>(cw, mp, a, s);
 }
 
 
 // The tensor-core kernel (17 <= M <= 32); -1 when it cannot be launched here.
 template <int NP>
-int launch_nvf4_tc_cfg(const DeviceInfo* info, const CUtensorMap& tmW, const uint16_t* x, const nvf4::Args& a,
+int launch_nvf4_tc_cfg(const DeviceInfo* info, const NvfMaps& mp, const uint16_t* x, const nvf4::Args& a,
                        cudaStream_t s) {
     using P = nvf4::tc::Plan<NP>;
     EncodeTiledFn enc = encode_tiled_fn();
@@ -1384,7 +1439,7 @@ int launch_nvf4_tc_cfg(const DeviceInfo* info, const CUtensorMap& tmW, const uin
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return -1; }
     (void)info;
     const dim3 grid((unsigned)((a.N + 127) / 128));
-    kern<<<grid, nvf4::tc::kThreads, P::kBytes, s>>>(tmW, tmX, a);
+    if (launch_pdl(kern, grid, nvf4::tc::kThreads, P::kBytes, s, mp.w, tmX, mp.s1, a) != cudaSuccess) { (void)cudaGetLastError(); return (int)BSQ_ERR_CUDA; }
     return (int)launch_status();
 }
 
@@ -1393,38 +1448,47 @@ bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t*
     const int cw = nvf4_warps(N, info->num_sms);
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return BSQ_ERR_UNSUPPORTED;
-    CUtensorMap tm;
     const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
     const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-    const cuuint32_t box[2] = {128, (cuuint32_t)(16 * cw)};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return BSQ_ERR_UNSUPPORTED;
+    const cuuint32_t es[3] = {1, 1, 1};
+    auto weight_map = [&](CUtensorMap* m, uint32_t rows) {
+        const cuuint32_t box[2] = {128, rows};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    // the scale buffer as 32-bit words {128 of an atom, atoms along K, 128-row tiles}
+    const int64_t cpd4 = pad_to(K / 16, 4) / 4;
+    auto scale_map = [&](CUtensorMap* m, uint32_t tiles) {
+        const cuuint64_t sd[3] = {128, (cuuint64_t)cpd4, (cuuint64_t)(pad_to(N, 128) / 128)};
+        const cuuint64_t ss[2] = {512, (cuuint64_t)(cpd4 * 512)};
+        const cuuint32_t sb[3] = {128, 4, tiles};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(sW), sd, ss, sb, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    NvfMaps mp;
+    if (!scale_map(&mp.s2, 2) || !scale_map(&mp.s1, 1)) return BSQ_ERR_UNSUPPORTED;
     nvf4::Args a;
     a.x = x; a.sW = sW; a.gW = gW; a.y = y; a.err = info->err; a.M = M; a.N = N; a.K = K;
-    a.cpd4 = pad_to(K / 16, 4) / 4;
+    a.cpd4 = cpd4;
     a.out_bf16 = out;
     if (M > 16) {
         // 17..32 activation rows: the tensor-core kernel (mma.sync issue would
         // bound the register-decode kernels); it reads the weight in 128-row tiles
-        CUtensorMap tm128;
-        const cuuint32_t box128[2] = {128, 128};
-        if (enc(&tm128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), dims, strides, box128, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
-            const int st = launch_nvf4_tc_cfg<32>(info, tm128, x, a, s);
+        if (weight_map(&mp.w, 128)) {
+            const int st = launch_nvf4_tc_cfg<32>(info, mp, x, a, s);
             if (st >= 0) return (bsq_status)st;
         }
     }
+    if (!weight_map(&mp.w, (uint32_t)(16 * cw))) return BSQ_ERR_UNSUPPORTED;
     if (M <= 8) {
-        const int st = launch_nvf4_res(cw, tm, a, s);
+        const int st = launch_nvf4_res(cw, mp, a, s);
         if (st >= 0) return (bsq_status)st;
-        return launch_nvf4_nt<1>(cw, tm, a, s);
+        return launch_nvf4_nt<1>(cw, mp, a, s);
     }
-    if (M <= 16) return launch_nvf4_nt<2>(cw, tm, a, s);
-    return launch_nvf4_nt<4>(cw, tm, a, s);
+    if (M <= 16) return launch_nvf4_nt<2>(cw, mp, a, s);
+    return launch_nvf4_nt<4>(cw, mp, a, s);
 }
 
 template <int WFMT>

@@ -73,6 +73,27 @@ def test_gemv_nvfp4_activations_outside_f16(bsq, M):
         check_products(y, want, s, f"gemv_nvfp4 mixed chunks M{M}")
 
 
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_gemv_nvfp4_activations_on_f16_subnormals(bsq, M):
+    """A whole activation row of values in [2^-17, 2^-14): bf16 values with
+    exponent field 110..112 are exact f16 subnormals, so they take the f16 path;
+    were subnormal operands flushed, that row's outputs would be lost entirely
+    (its sum_k |x_k w_k| is of the same tiny size).  Values of field 109 and below
+    elsewhere still take the exact bf16 path."""
+    N, K = 300, 1024
+    g = np.random.default_rng(70 + M)
+    x = S.normal_bf16((M, K), 1.0, 71 + M)
+    field = g.integers(110, 113, K).astype(np.uint16)
+    x[0] = (g.integers(0, 2, K).astype(np.uint16) << 15) | (field << 7) | g.integers(0, 128, K).astype(np.uint16)
+    if M > 1:
+        x[1, ::97] = 0x3480                     # 2^-22: below the f16-exact range (a bf16 stage)
+    W, sc = nvfp4_operand(N, K, 72)
+    want, s = O.gemv_nvfp4(x, W, sc, 1.0, M, N, K)
+    for out in (torch.float32, torch.bfloat16):
+        y = bsq.gemv_nvfp4(dev_tensor(x), dev_tensor(W), dev_tensor(sc), None, K, out_dtype=out)
+        check_products(y, want, s, f"gemv_nvfp4 f16-subnormal activations M{M}")
+
+
 @pytest.mark.parametrize("M", [17, 32])
 def test_gemv_nvfp4_tensor_core_many_tiles(bsq, M):
     """The tensor-core decode product with more 128-row weight tiles than SMs
