@@ -357,6 +357,89 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 }
             }
         }
+    } else if (NVF4 && PAIR && warp == 1) {
+        if (prank == 0) {
+            // ------------------------------------ MMA issue, nvfp4 CTA pairs --
+            // The single thread that feeds the tensor pipe is the limit here (a
+            // stage of four 256x256x64 MMAs is 512 cycles of tensor work; every
+            // instruction the issuing thread spends between them shows up as
+            // idle pipe), so this loop is kept lean: the whole warp runs it
+            // (warp-uniform control flow) and lane 0 issues; the ring is walked
+            // kStages slots per outer iteration, so each slot's barrier,
+            // descriptor and TMEM column offsets are immediates added to
+            // 32-bit bases.
+            const bool leader = lane == 0;
+            const uint64_t dA0 = smem_desc(smem_u32(sA_st), 16, 1024, 2);
+            const uint64_t dB0 = smem_desc(smem_u32(sB_st), 16, 1024, 2);
+            const uint32_t d_hi = (uint32_t)(dA0 >> 32);            // equal for A and B
+            uint32_t a_lo = (uint32_t)dA0, b_lo = (uint32_t)dB0, sf_base = tmem + (uint32_t)BN;
+            const uint32_t sf_full_b = smem_u32(sf_full), empty_b = smem_u32(empty);
+            const int64_t nks = ks_end - ks_begin;
+            const int64_t my_tiles = n_units > tile_first ? (n_units - tile_first + tile_step - 1) / tile_step : 0;
+            const int64_t total = my_tiles * nks;
+            // the stage cut by K (K % 256 != 0): its index within a tile and its MMA count
+            const int64_t ks_cut = (K % C::kStageK) != 0 ? nks - 1 : -1;
+            const int n_cut = (int)((K % C::kStageK) / 64);
+            int64_t ks = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int64_t g = 0; g < total && ok; g += C::kStages) {
+                // opaque to the compiler, so the per-slot operands are formed here
+                // by a few adds rather than all held in registers across the loop
+                asm volatile("" : "+r"(a_lo), "+r"(b_lo), "+r"(sf_base));
+#pragma unroll
+                for (int j = 0; j < C::kStages; ++j) {
+                    if (g + j < total && ok) {
+                        if (ks == 0) {
+                            ok = mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, args.err, abort_flag, kErrGemmMma);
+                            tc_fence_after();
+                        }
+                        // the slot's scales are in TMEM and both CTAs' tiles have landed
+                        if (ok) ok = mbar_wait(sf_full_b + 8 * j, phase, args.err, abort_flag, kErrGemmMma);
+                        if (ok) {
+                            tc_fence_after();
+                            if (leader) {
+                                const uint32_t sfc = sf_base + (uint32_t)(j * C::kSfColsPerStage);
+                                const uint32_t al = a_lo + (uint32_t)(j * (C::kABytes >> 4));
+                                const uint32_t bl = b_lo + (uint32_t)(j * (C::kBBytes >> 4));
+                                // K step kk: +32 bytes in both operands, scale atom kk
+                                auto issue = [&](int kk, uint32_t acc) {
+                                    tc_mma_mxf4nvf4_pair(tmem, ((uint64_t)d_hi << 32) | (al + 2u * kk),
+                                                         ((uint64_t)d_hi << 32) | (bl + 2u * kk), args.idesc, sfc + 4 * kk,
+                                                         sfc + C::kSfaCols + kk * C::kRowTilesB * 4, acc);
+                                };
+                                const uint32_t acc0 = ks != 0 ? 1u : 0u;
+                                if (ks != ks_cut) {
+                                    issue(0, acc0);
+                                    issue(1, 1u);
+                                    issue(2, 1u);
+                                    issue(3, 1u);
+                                } else {
+                                    for (int kk = 0; kk < n_cut; ++kk) issue(kk, kk > 0 ? 1u : acc0);
+                                }
+                                // the slot is free again in both CTAs once these MMAs complete
+                                tc_commit_pair_both(empty_b + 8 * j);
+                            }
+                            if (++ks == nks) {
+                                if (leader) tc_commit_pair_both(smem_u32(acc_full));
+                                ks = 0;
+                                acc_phase ^= 1;
+                            }
+                        }
+                    }
+                }
+                phase ^= 1;
+            }
+            if (leader) {
+                // every MMA issued has completed before TMEM is released
+                tc_commit_pair_local(smem_u32(drain));
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(smem_u32(drain), 0)) {
+                    if (globaltimer() - t0 > kWaitLimitNs) { atomicCAS(args.err, 0u, (uint32_t)kErrGemmDrain); break; }
+                }
+            }
+            __syncwarp();
+        }
     } else if (warp == 1) {
         if (lane == 0 && prank == 0) {
             // --------------------------------------------------- MMA issue --

@@ -289,7 +289,6 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
 //    and are lifted by 2^7 at the end.
 namespace nvf4 {
 
-constexpr int kPitch = 36;          // 16-byte units per staged x row (32 used; == 4 mod 8)
 constexpr int kMaxRowBlocks = 3;    // 128-row scale blocks one tile can touch (R <= 256)
 constexpr int kSmemLimit = 232448;  // opt-in shared memory per CTA
 
@@ -329,11 +328,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
-// AND of `ok` over the consumer threads (named barrier 1).
-__device__ __forceinline__ bool consumers_and(bool ok, int nthreads) {
+// AND of `ok` over the nthreads threads that meet at named barrier `id`.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool ok) {
     uint32_t r;
-    asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; barrier.red.and.pred p, 1, %2, q; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(r) : "r"((uint32_t)ok), "r"(nthreads) : "memory");
+    asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; barrier.red.and.pred p, %2, %3, q; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(r) : "r"((uint32_t)ok), "r"(id), "r"(nthreads) : "memory");
     return r != 0;
 }
 
@@ -393,41 +392,51 @@ struct Args {
     int out_bf16;
 };
 
-// Shared memory plan: ring stages (codes + scale atoms), two x buffers in
-// two copies (f16, bf16), barriers; as many stages as fit, at most 8.
+// Shared memory plan: ring stages (codes, x, scale atoms), barriers and the
+// per-stage x flags; as many stages as fit, at most 8.  A stage's x is four
+// {64 values, 8 NT rows} boxes with the 128-byte swizzle (rows >= M and
+// values past K read as zeros).
 template <int NT, int CW>
 struct Plan {
-    static constexpr int kXBuf = 8 * NT * kPitch * 16;             // bytes of one staged x copy
-    static constexpr int kStageBytes = 16 * CW * 128 + kMaxRowBlocks * 2048;
-    static constexpr int kFixed = 1024 + 4 * kXBuf + 256;
+    static constexpr int kXBox = 8 * NT * 128;                      // one {64, 8 NT} bf16 box
+    static constexpr int kWBytes = 16 * CW * 128;
+    static constexpr int kSBytes = kMaxRowBlocks * 2048;
+    static constexpr int kStageBytes = kWBytes + 4 * kXBox + kSBytes;   // codes first: 1024-aligned
+    static constexpr int kFixed = 1024 + 512;
     static constexpr int kFit = (kSmemLimit - kFixed) / kStageBytes;
     static constexpr int kStages = kFit < 8 ? kFit : 8;
     static constexpr int kBytes = kFixed + kStages * kStageBytes;
     static_assert(kStages >= 3, "too little shared memory for the ring");
+    static_assert(kWBytes % 1024 == 0 && kXBox % 1024 == 0, "128-byte-swizzled boxes start 1024-aligned");
+    static_assert((3 * kStages + 1) * 8 + kStages * 4 <= 512, "barrier area");
 };
 
+// Staged kernel (3 <= M <= 16 activation rows).  Per stage the producer warp
+// loads the codes, the scale atoms and x (four 2-D boxes of NT x 8 rows); kXW
+// dedicated x warps check the stage's x (is every value zero or exact in f16?
+// one AND over the x warps), convert it in place to f16 when it is, record
+// the choice in a per-stage flag and release the stage to the consumers with
+// an mbarrier.  The consumer warps so never stage x themselves nor wait for
+// one another: each walks the ring at its own pace.
+template <int NT>
+__host__ __device__ constexpr int x_warps() { return NT < 2 ? 2 : 4; }   // x warps of the staged kernel
+
 template <int NT, int CW>
-__global__ void __launch_bounds__((CW + 1) * 32, 1)
+__global__ void __launch_bounds__((CW + 1 + x_warps<NT>()) * 32, 1)
 gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS2,
-                 const __grid_constant__ CUtensorMap tmS1, const Args args) {
+                 const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmX, const Args args) {
+    using P = Plan<NT, CW>;
     constexpr int R = 16 * CW;
-    constexpr int kCons = CW * 32;
-    constexpr int kWBytes = R * 128;                        // one stage of codes
-    constexpr int kSBytes = kMaxRowBlocks * 2048;           // one stage of scale atoms (room)
-    constexpr int kRowsX = 8 * NT;
-    constexpr int kUnits = kRowsX * 32;                     // 16-byte x units per stage
-    constexpr int kPer = (kUnits + kCons - 1) / kCons;
-    constexpr int kXBuf = Plan<NT, CW>::kXBuf;
-    constexpr int kStages = Plan<NT, CW>::kStages;
+    constexpr int kStages = P::kStages;
+    constexpr int kXRows = 8 * NT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sWst = smem;                                   // kStages x kWBytes (1024-aligned stages)
-    uint8_t* sSst = sWst + kStages * kWBytes;               // kStages x kSBytes
-    uint8_t* sXh = sSst + kStages * kSBytes;                // 2 x kXBuf (f16)
-    uint8_t* sXb = sXh + 2 * kXBuf;                         // 2 x kXBuf (bf16)
-    uint64_t* full = reinterpret_cast<uint64_t*>(sXb + 2 * kXBuf);
+    // stage s: codes at s * kStageBytes, x boxes after them, then the scale atoms
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * P::kStageBytes);
     uint64_t* empty = full + kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    uint64_t* xready = empty + kStages;                      // [kStages]: x checked (and converted)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(xready + kStages);
+    uint32_t* xflag = reinterpret_cast<uint32_t*>(xready + kStages + 1);   // [kStages]: 1 = x is f16
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t M = args.M, N = args.N, K = args.K;
@@ -441,6 +450,7 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(full + s), 1);
             mbar_init(smem_u32(empty + s), CW);
+            mbar_init(smem_u32(xready + s), x_warps<NT>());
         }
         fence_mbar_init();
     }
@@ -453,16 +463,22 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmS2);
             prefetch_tmap(&tmS1);
+            prefetch_tmap(&tmX);
             int issued = 0;
             for (int i = 0; i < nst; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages &&
                     !mbar_wait(smem_u32(empty + s), ((i / kStages) - 1) & 1, args.err, abort_flag, kErrGemvProducer))
                     break;
+                uint8_t* st = smem + s * P::kStageBytes;
                 const int n_rb = rb1 - rb0 + 1;
-                mbar_arrive_expect_tx(smem_u32(full + s), kWBytes + (uint32_t)n_rb * 2048u);
-                tma_load_2d(smem_u32(sWst + s * kWBytes), &tmW, smem_u32(full + s), i * 128, (int32_t)row_base);
-                load_scale_tiles(smem_u32(sSst + s * kSBytes), &tmS2, &tmS1, smem_u32(full + s), i, rb0, n_rb);
+                const uint32_t fb = smem_u32(full + s);
+                mbar_arrive_expect_tx(fb, P::kWBytes + 4 * P::kXBox + (uint32_t)n_rb * 2048u);
+                tma_load_2d(smem_u32(st), &tmW, fb, i * 128, (int32_t)row_base);
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    tma_load_2d(smem_u32(st + P::kWBytes + b * P::kXBox), &tmX, fb, i * 256 + 64 * b, 0);
+                load_scale_tiles(smem_u32(st + P::kWBytes + 4 * P::kXBox), &tmS2, &tmS1, fb, i, rb0, n_rb);
                 issued = i + 1;
             }
             if (*abort_flag) {
@@ -478,42 +494,50 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         return;
     }
 
+    if (warp > CW) {
+        // ---------------- x warps ----------------
+        // A stage's x is 4 boxes x 8 NT rows x 8 slots of 16 bytes; x warp j takes
+        // slots [j kPer * 32, (j + 1) kPer * 32), kPer per lane.
+        constexpr int kXW = x_warps<NT>();
+        constexpr int kPer = 256 * NT / (32 * kXW);
+        const int j = warp - CW - 1;
+        for (int i = 0; i < nst; ++i) {
+            const int s = i % kStages;
+            uint8_t* xs = smem + s * P::kStageBytes + P::kWBytes;
+            const bool have = mbar_wait(smem_u32(full + s), (i / kStages) & 1, args.err, abort_flag, kErrGemvConsumer);
+            // slot u: byte offset 16 u within the stage's four boxes (the check and the
+            // conversion are per value, so the swizzled order is immaterial)
+            uint4 h[kPer];
+            bool ok = true;
+#pragma unroll
+            for (int q = 0; q < kPer; ++q) {
+                const int u = 32 * (j * kPer + q) + lane;
+                const uint4 v = have ? *reinterpret_cast<const uint4*>(xs + 16 * u) : make_uint4(0, 0, 0, 0);
+                bool a, b, c, d;
+                h[q] = make_uint4(bf16x2_to_f16x2(v.x, a), bf16x2_to_f16x2(v.y, b), bf16x2_to_f16x2(v.z, c),
+                                  bf16x2_to_f16x2(v.w, d));
+                ok = ok && a && b && c && d;
+            }
+            const bool f16 = bar_and(1, 32 * kXW, ok);
+            if (have && f16) {
+#pragma unroll
+                for (int q = 0; q < kPer; ++q) *reinterpret_cast<uint4*>(xs + 16 * (32 * (j * kPer + q) + lane)) = h[q];
+            }
+            // the slot is refilled by TMA (the async proxy) after the consumers release it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                if (j == 0) xflag[s] = f16 ? 1u : 0u;
+                mbar_arrive(smem_u32(xready + s));
+            }
+        }
+        return;
+    }
+
     // ---------------- consumers ----------------
     const int g = lane >> 2, t = lane & 3;
     const int64_t row0 = row_base + warp * 16 + g, row1 = row0 + 8;
     const int nblocks32 = (int)(K / 16);     // K < 2^31: the entry point bounds every dimension
-
-    auto x_load = [&](int64_t st, uint4 (&v)[kPer]) {
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const int idx = threadIdx.x + i * kCons;
-            const int r = idx >> 5, u = idx & 31;
-            const int64_t k = st * 256 + 8 * u;
-            v[i] = make_uint4(0, 0, 0, 0);
-            if (idx < kUnits && r < M && k < K) v[i] = __ldg(reinterpret_cast<const uint4*>(args.x + r * K + k));
-        }
-    };
-    auto x_store = [&](int buf, const uint4 (&v)[kPer]) -> bool {
-        bool ok = true;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const int idx = threadIdx.x + i * kCons;
-            if (idx < kUnits) {
-                const int r = idx >> 5, u = idx & 31;
-                const int off = (r * kPitch + u) * 16;
-                uint4 hv = make_uint4(0, 0, 0, 0);          // rows >= M are zero in both copies
-                if (r < M) {
-                    bool a, b, c, d;
-                    hv = make_uint4(bf16x2_to_f16x2(v[i].x, a), bf16x2_to_f16x2(v[i].y, b),
-                                    bf16x2_to_f16x2(v[i].z, c), bf16x2_to_f16x2(v[i].w, d));
-                    ok = ok && a && b && c && d;
-                }
-                *reinterpret_cast<uint4*>(sXh + buf * kXBuf + off) = hv;
-                *reinterpret_cast<uint4*>(sXb + buf * kXBuf + off) = v[i];
-            }
-        }
-        return ok;
-    };
 
     float acc_h[NT][4], acc_b[NT][4];
 #pragma unroll
@@ -526,12 +550,11 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     const int mrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);   // row within the tile
     const int mcol = lane >> 4;                                        // 0: chunk c, 1: chunk c+1
     // scale word of rows g, g+8 (chunk pair c, c+1 share one 4-byte group)
-    int srb[2], soff[2];
+    int soff[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int64_t row = r ? row1 : row0;
-        srb[r] = (int)((row >> 7) - rb0);
-        soff[r] = srb[r] * 2048 + (int)(row & 31) * 16 + (int)((row >> 5) & 3) * 4;
+        soff[r] = (int)((row >> 7) - rb0) * 2048 + (int)(row & 31) * 16 + (int)((row >> 5) & 3) * 4;
     }
     const uint32_t ssel = (t >> 1) ? 0x31u : 0x20u;   // bytes (t>>1) and 2 + (t>>1) of the group
 
@@ -568,25 +591,29 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             }
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {               // chunk 2cp + ch
-                uint32_t P[2][4];   // pairs j = 0..3 of rows g (wr[2ch]) and g+8 (wr[2ch+1])
+                uint32_t P2[2][4];   // pairs j = 0..3 of rows g (wr[2ch]) and g+8 (wr[2ch+1])
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     if constexpr (F16) {
-                        e2m1x8_to_f16x2(wr[2 * ch + r], P[r]);
+                        e2m1x8_to_f16x2(wr[2 * ch + r], P2[r]);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) P[r][j] = hmul2(P[r][j], S[r][ch]);
+                        for (int j = 0; j < 4; ++j) P2[r][j] = hmul2(P2[r][j], S[r][ch]);
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            P[r][j] = bmul2(place_byte_bf16x2((wr[2 * ch + r] >> (8 * j)) & 0xFFu), S[r][ch]);
+                            P2[r][j] = bmul2(place_byte_bf16x2((wr[2 * ch + r] >> (8 * j)) & 0xFFu), S[r][ch]);
                     }
                 }
+                // x units 4 (2cp + ch) + t of rows 8 nt + g: box (2cp + ch) >> 1, piece
+                // (4 (2cp + ch) + t) & 7, 128-byte swizzle by the row
+                const int c = 4 * (2 * cp + ch) + t;
                 uint4 xv[NT];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xv[nt] = lds128(xs + ((8 * nt + g) * kPitch + 4 * (2 * cp + ch) + t) * 16);
+                for (int nt = 0; nt < NT; ++nt)
+                    xv[nt] = lds128(xs + (uint32_t)((c >> 3) * P::kXBox + (8 * nt + g) * 128 + (((c & 7) ^ g) << 4)));
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const uint32_t a[4] = {P[0][2 * e], P[1][2 * e], P[0][2 * e + 1], P[1][2 * e + 1]};
+                    const uint32_t a[4] = {P2[0][2 * e], P2[1][2 * e], P2[0][2 * e + 1], P2[1][2 * e + 1]};
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         mma16816<F16>(acc[nt], a, e ? xv[nt].z : xv[nt].x, e ? xv[nt].w : xv[nt].y);
@@ -595,41 +622,26 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         }
     };
 
-    uint4 xa[kPer], xn[kPer];
-    x_load(0, xa);
-    bool f16_cur;
-    {
-        const bool ok = x_store(0, xa);
-        if (1 < nst) x_load(1, xa);
-        f16_cur = consumers_and(ok, kCons);
-    }
-
     for (int i = 0; i < nst; ++i) {
-        const int s = i % kStages, buf = i & 1;
-        if (i + 2 < nst) x_load(i + 2, xn);
-        // a failed wait (abort) skips the stage's math but keeps the named
-        // barriers below balanced across the consumer warps
-        const bool have = mbar_wait(smem_u32(full + s), (i / kStages) & 1, args.err, abort_flag, kErrGemvConsumer);
+        const int s = i % kStages;
+        const uint32_t par = (i / kStages) & 1;
+        const bool have = mbar_wait(smem_u32(full + s), par, args.err, abort_flag, kErrGemvConsumer) &&
+                          mbar_wait(smem_u32(xready + s), par, args.err, abort_flag, kErrGemvConsumer);
         if (have) {
-            const uint32_t wst = smem_u32(sWst + s * kWBytes);
-            const uint32_t sst = smem_u32(sSst + s * kSBytes);
+            const uint32_t wst = smem_u32(smem + s * P::kStageBytes);
+            const uint32_t xs = wst + P::kWBytes;
+            const uint32_t sst = xs + 4 * P::kXBox;
             const bool tail = 16 * (i + 1) > nblocks32;
-            const uint32_t xh = smem_u32(sXh + buf * kXBuf), xb = smem_u32(sXb + buf * kXBuf);
-            if (f16_cur) {
-                if (tail) consume(std::true_type{}, std::true_type{}, wst, sst, xh, i, acc_h);
-                else consume(std::true_type{}, std::false_type{}, wst, sst, xh, i, acc_h);
+            if (xflag[s]) {
+                if (tail) consume(std::true_type{}, std::true_type{}, wst, sst, xs, i, acc_h);
+                else consume(std::true_type{}, std::false_type{}, wst, sst, xs, i, acc_h);
             } else {
-                if (tail) consume(std::false_type{}, std::true_type{}, wst, sst, xb, i, acc_b);
-                else consume(std::false_type{}, std::false_type{}, wst, sst, xb, i, acc_b);
+                if (tail) consume(std::false_type{}, std::true_type{}, wst, sst, xs, i, acc_b);
+                else consume(std::false_type{}, std::false_type{}, wst, sst, xs, i, acc_b);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(empty + s));
-        bool ok = true;
-        if (i + 1 < nst) ok = x_store(buf ^ 1, xa);
-        f16_cur = consumers_and(ok, kCons);
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) xa[u] = xn[u];
     }
 
     // ---- epilogue: acc_h + 2^7 acc_b, times gW ----
@@ -677,12 +689,6 @@ __device__ __forceinline__ bool f16_exact2(uint32_t w) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_rn(uint32_t w) {
     bool unused;
     return bf16x2_to_f16x2(w, unused);
-}
-__device__ __forceinline__ bool bar_and(int id, int nthreads, bool ok) {
-    uint32_t r;
-    asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; barrier.red.and.pred p, %2, %3, q; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(r) : "r"((uint32_t)ok), "r"(id), "r"(nthreads) : "memory");
-    return r != 0;
 }
 
 // ue4m3 byte -> fp32, exact: its 7 bits placed as an fp32 exponent/mantissa
@@ -1342,10 +1348,23 @@ cudaError_t launch_pdl(KernelT kernel, dim3 grid, int threads, size_t smem, cuda
 }
 
 template <int NT, int CW>
-bsq_status launch_nvf4_cfg(const NvfMaps& mp, const nvf4::Args& a, cudaStream_t s) {
+bsq_status launch_nvf4_cfg(const NvfMaps& mp, const uint16_t* x, const nvf4::Args& a, cudaStream_t s) {
     constexpr int R = 16 * CW;
     constexpr size_t smem = nvf4::Plan<NT, CW>::kBytes;
     auto kern = nvf4::gemv_nvf4_kernel<NT, CW>;
+    // x [M, K] bf16 as {64 values, 8 NT rows} boxes, 128-byte swizzle; rows >= M
+    // and values past K are zero fill
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return BSQ_ERR_UNSUPPORTED;
+    CUtensorMap tmX;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K * 2)};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(8 * NT)};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(x), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return BSQ_ERR_UNSUPPORTED;
     static std::once_flag once[64];
     static bool ok_dev[64];
     int dev = 0;
@@ -1355,17 +1374,17 @@ bsq_status launch_nvf4_cfg(const NvfMaps& mp, const nvf4::Args& a, cudaStream_t 
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return BSQ_ERR_UNSUPPORTED; }
     const dim3 grid((unsigned)((a.N + R - 1) / R));
-    if (launch_pdl(kern, grid, (CW + 1) * 32, smem, s, mp.w, mp.s2, mp.s1, a) != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
+    if (launch_pdl(kern, grid, (CW + 1 + nvf4::x_warps<NT>()) * 32, smem, s, mp.w, mp.s2, mp.s1, tmX, a) != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
     return launch_status();
 }
 
 template <int NT>
-bsq_status launch_nvf4_nt(int cw, const NvfMaps& mp, const nvf4::Args& a, cudaStream_t s) {
+bsq_status launch_nvf4_nt(int cw, const NvfMaps& mp, const uint16_t* x, const nvf4::Args& a, cudaStream_t s) {
     switch (cw) {
-    case 12: return launch_nvf4_cfg<NT, 12>(mp, a, s);
-    case 8: return launch_nvf4_cfg<NT, 8>(mp, a, s);
-    case 6: return launch_nvf4_cfg<NT, 6>(mp, a, s);
-    default: return launch_nvf4_cfg<NT, 4>(mp, a, s);
+    case 12: return launch_nvf4_cfg<NT, 12>(mp, x, a, s);
+    case 8: return launch_nvf4_cfg<NT, 8>(mp, x, a, s);
+    case 6: return launch_nvf4_cfg<NT, 6>(mp, x, a, s);
+    default: return launch_nvf4_cfg<NT, 4>(mp, x, a, s);
     }
 }
 
@@ -1485,10 +1504,10 @@ bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t*
     if (M <= 8) {
         const int st = launch_nvf4_res(cw, mp, a, s);
         if (st >= 0) return (bsq_status)st;
-        return launch_nvf4_nt<1>(cw, mp, a, s);
+        return launch_nvf4_nt<1>(cw, mp, x, a, s);
     }
-    if (M <= 16) return launch_nvf4_nt<2>(cw, mp, a, s);
-    return launch_nvf4_nt<4>(cw, mp, a, s);
+    if (M <= 16) return launch_nvf4_nt<2>(cw, mp, x, a, s);
+    return launch_nvf4_nt<4>(cw, mp, x, a, s);
 }
 
 template <int WFMT>
