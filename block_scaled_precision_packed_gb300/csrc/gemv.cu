@@ -418,11 +418,10 @@ struct Plan {
 // the choice in a per-stage flag and release the stage to the consumers with
 // an mbarrier.  The consumer warps so never stage x themselves nor wait for
 // one another: each walks the ring at its own pace.
-template <int NT>
-__host__ __device__ constexpr int x_warps() { return NT < 2 ? 2 : 4; }   // x warps of the staged kernel
+constexpr int kXWarps = 4;          // x warps of the staged kernel (one was the bottleneck at M = 8)
 
 template <int NT, int CW>
-__global__ void __launch_bounds__((CW + 1 + x_warps<NT>()) * 32, 1)
+__global__ void __launch_bounds__((CW + 1 + kXWarps) * 32, 1)
 gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS2,
                  const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmX, const Args args) {
     using P = Plan<NT, CW>;
@@ -450,7 +449,7 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(full + s), 1);
             mbar_init(smem_u32(empty + s), CW);
-            mbar_init(smem_u32(xready + s), x_warps<NT>());
+            mbar_init(smem_u32(xready + s), kXWarps);
         }
         fence_mbar_init();
     }
@@ -498,7 +497,7 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         // ---------------- x warps ----------------
         // A stage's x is 4 boxes x 8 NT rows x 8 slots of 16 bytes; x warp j takes
         // slots [j kPer * 32, (j + 1) kPer * 32), kPer per lane.
-        constexpr int kXW = x_warps<NT>();
+        constexpr int kXW = kXWarps;
         constexpr int kPer = 256 * NT / (32 * kXW);
         const int j = warp - CW - 1;
         for (int i = 0; i < nst; ++i) {
@@ -1374,7 +1373,7 @@ bsq_status launch_nvf4_cfg(const NvfMaps& mp, const uint16_t* x, const nvf4::Arg
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return BSQ_ERR_UNSUPPORTED; }
     const dim3 grid((unsigned)((a.N + R - 1) / R));
-    if (launch_pdl(kern, grid, (CW + 1 + nvf4::x_warps<NT>()) * 32, smem, s, mp.w, mp.s2, mp.s1, tmX, a) != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
+    if (launch_pdl(kern, grid, (CW + 1 + nvf4::kXWarps) * 32, smem, s, mp.w, mp.s2, mp.s1, tmX, a) != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
     return launch_status();
 }
 
