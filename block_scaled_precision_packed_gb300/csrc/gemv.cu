@@ -350,18 +350,30 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// bf16x2 word of x -> f16x2, and whether both halves are zero or f16 normals
-// (bf16 exponent field 113..142; every such bf16 value is an f16 normal).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& ok) {
-    const uint32_t lo_e = (w >> 7) & 0xFFu, hi_e = (w >> 23) & 0xFFu;
-    // exact in f16: zero, an f16 normal, or an f16 subnormal a bf16 value lands
-    // on exactly (exponent field 110..112: 8 significant bits at >= 2^-17)
-    const bool lo_ok = (w & 0x7FFFu) == 0 || (lo_e >= 110 && lo_e <= 142);
-    const bool hi_ok = (w & 0x7FFF0000u) == 0 || (hi_e >= 110 && hi_e <= 142);
-    ok = lo_ok && hi_ok;
+// Bits 15 and 31 are set when the low / high bf16 half of w is exactly an f16
+// value: zero, or exponent field 110..142 (the f16 normals, and the f16
+// subnormals on which a bf16 value's 8 significant bits land exactly: values
+// of at least 2^-17).  Both halves are tested at once, a guard bit in each
+// sign position keeping borrows from crossing into the other half: for a
+// half's 15 magnitude bits m, (0x8000 + m) - 1 keeps bit 15 iff m != 0,
+// - (110 << 7) iff m >= 110 << 7, - (143 << 7) iff m >= 143 << 7.  AND the
+// results over many words and test once with f16_exact.
+__device__ __forceinline__ uint32_t f16_exact_bits(uint32_t w) {
+    const uint32_t a = w | 0x80008000u;
+    return ~(a - 0x00010001u) | ((a - 0x37003700u) & ~(a - 0x47804780u));
+}
+__device__ __forceinline__ bool f16_exact(uint32_t bits) { return (bits & 0x80008000u) == 0x80008000u; }
+__device__ __forceinline__ uint32_t f16_exact_bits4(const uint4& v) {
+    return f16_exact_bits(v.x) & f16_exact_bits(v.y) & f16_exact_bits(v.z) & f16_exact_bits(v.w);
+}
+// bf16x2 -> f16x2, round to nearest (exact whenever f16_exact holds)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
     return r;
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v) {
+    return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
 }
 
 // A stage's scale atoms of n_rb consecutive 128-row tiles from rb0: one load of
@@ -427,7 +439,6 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     using P = Plan<NT, CW>;
     constexpr int R = 16 * CW;
     constexpr int kStages = P::kStages;
-    constexpr int kXRows = 8 * NT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // stage s: codes at s * kStageBytes, x boxes after them, then the scale atoms
@@ -507,17 +518,15 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             // slot u: byte offset 16 u within the stage's four boxes (the check and the
             // conversion are per value, so the swizzled order is immaterial)
             uint4 h[kPer];
-            bool ok = true;
+            uint32_t okb = ~0u;
 #pragma unroll
             for (int q = 0; q < kPer; ++q) {
                 const int u = 32 * (j * kPer + q) + lane;
                 const uint4 v = have ? *reinterpret_cast<const uint4*>(xs + 16 * u) : make_uint4(0, 0, 0, 0);
-                bool a, b, c, d;
-                h[q] = make_uint4(bf16x2_to_f16x2(v.x, a), bf16x2_to_f16x2(v.y, b), bf16x2_to_f16x2(v.z, c),
-                                  bf16x2_to_f16x2(v.w, d));
-                ok = ok && a && b && c && d;
+                okb &= f16_exact_bits4(v);
+                h[q] = bf16x8_to_f16x8(v);
             }
-            const bool f16 = bar_and(1, 32 * kXW, ok);
+            const bool f16 = bar_and(1, 32 * kXW, f16_exact(okb));
             if (have && f16) {
 #pragma unroll
                 for (int q = 0; q < kPer; ++q) *reinterpret_cast<uint4*>(xs + 16 * (32 * (j * kPer + q) + lane)) = h[q];
@@ -678,17 +687,6 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 // conversions drop out of the stage loop.
 constexpr int kResMaxStages = 8;
 
-// both halves of a bf16x2 word exactly representable in f16: zero, or bf16
-// exponent field 110..142 (f16 normals, and f16 subnormals: a bf16 value's 8
-// significant bits at 2^-17 or above are whole multiples of 2^-24)
-__device__ __forceinline__ bool f16_exact2(uint32_t w) {
-    const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
-    return (lo == 0 || lo - (110u << 7) < (33u << 7)) && (hi == 0 || hi - (110u << 7) < (33u << 7));
-}
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_rn(uint32_t w) {
-    bool unused;
-    return bf16x2_to_f16x2(w, unused);
-}
 
 // ue4m3 byte -> fp32, exact: its 7 bits placed as an fp32 exponent/mantissa
 // (normal or subnormal) are the value times 2^-120.
@@ -781,15 +779,12 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
     //    of padding.
     const bool x_ok = mbar_wait(smem_u32(xbar), 0, args.err, abort_flag, kErrGemvConsumer);
     const int64_t row_units = (int64_t)nst * 32;                        // 16-byte units per staged row
-    bool ok = true;
+    uint32_t okb = ~0u;
     for (int64_t u = threadIdx.x; u < M * row_units; u += kCons) {
         const int64_t r = u / row_units, c = u - r * row_units;
-        if (c < K / 8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(sX + r * x_pitch + 16 * c);
-            ok = ok && f16_exact2(v.x) && f16_exact2(v.y) && f16_exact2(v.z) && f16_exact2(v.w);
-        }
+        if (c < K / 8) okb &= f16_exact_bits4(*reinterpret_cast<const uint4*>(sX + r * x_pitch + 16 * c));
     }
-    const bool use_f16 = bar_and(1, kCons, ok);
+    const bool use_f16 = bar_and(1, kCons, f16_exact(okb));
     for (int64_t u = threadIdx.x; u < M * row_units; u += kCons) {
         const int64_t r = u / row_units, c = u - r * row_units;
         uint4* p = reinterpret_cast<uint4*>(sX + r * x_pitch + 16 * c);
@@ -797,8 +792,7 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
             *p = make_uint4(0, 0, 0, 0);
         } else if (use_f16) {
             const uint4 v = *p;
-            *p = make_uint4(bf16x2_to_f16x2_rn(v.x), bf16x2_to_f16x2_rn(v.y), bf16x2_to_f16x2_rn(v.z),
-                            bf16x2_to_f16x2_rn(v.w));
+            *p = bf16x8_to_f16x8(v);
         }
     }
     bar_and(1, kCons, x_ok);                                            // x staged for every warp
@@ -1025,18 +1019,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
     asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;"
                  :: "r"(d), "r"(a_tmem), "l"(bdesc), "r"(idesc) : "memory");
 }
-// Both bf16 halves of w are exactly f16 values: zero, or a magnitude in
-// [2^-17, 2^16) (exponent field 110..142), where every bf16 value has at most
-// 8 significant bits that an f16 normal or subnormal holds.
-__device__ __forceinline__ bool f16_exact_pair(uint32_t w) {
-    const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
-    return ((lo == 0) | (lo - (110u << 7) < (33u << 7))) & ((hi == 0) | (hi - (110u << 7) < (33u << 7)));
-}
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
-    return r;
-}
 
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -1182,16 +1164,15 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 return v < half ? xb + v * 16 : xb + P::kXBox + (v - half) * 16;
             };
             uint4 xv[kXPer];
-            bool ok = true;
+            uint32_t okb = ~0u;
 #pragma unroll
             for (int u = 0; u < kXPer; ++u) {
                 const int v = ptid + 128 * u;
                 xv[u] = make_uint4(0, 0, 0, 0);
                 if (have && v < xunits) xv[u] = *reinterpret_cast<const uint4*>(xaddr(v));
-                ok &= f16_exact_pair(xv[u].x) & f16_exact_pair(xv[u].y) & f16_exact_pair(xv[u].z) &
-                      f16_exact_pair(xv[u].w);
+                okb &= f16_exact_bits4(xv[u]);
             }
-            const bool f16 = bar_and(1 + h, 128, ok);
+            const bool f16 = bar_and(1 + h, 128, f16_exact(okb));
             if (gi >= kSlots &&
                 !mbar_wait(smem_u32(a_empty + slot), ((gi / kSlots) - 1) & 1, args.err, abort_flag, kErrGemvConsumer))
                 continue;
@@ -1201,9 +1182,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 for (int u = 0; u < kXPer; ++u) {
                     const int v = ptid + 128 * u;
                     if (v < xunits)
-                        *reinterpret_cast<uint4*>(xaddr(v)) =
-                            make_uint4(bf16x2_to_f16x2(xv[u].x), bf16x2_to_f16x2(xv[u].y), bf16x2_to_f16x2(xv[u].z),
-                                       bf16x2_to_f16x2(xv[u].w));
+                        *reinterpret_cast<uint4*>(xaddr(v)) = bf16x8_to_f16x8(xv[u]);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
