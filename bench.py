@@ -831,6 +831,26 @@ def cpu_baseline(workload, gemv_m, unit):
     return out
 
 
+def config_cpu_baselines(configs):
+    """The oracle at 1 core and at every host core on each other configuration
+    (the same bounded samples as the headline's cpu_baseline)."""
+    import oracle as O
+    O.build()
+    for name, entry in configs.items():
+        subs = [(k, int(k[2:])) for k in entry] if name == "nvfp4_decode_gemv_Mx28672x8192" else [(None, 32)]
+        for key, m in subs:
+            e = entry[key] if key else entry
+            unit = e["unit"]
+            per_step = per_step_units(name, m)
+            out = {"kind": "oracle", "unit": unit}
+            for threads, leg in ((1, "one_core"), (0, "all_cores")):
+                smp = OracleSample(name, threads, m)
+                t = smp.step_seconds()
+                out[leg] = {"value": per_step / t, "cores": 1 if threads == 1 else host_cores(),
+                            "ms_per_step_extrapolated": round(t * 1e3, 3), "sample": smp.desc}
+            e["cpu_baseline"] = out
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -900,6 +920,8 @@ def main():
             "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "cpu_baseline": cpu}
     line.update(r["extras"])
     if r["configs"] is not None:
+        if not args.no_cpu_baseline:
+            config_cpu_baselines(r["configs"])
         line["configs"] = r["configs"]
     print(json.dumps(line))
     if world > 1:

@@ -94,6 +94,30 @@ def test_gemv_nvfp4_activations_on_f16_subnormals(bsq, M):
         check_products(y, want, s, f"gemv_nvfp4 f16-subnormal activations M{M}")
 
 
+# bf16 magnitudes at the edges of "exactly an f16 value": exponent fields 109
+# (not exact: an f16 subnormal cannot hold 8 significant bits there), 110 and
+# 112 (exact f16 subnormals), 113 (smallest f16 normal binade), 142 (largest
+# f16 binade) and 143 (beyond f16), each with mantissas 0, 1 and 127.
+F16_EDGE_BITS = [(e << 7) | m for e in (109, 110, 112, 113, 142, 143) for m in (0, 1, 127)]
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_gemv_nvfp4_activations_at_the_f16_edges(bsq, M):
+    """Each activation row made of one edge magnitude (random signs), so that a
+    wrong f16 decision shows in every output: a value taken as exact in f16
+    when it is not is rounded by ~2^-7 relative (or overflows), far beyond
+    the tolerance for outputs made only of such values."""
+    N, K = 96, 512
+    W, sc = nvfp4_operand(N, K, 80 + M)
+    g = np.random.default_rng(81 + M)
+    for bits in F16_EDGE_BITS:
+        sign = g.integers(0, 2, (M, K)).astype(np.uint16) << 15
+        x = (sign | np.uint16(bits)).astype(np.uint16)
+        want, s = O.gemv_nvfp4(x, W, sc, 1.0, M, N, K)
+        y = bsq.gemv_nvfp4(dev_tensor(x), dev_tensor(W), dev_tensor(sc), None, K, out_dtype=torch.float32)
+        check_products(y, want, s, f"gemv_nvfp4 M{M} activations 0x{bits:04x}")
+
+
 @pytest.mark.parametrize("M", [17, 32])
 def test_gemv_nvfp4_tensor_core_many_tiles(bsq, M):
     """The tensor-core decode product with more 128-row weight tiles than SMs
