@@ -423,14 +423,15 @@ struct Plan {
     static_assert((3 * kStages + 1) * 8 + kStages * 4 <= 512, "barrier area");
 };
 
-// Staged kernel (3 <= M <= 16 activation rows).  Per stage the producer warp
-// loads the codes, the scale atoms and x (four 2-D boxes of NT x 8 rows); kXW
-// dedicated x warps check the stage's x (is every value zero or exact in f16?
-// one AND over the x warps), convert it in place to f16 when it is, record
-// the choice in a per-stage flag and release the stage to the consumers with
-// an mbarrier.  The consumer warps so never stage x themselves nor wait for
-// one another: each walks the ring at its own pace.
-constexpr int kXWarps = 4;          // x warps of the staged kernel (one was the bottleneck at M = 8)
+// Staged kernel (M >= 3, or M <= 2 when x does not fit beside the resident
+// kernel's ring).  Per stage the producer warp loads the codes, the scale
+// atoms and x (four 2-D boxes of 8 NT rows); four dedicated x warps check the
+// stage's x (is every value zero or exact in f16?  one AND over the x warps),
+// convert it in place to f16 when it is, record the choice in a per-stage flag
+// and release the stage to the consumers with an mbarrier.  The consumer warps
+// so never stage x themselves nor wait for one another: each walks the ring at
+// its own pace.  (A single x warp per CTA fell behind the consumers.)
+constexpr int kXWarps = 4;
 
 template <int NT, int CW>
 __global__ void __launch_bounds__((CW + 1 + kXWarps) * 32, 1)
