@@ -999,6 +999,11 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 namespace tc {
 
 constexpr int kStages = 3;
+// Weight rows per CTA: 96 of the MMA's 128 lanes carry rows (lane quarter 3
+// decodes nothing; its accumulator lanes are never stored), so that two CTAs
+// per SM cover 28672 rows in 299 CTAs on 150 SMs instead of 224 128-row CTAs
+// that leave 72 SMs with twice the work of the other 80.
+constexpr int kRows = 96;
 constexpr int kDecWarps = 8;
 constexpr int kThreads = (2 + kDecWarps) * 32;
 constexpr uint32_t kTmemCols = 256;
@@ -1007,8 +1012,8 @@ constexpr uint32_t kColDh = 192, kColDb = 224;
 
 template <int NP>
 struct Plan {
-    static constexpr int kW = 128 * 128;
-    static constexpr int kS = 4 * 512;
+    static constexpr int kW = kRows * 128;
+    static constexpr int kS = 2 * 4 * 512;                // the atoms of the two 128-row tiles the rows can span
     static constexpr int kXBox = NP * 128;
     static constexpr int kX = 4 * kXBox;
     static constexpr int kStage = kW + kS + kX;          // a multiple of 1024
@@ -1024,7 +1029,7 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 2)
 gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    const __grid_constant__ CUtensorMap tmS1, const Args args) {
+                    const __grid_constant__ CUtensorMap tmS2, const Args args) {
     using P = Plan<NP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1040,11 +1045,11 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t M = args.M, N = args.N, K = args.K;
-    const int64_t row_base = (int64_t)blockIdx.x * 128;
+    const int64_t row_base = (int64_t)blockIdx.x * kRows;
     const int nst = (int)((K + 255) / 256);
     const int ngr = 2 * nst;
     const int nblocks = (int)(K / 16);
-    const int64_t rb = row_base >> 7;
+    const int64_t rb = row_base >> 7;                 // first 128-row scale tile the rows touch
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -1075,7 +1080,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         if (lane == 0) {
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
-            prefetch_tmap(&tmS1);
+            prefetch_tmap(&tmS2);
             int issued = 0;
             for (int i = 0; i < nst; ++i) {
                 const int s = i % kStages;
@@ -1086,7 +1091,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 const uint32_t fb = smem_u32(full + s);
                 mbar_arrive_expect_tx(fb, P::kW + P::kS + P::kX);
                 tma_load_2d(smem_u32(st), &tmW, fb, i * 128, (int32_t)row_base);
-                tma_load_3d(smem_u32(st + P::kW), &tmS1, fb, 0, 4 * i, (int32_t)rb);
+                tma_load_3d(smem_u32(st + P::kW), &tmS2, fb, 0, 4 * i, (int32_t)rb);   // tiles rb, rb + 1 (zeros past N)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     tma_load_2d(smem_u32(st + P::kW + P::kS + j * P::kXBox), &tmX, fb, i * 256 + 64 * j, 0);
@@ -1150,7 +1155,9 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             tc_st_cols(lane_base + kColDb, z);
             tc_wait_st();
         }
-        const uint32_t soff = (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4);
+        const int64_t nrow = row_base + r;                 // this thread's weight row (when r < kRows)
+        const bool row_live = r < kRows;
+        const uint32_t soff = (uint32_t)(((nrow >> 7) - rb) * 2048 + (nrow & 31) * 16 + ((nrow >> 5) & 3) * 4);
         const int xunits = (int)(16 * M);            // 16-byte x units of rows < M in the pair's two boxes
         constexpr int kXPer = NP / 8;                  // at most this many per pair thread
         for (int gi = h; gi < ngr; gi += 2) {
@@ -1192,7 +1199,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             const uint8_t* srow = st + P::kW + soff;
             const bool tail = 16 * (i + 1) > nblocks;        // uniform: only the last stage
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < 4 && row_live; ++cc) {
                 const int c = 4 * h + cc;
                 const uint4 w = lds128(wrow + ((c ^ (r & 7)) << 4));
                 uint32_t two = *reinterpret_cast<const uint16_t*>(srow + (c >> 1) * 512 + ((2 * c) & 3));
@@ -1243,7 +1250,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         if (mbar_wait(smem_u32(acc_full), 0, args.err, abort_flag, kErrGemvConsumer) && !*abort_flag) {
             tc_fence_after();
             const float gw = args.gW ? __ldg(args.gW) : 1.0f;
-            const int64_t n = row_base + r;
+            const int64_t n = row_live ? row_base + r : N;     // lanes past the CTA's rows store nothing
             // pair h stores activation rows [h NP/2, (h+1) NP/2)
             constexpr int kHalf = NP / 2;
             float v[kHalf];
@@ -1436,8 +1443,8 @@ int launch_nvf4_tc_cfg(const DeviceInfo* info, const NvfMaps& mp, const uint16_t
     });
     if (!ok_dev[dev]) { (void)cudaGetLastError(); return -1; }
     (void)info;
-    const dim3 grid((unsigned)((a.N + 127) / 128));
-    if (launch_pdl(kern, grid, nvf4::tc::kThreads, P::kBytes, s, mp.w, tmX, mp.s1, a) != cudaSuccess) { (void)cudaGetLastError(); return (int)BSQ_ERR_CUDA; }
+    const dim3 grid((unsigned)((a.N + nvf4::tc::kRows - 1) / nvf4::tc::kRows));
+    if (launch_pdl(kern, grid, nvf4::tc::kThreads, P::kBytes, s, mp.w, tmX, mp.s2, a) != cudaSuccess) { (void)cudaGetLastError(); return (int)BSQ_ERR_CUDA; }
     return (int)launch_status();
 }
 
@@ -1474,7 +1481,7 @@ bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t*
     if (M > 16) {
         // 17..32 activation rows: the tensor-core kernel (mma.sync issue would
         // bound the register-decode kernels); it reads the weight in 128-row tiles
-        if (weight_map(&mp.w, 128)) {
+        if (weight_map(&mp.w, (uint32_t)nvf4::tc::kRows)) {
             const int st = launch_nvf4_tc_cfg<32>(info, mp, x, a, s);
             if (st >= 0) return (bsq_status)st;
         }
