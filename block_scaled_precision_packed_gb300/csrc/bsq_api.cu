@@ -305,7 +305,7 @@ bsq_status bsq_get_device_error(cudaStream_t stream, uint32_t* code_out) {
     }
     *code_out = v;
     if (v == 0) return BSQ_OK;
-    return (v & 0xF00u) ? BSQ_ERR_TIMEOUT : BSQ_ERR_DEVICE_CHECK;
+    return (v & kCheckFlag) ? BSQ_ERR_DEVICE_CHECK : BSQ_ERR_TIMEOUT;
 }
 
 uint64_t bsq_launch_count(int kernel_id) {

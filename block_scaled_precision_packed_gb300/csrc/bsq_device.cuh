@@ -46,6 +46,50 @@ enum ErrorSite : uint32_t {
     kErrQuantBarrier = 0x302,
 };
 
+// ------------------------------------------------------ device bounds checks --
+// A build with -DBSQ_DEVICE_CHECKS checks every global store of these kernels,
+// and every global load addressed from a row and a column (TMA tensor-map
+// loads are bounded by their maps, the amax passes' linear loads by the element
+// count of their loop), against the extent of its buffer as the call's sizes
+// give it.  An access that leaves the buffer is skipped; the first one is
+// recorded in the error word as kCheckFlag | site << 24 | (its offset & 0xFFFFFF),
+// the offset in the buffer's own units.  Timeout sites never have bit 31 set.
+// Without the flag BSQ_IN_BUFFER is the constant true and nothing is compiled.
+constexpr uint32_t kCheckFlag = 0x80000000u;
+enum CheckSite : uint32_t {
+    kChkQuantX = 0x01,        // quantizer: load of x
+    kChkQuantCodes = 0x02,    // quantizer: store of codes
+    kChkQuantScales = 0x03,   // quantizer: store of block scales
+    kChkQuantAct = 0x04,      // fused activation quantizer: store of the activation
+    kChkGemmY = 0x11,         // GEMM: store of Y
+    kChkGemvX = 0x21,         // GEMV: load of x
+    kChkGemvW = 0x22,         // GEMV: load of weight codes
+    kChkGemvScales = 0x23,    // GEMV: load of weight block scales
+    kChkGemvY = 0x24,         // GEMV: store of y
+    kChkDequantIn = 0x31,     // dequantizer: load of codes or scales
+    kChkDequantOut = 0x32,    // dequantizer: store of the output
+};
+
+#ifdef BSQ_DEVICE_CHECKS
+// A test build may tighten one site's extent by one unit (BSQ_TEST_CHECK_TIGHT_SITE):
+// the last in-bounds access of that site is then recorded and skipped.
+#ifdef BSQ_TEST_CHECK_TIGHT_SITE
+constexpr uint32_t kTightSite = BSQ_TEST_CHECK_TIGHT_SITE;
+#else
+constexpr uint32_t kTightSite = 0;
+#endif
+// [off, off + n) inside [0, size)?  Records the first failure (see above).
+__device__ __forceinline__ bool in_buffer(uint32_t* err, uint32_t site, int64_t off, int64_t n, int64_t size) {
+    if (site == kTightSite) size -= 1;
+    if (off >= 0 && n >= 0 && off + n <= size) return true;
+    atomicCAS(err, 0u, kCheckFlag | (site << 24) | ((uint32_t)off & 0xFFFFFFu));
+    return false;
+}
+#define BSQ_IN_BUFFER(err, site, off, n, size) ::bsq::in_buffer((err), (site), (off), (n), (size))
+#else
+#define BSQ_IN_BUFFER(err, site, off, n, size) true
+#endif
+
 // Wall-clock bound of every spin-wait in these kernels (ns).  A test build
 // may set a shorter one (BSQ_WAIT_LIMIT_NS) to make a wait run out quickly.
 #ifndef BSQ_WAIT_LIMIT_NS

@@ -34,12 +34,20 @@ __device__ __forceinline__ float dec_ue8m0(uint32_t c) {
 
 template <int FMT>
 __global__ void dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                               const float* __restrict__ g, float* __restrict__ out, int64_t R, int64_t K) {
+                               const float* __restrict__ g, float* __restrict__ out, int64_t R, int64_t K,
+                               uint32_t* __restrict__ err) {
     const float gg = g ? __ldg(g) : 1.0f;
     const int64_t blk = FMT == kNvfp4 ? 16 : 32;
     const int64_t cpd4 = pad_to(K / blk, 4) / 4;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < R * K; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / K, k = i % K;
+        [[maybe_unused]] constexpr int64_t kRowNum = FMT == kNvfp4 ? 2 : FMT == kE4M3 ? 4 : 3;   // code bytes per 4 values
+        [[maybe_unused]] const int64_t cbyte = FMT == kNvfp4 ? 4 * (r * (K / 8) + k / 8) : FMT == kE4M3 ? r * K + k
+                                                                          : r * (3 * K / 4) + 3 * (k / 4);
+        if (!BSQ_IN_BUFFER(err, kChkDequantIn, swz_offset(r, k / blk, cpd4), 1, pad_to(R, 128) * 4 * cpd4) ||
+            !BSQ_IN_BUFFER(err, kChkDequantIn, cbyte, FMT == kNvfp4 ? 4 : FMT == kE4M3 ? 1 : 3, R * (kRowNum * K / 4)) ||
+            !BSQ_IN_BUFFER(err, kChkDequantOut, i, 1, R * K))
+            continue;
         const uint32_t sc = scales[swz_offset(r, k / blk, cpd4)];
         float v, s;
         if constexpr (FMT == kNvfp4) {
@@ -72,10 +80,10 @@ bsq_status dequant_launch(const void* codes, int fmt, const uint8_t* scales, con
     const int64_t cap = (int64_t)info->num_sms * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (nvfp4) dequant_kernel<kNvfp4><<<(unsigned)blocks, 256, 0, s>>>(c, scales, g, out, R, K);
-    else if (fmt == kE3M2) dequant_kernel<kE3M2><<<(unsigned)blocks, 256, 0, s>>>(c, scales, g, out, R, K);
-    else if (fmt == kE2M3) dequant_kernel<kE2M3><<<(unsigned)blocks, 256, 0, s>>>(c, scales, g, out, R, K);
-    else dequant_kernel<kE4M3><<<(unsigned)blocks, 256, 0, s>>>(c, scales, g, out, R, K);
+    if (nvfp4) dequant_kernel<kNvfp4><<<(unsigned)blocks, 256, 0, s>>>(c, scales, g, out, R, K, info->err);
+    else if (fmt == kE3M2) dequant_kernel<kE3M2><<<(unsigned)blocks, 256, 0, s>>>(c, scales, g, out, R, K, info->err);
+    else if (fmt == kE2M3) dequant_kernel<kE2M3><<<(unsigned)blocks, 256, 0, s>>>(c, scales, g, out, R, K, info->err);
+    else dequant_kernel<kE4M3><<<(unsigned)blocks, 256, 0, s>>>(c, scales, g, out, R, K, info->err);
     count_launch(BSQ_KERNEL_DEQUANT);
     return launch_status();
 }

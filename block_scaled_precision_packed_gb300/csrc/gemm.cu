@@ -748,7 +748,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         const int64_t col = nb * BN + kHalf * half + 64 * h + 16 * gi;
 #pragma unroll
                         for (int j = 0; j < 4; ++j)                           // row lrow0 + j, columns col .. col+15
-                            if (lrow0 + j < rows_valid && col + 16 <= N)
+                            if (lrow0 + j < rows_valid && col + 16 <= N &&
+                                BSQ_IN_BUFFER(args.err, kChkGemmY, (grp * M + lrow0 + j) * N + col, 16, args.G * M * N))
                                 st_global_v8(ybase + j * N + 64 * h + 16 * gi, x[8 * j], x[8 * j + 1], x[8 * j + 2],
                                              x[8 * j + 3], x[8 * j + 4], x[8 * j + 5], x[8 * j + 6], x[8 * j + 7]);
                     }
@@ -757,6 +758,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
                     for (int c = 0; c < kHalf / 32; ++c) {
                         const int64_t col0 = nb * BN + kHalf * half + 32 * c;
+                        if (col0 < N && !BSQ_IN_BUFFER(args.err, kChkGemmY, row * N + col0, N - col0 < 32 ? N - col0 : 32,
+                                                       args.G * M * N))
+                            continue;
                         if (vec && col0 + 32 <= N) {
 #pragma unroll
                             for (int v = 0; v < 4; ++v)
@@ -782,7 +786,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kHalf * half + 32 * c), r);
                 tc_wait_ld();
                 const int64_t col0 = nb * BN + kHalf * half + 32 * c;
-                if (row_ok && col0 < N) {
+                if (row_ok && col0 < N &&
+                    BSQ_IN_BUFFER(args.err, kChkGemmY, row * N + col0, N - col0 < 32 ? N - col0 : 32, args.G * M * N)) {
                     // fp32 output (the bf16 case returned above)
                     float* yr = static_cast<float*>(args.Y) + row * N + col0;
                     float o[32];
@@ -850,6 +855,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
             const int64_t row = mb * kBM + lr, col = nb * BN + 4 * cg;
             if (row >= M || col >= N) continue;
+            if (!BSQ_IN_BUFFER(args.err, kChkGemmY, row * N + col, N - col < 4 ? N - col : 4, args.G * M * N)) continue;
             const float o[4] = {__fmul_rn(acc.x, f), __fmul_rn(acc.y, f), __fmul_rn(acc.z, f), __fmul_rn(acc.w, f)};
             if (args.out_bf16) {
                 uint16_t* y = static_cast<uint16_t*>(args.Y) + row * N + col;

@@ -39,6 +39,13 @@ constexpr int kRowsPerCta = 128;         // 16 rows per warp
 constexpr int kChunk = 256;              // K elements staged per step (2 sub-chunks of 128)
 constexpr int kPitch = kChunk / 8 + 4;   // 16-byte units per staged x row (== 4 mod 8)
 
+// y[i] (i = m N + n, `size` = M N) in the output type: bf16 bits or f32.
+__device__ __forceinline__ void store_y(void* y, int out_bf16, int64_t i, float v, uint32_t* err, int64_t size) {
+    if (!BSQ_IN_BUFFER(err, kChkGemvY, i, 1, size)) return;
+    if (out_bf16) reinterpret_cast<uint16_t*>(y)[i] = f32_to_bf16_bits(v);
+    else reinterpret_cast<float*>(y)[i] = v;
+}
+
 // Raw packed bytes of one thread's share of one row's 128-element sub-chunk:
 // codes 8t..8t+7 of each of the sub-chunk's four MX blocks (thread t of the
 // quad), plus the four blocks' UE8M0 bytes.
@@ -50,7 +57,12 @@ struct RowRaw {
 
 template <int WFMT>
 __device__ __forceinline__ void load_row(RowRaw<WFMT>& rr, const uint8_t* __restrict__ W, const uint8_t* __restrict__ sW,
-                                         int64_t row, int64_t k, int t, bool valid, int64_t K, int64_t cpd4) {
+                                         int64_t row, int64_t k, int t, bool valid, int64_t N, int64_t K, int64_t cpd4,
+                                         uint32_t* err) {
+    [[maybe_unused]] constexpr int64_t kRowNum = WFMT == kE4M3 ? 4 : 3;   // row bytes = kRowNum K / 4
+    valid = valid && BSQ_IN_BUFFER(err, kChkGemvW, row * (kRowNum * K / 4) + (kRowNum * k) / 4,
+                                   kRowNum * 32, N * (kRowNum * K / 4)) &&
+            BSQ_IN_BUFFER(err, kChkGemvScales, swz_offset(row, k / 32, cpd4), 4, pad_to(N, 128) * 4 * cpd4);
     if (!valid) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) rr.w[i] = 0;
@@ -157,7 +169,8 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 template <int NT, int WFMT>
 __global__ void __launch_bounds__(kThreads)
 gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const uint8_t* __restrict__ sW,
-            const float* __restrict__ gW, void* __restrict__ y, int out_bf16, int64_t M, int64_t N, int64_t K) {
+            const float* __restrict__ gW, void* __restrict__ y, int out_bf16, int64_t M, int64_t N, int64_t K,
+            uint32_t* __restrict__ err) {
     constexpr int kRowsX = 8 * NT;
     __shared__ __align__(16) uint4 xs[2][kRowsX * kPitch];
 
@@ -175,7 +188,8 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
             const int r = idx >> 5, u = idx & 31;
             const int64_t k = ck * kChunk + u * 8;
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < M && k < K) v = __ldg(reinterpret_cast<const uint4*>(x + r * K + k));
+            if (r < M && k < K && BSQ_IN_BUFFER(err, kChkGemvX, r * K + k, 8, M * K))
+                v = __ldg(reinterpret_cast<const uint4*>(x + r * K + k));
             xr[i] = v;
         }
     };
@@ -191,8 +205,8 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
         for (int h = 0; h < 2; ++h) {
             const int64_t k = ck * kChunk + 128 * h;
             const bool kv = ck < nck && k < K;
-            load_row<WFMT>(rr[h][0], W, sW, row0, k, t, kv && row0 < N, K, cpd4);
-            load_row<WFMT>(rr[h][1], W, sW, row1, k, t, kv && row1 < N, K, cpd4);
+            load_row<WFMT>(rr[h][0], W, sW, row0, k, t, kv && row0 < N, N, K, cpd4, err);
+            load_row<WFMT>(rr[h][1], W, sW, row1, k, t, kv && row1 < N, N, K, cpd4, err);
         }
     };
 
@@ -251,11 +265,7 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ W, const
         for (int i = 0; i < 4; ++i) {
             const int64_t m = 8 * nt + 2 * t + (i & 1);
             const int64_t n = (i < 2) ? row0 : row1;
-            if (m < M && n < N) {
-                const float v = __fmul_rn(acc[nt][i], f);
-                if (out_bf16) reinterpret_cast<uint16_t*>(y)[m * N + n] = f32_to_bf16_bits(v);
-                else reinterpret_cast<float*>(y)[m * N + n] = v;
-            }
+            if (m < M && n < N) store_y(y, out_bf16, m * N + n, __fmul_rn(acc[nt][i], f), err, M * N);
         }
     }
 }
@@ -662,11 +672,9 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         for (int i = 0; i < 4; ++i) {
             const int64_t m = 8 * nt + 2 * t + (i & 1);
             const int64_t n = (i < 2) ? row0 : row1;
-            if (m < M && n < N) {
-                const float v = __fmul_rn(__fmaf_rn(acc_b[nt][i], 0x1p7f, acc_h[nt][i]), gw);
-                if (args.out_bf16) reinterpret_cast<uint16_t*>(args.y)[m * N + n] = f32_to_bf16_bits(v);
-                else reinterpret_cast<float*>(args.y)[m * N + n] = v;
-            }
+            if (m < M && n < N)
+                store_y(args.y, args.out_bf16, m * N + n, __fmul_rn(__fmaf_rn(acc_b[nt][i], 0x1p7f, acc_h[nt][i]), gw),
+                        args.err, M * N);
         }
     }
 }
@@ -736,10 +744,12 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
         // ---------------- producer (as in gemv_nvf4_kernel) ----------------
         if (lane == 0) {
             // x first, before the weight ring's traffic: each row one bulk copy
-            // of its K bf16 values into its shared-memory row
+            // of its K bf16 values into its shared-memory row (a row a device
+            // check skips leaves the barrier short: its bounded wait ends it)
             mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)(M * K * 2));
             for (int64_t r = 0; r < M; ++r)
-                bulk_load(smem_u32(sX + r * x_pitch), args.x + r * K, (uint32_t)(K * 2), smem_u32(xbar));
+                if (BSQ_IN_BUFFER(args.err, kChkGemvX, r * K, K, M * K))
+                    bulk_load(smem_u32(sX + r * x_pitch), args.x + r * K, (uint32_t)(K * 2), smem_u32(xbar));
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmS2);
             prefetch_tmap(&tmS1);
@@ -947,11 +957,7 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int64_t n = r ? row1 : row0;
-                if (n < N) {
-                    const float v = __fmul_rn(r ? v1 : v0, gw);
-                    if (args.out_bf16) reinterpret_cast<uint16_t*>(args.y)[n] = f32_to_bf16_bits(v);
-                    else reinterpret_cast<float*>(args.y)[n] = v;
-                }
+                if (n < N) store_y(args.y, args.out_bf16, n, __fmul_rn(r ? v1 : v0, gw), args.err, M * N);
             }
         }
         return;
@@ -960,11 +966,7 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
     for (int i = 0; i < 4; ++i) {
         const int64_t m = 2 * t + (i & 1);
         const int64_t n = (i < 2) ? row0 : row1;
-        if (m < M && n < N) {
-            const float v = __fmul_rn(acc[i], gw);
-            if (args.out_bf16) reinterpret_cast<uint16_t*>(args.y)[m * N + n] = f32_to_bf16_bits(v);
-            else reinterpret_cast<float*>(args.y)[m * N + n] = v;
-        }
+        if (m < M && n < N) store_y(args.y, args.out_bf16, m * N + n, __fmul_rn(acc[i], gw), args.err, M * N);
     }
 }
 
@@ -1277,11 +1279,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
 #pragma unroll
                 for (int j = 0; j < kHalf; ++j) {
                     const int64_t m = kHalf * h + j;
-                    if (m < M) {
-                        const float o = __fmul_rn(v[j], gw);
-                        if (args.out_bf16) reinterpret_cast<uint16_t*>(args.y)[m * N + n] = f32_to_bf16_bits(o);
-                        else reinterpret_cast<float*>(args.y)[m * N + n] = o;
-                    }
+                    if (m < M) store_y(args.y, args.out_bf16, m * N + n, __fmul_rn(v[j], gw), args.err, M * N);
                 }
             }
         }
@@ -1498,11 +1496,11 @@ bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t*
 
 template <int WFMT>
 bsq_status launch_fmt(const uint16_t* x, const uint8_t* W, const uint8_t* sW, const float* gW, void* y, int out,
-                      int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+                      int64_t M, int64_t N, int64_t K, uint32_t* err, cudaStream_t s) {
     const dim3 grid((unsigned)((N + kRowsPerCta - 1) / kRowsPerCta));
-    if (M <= 8) gemv_kernel<1, WFMT><<<grid, kThreads, 0, s>>>(x, W, sW, gW, y, out, M, N, K);
-    else if (M <= 16) gemv_kernel<2, WFMT><<<grid, kThreads, 0, s>>>(x, W, sW, gW, y, out, M, N, K);
-    else gemv_kernel<4, WFMT><<<grid, kThreads, 0, s>>>(x, W, sW, gW, y, out, M, N, K);
+    if (M <= 8) gemv_kernel<1, WFMT><<<grid, kThreads, 0, s>>>(x, W, sW, gW, y, out, M, N, K, err);
+    else if (M <= 16) gemv_kernel<2, WFMT><<<grid, kThreads, 0, s>>>(x, W, sW, gW, y, out, M, N, K, err);
+    else gemv_kernel<4, WFMT><<<grid, kThreads, 0, s>>>(x, W, sW, gW, y, out, M, N, K, err);
     return launch_status();
 }
 
@@ -1519,9 +1517,9 @@ bsq_status gemv_launch(const uint16_t* x, const void* W, int fw, const uint8_t* 
         r = launch_nvf4(info, x, Wb, sW, gW, y, out, M, N, K, s);
         count_launch(BSQ_KERNEL_GEMV_NVFP4);
     } else {
-        if (fw == kE3M2) r = launch_fmt<kE3M2>(x, Wb, sW, gW, y, out, M, N, K, s);
-        else if (fw == kE2M3) r = launch_fmt<kE2M3>(x, Wb, sW, gW, y, out, M, N, K, s);
-        else r = launch_fmt<kE4M3>(x, Wb, sW, gW, y, out, M, N, K, s);
+        if (fw == kE3M2) r = launch_fmt<kE3M2>(x, Wb, sW, gW, y, out, M, N, K, info->err, s);
+        else if (fw == kE2M3) r = launch_fmt<kE2M3>(x, Wb, sW, gW, y, out, M, N, K, info->err, s);
+        else r = launch_fmt<kE4M3>(x, Wb, sW, gW, y, out, M, N, K, info->err, s);
         count_launch(BSQ_KERNEL_GEMV_MX);
     }
     return r;

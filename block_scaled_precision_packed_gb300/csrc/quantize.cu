@@ -191,7 +191,7 @@ template <int FMT, bool FUSED, bool CONT = false>
 __global__ void __launch_bounds__(kEncThreads)
 quant_mx_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint32_t* __restrict__ partial,
                 int n_partial, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                float* __restrict__ s_global) {
+                float* __restrict__ s_global, uint32_t* __restrict__ err) {
     __shared__ uint32_t red[32];
     __shared__ uint32_t xchg;
     const uint32_t am_bits = tensor_amax_bits<FUSED>(x, M * K, partial, n_partial, red, &xchg);
@@ -211,7 +211,7 @@ quant_mx_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint
         const uint32_t r = gb / nbp, b = gb - r * nbp;
         const bool valid = r < M && b < nb;
         uint4 v[4];
-        if (valid) {
+        if (valid && BSQ_IN_BUFFER(err, kChkQuantX, (int64_t)r * K + 32 * (int64_t)b, 32, M * K)) {
             const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * K + 32 * (int64_t)b);
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
@@ -224,13 +224,15 @@ quant_mx_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint
         mx_block_scale<FMT>(absmax32_bits(v), gs, ue, inv);
         uint32_t w[8];
         mx_encode_words<FMT, CONT>(v, inv, w);
-        if (valid)
-            mx_store_words<FMT, CONT>(codes + (int64_t)r * row_bytes + (FMT == kE4M3 || CONT ? 32 : 24) * (int64_t)b, w);
+        constexpr int kBlockBytes = FMT == kE4M3 || CONT ? 32 : 24;
+        if (valid && BSQ_IN_BUFFER(err, kChkQuantCodes, (int64_t)r * row_bytes + kBlockBytes * (int64_t)b, kBlockBytes,
+                                   M * row_bytes))
+            mx_store_words<FMT, CONT>(codes + (int64_t)r * row_bytes + kBlockBytes * (int64_t)b, w);
         // four consecutive blocks' scale bytes (four consecutive lanes, the same
         // row: nbp % 4 == 0) -> one 32-bit store
         const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
                             (__shfl_down_sync(0xFFFFFFFFu, ue, 2) << 16) | (__shfl_down_sync(0xFFFFFFFFu, ue, 3) << 24);
-        if ((lane & 3) == 0)
+        if ((lane & 3) == 0 && BSQ_IN_BUFFER(err, kChkQuantScales, swz_offset(r, b, cpd4), 4, (int64_t)total))
             *reinterpret_cast<uint32_t*>(scales + swz_offset(r, b, cpd4)) = s4;
     }
 }
@@ -242,7 +244,7 @@ template <bool FUSED>
 __global__ void __launch_bounds__(kEncThreads)
 quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint32_t* __restrict__ partial,
                    int n_partial, uint32_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                   float* __restrict__ s_global) {
+                   float* __restrict__ s_global, uint32_t* __restrict__ err) {
     __shared__ uint32_t red[32];
     __shared__ uint32_t xchg;
     const uint32_t am_bits = tensor_amax_bits<FUSED>(x, M * K, partial, n_partial, red, &xchg);
@@ -267,7 +269,7 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const u
             const uint32_t b = b0 + h;
             const bool valid = r < M && b < nb;
             uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-            if (valid) {
+            if (valid && BSQ_IN_BUFFER(err, kChkQuantX, (int64_t)r * K + 16 * (int64_t)b, 16, M * K)) {
                 const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * K + 16 * (int64_t)b);
                 v0 = __ldg(src);
                 v1 = __ldg(src + 1);
@@ -277,15 +279,16 @@ quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const u
             word[2 * h] = w0;
             word[2 * h + 1] = w1;
         }
-        if (r < M && b0 < nb) {
-            uint32_t* dst = codes + (int64_t)r * (K / 8) + 2 * (int64_t)b0;   // 8-byte aligned rows (K % 16 == 0)
+        const int64_t woff = (int64_t)r * (K / 8) + 2 * (int64_t)b0;       // in 32-bit words
+        if (r < M && b0 < nb && BSQ_IN_BUFFER(err, kChkQuantCodes, woff, b0 + 1 < nb ? 4 : 2, M * (K / 8))) {
+            uint32_t* dst = codes + woff;                                     // 8-byte aligned rows (K % 16 == 0)
             *reinterpret_cast<uint2*>(dst) = make_uint2(word[0], word[1]);
             if (b0 + 1 < nb) *reinterpret_cast<uint2*>(dst + 2) = make_uint2(word[2], word[3]);
         }
         // blocks b0, b0+1 from this lane and b0+2, b0+3 from the next -> one 32-bit store
         const uint32_t s2 = sb[0] | (sb[1] << 8);
         const uint32_t s4 = s2 | (__shfl_down_sync(0xFFFFFFFFu, s2, 1) << 16);
-        if ((lane & 1) == 0)
+        if ((lane & 1) == 0 && BSQ_IN_BUFFER(err, kChkQuantScales, swz_offset(r, b0, cpd4), 4, 2 * (int64_t)total))
             *reinterpret_cast<uint32_t*>(scales + swz_offset(r, b0, cpd4)) = s4;
     }
 }
@@ -442,8 +445,12 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
         const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x) + f0 * 64;
         for (uint32_t k = 0; k < n_chunks; ++k) {
             const uint32_t off = k * kChunkBytes, n = min(kChunkBytes, bytes - off);
-            mbar_arrive_expect_tx(smem_u32(bar + k), n);
-            bulk_load(slice_addr + off, src + off, n, smem_u32(bar + k));
+            if (BSQ_IN_BUFFER(args.err, kChkQuantX, f0 * 64 + off, n, a.M * a.K * 2)) {
+                mbar_arrive_expect_tx(smem_u32(bar + k), n);
+                bulk_load(slice_addr + off, src + off, n, smem_u32(bar + k));
+            } else {
+                mbar_arrive(smem_u32(bar + k));   // skipped: the chunk completes with no bytes
+            }
         }
         // control block: initialize it (CTA 0) or wait for it if it is not valid
         uint32_t* ctl = args.ws + kCtlWord;
@@ -596,23 +603,31 @@ __global__ void __launch_bounds__(kOneThreads, 1) quant_onepass_kernel(const __g
             for (int j = 0; j < 4; ++j) v[j] = make_uint4(0, 0, 0, 0);
         }
         uint8_t* const row_codes = static_cast<uint8_t*>(a.codes) + (int64_t)r * row_bytes;
+        constexpr int kUnitBytes = FMT == kNvfp4 ? 16 : FMT == kE4M3 ? 32 : 24;   // code bytes of one slot
+        const bool store = valid && BSQ_IN_BUFFER(args.err, kChkQuantCodes, (int64_t)r * row_bytes + kUnitBytes * b,
+                                                  kUnitBytes, a.M * row_bytes);
+        const int64_t scale_bytes = pad_to(a.M, 128) * 4 * (int64_t)cpd4;
         if constexpr (FMT == kNvfp4) {
             uint32_t sb0, sb1, w[4];
             nvfp4_encode_block(v[0], v[1], bm[it] & 0xFFFFu, gs, sb0, w[0], w[1]);
             nvfp4_encode_block(v[2], v[3], bm[it] >> 16, gs, sb1, w[2], w[3]);
-            if (valid) *reinterpret_cast<uint4*>(row_codes + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (store) *reinterpret_cast<uint4*>(row_codes + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
             const uint32_t s2 = sb0 | (sb1 << 8);
             const uint32_t s4 = s2 | (__shfl_down_sync(0xFFFFFFFFu, s2, 1) << 16);
-            if (in_range && (lane & 1) == 0) *reinterpret_cast<uint32_t*>(a.scales + swz_offset32(r, 2 * b, cpd4)) = s4;
+            if (in_range && (lane & 1) == 0 &&
+                BSQ_IN_BUFFER(args.err, kChkQuantScales, swz_offset32(r, 2 * b, cpd4), 4, scale_bytes))
+                *reinterpret_cast<uint32_t*>(a.scales + swz_offset32(r, 2 * b, cpd4)) = s4;
         } else {
             uint32_t ue, w[8];
             float inv;
             mx_block_scale<FMT>(bm[it], gs, ue, inv);
             mx_encode_words<FMT>(v, inv, w);
-            if (valid) mx_store_words<FMT>(row_codes + (FMT == kE4M3 ? 32 : 24) * b, w);
+            if (store) mx_store_words<FMT>(row_codes + kUnitBytes * b, w);
             const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
                                 (__shfl_down_sync(0xFFFFFFFFu, ue, 2) << 16) | (__shfl_down_sync(0xFFFFFFFFu, ue, 3) << 24);
-            if (in_range && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.scales + swz_offset32(r, b, cpd4)) = s4;
+            if (in_range && (lane & 3) == 0 &&
+                BSQ_IN_BUFFER(args.err, kChkQuantScales, swz_offset32(r, b, cpd4), 4, scale_bytes))
+                *reinterpret_cast<uint32_t*>(a.scales + swz_offset32(r, b, cpd4)) = s4;
         }
         b += db;
         r += dr;
@@ -648,9 +663,14 @@ __device__ __forceinline__ float silu_mul_f32(float g, float u) {
     const float d = __fadd_rn(1.0f, e);
     return __fmul_rn(__fdiv_rn(g, d), u);
 }
-// Activated outputs (row, col .. col + 7) as bf16 bits; K = output columns.
+// Activated outputs (row, col .. col + 7) as bf16 bits; K = output columns,
+// M = rows of x (for the device bounds checks).
 template <int ACT>
-__device__ __forceinline__ uint4 act8(const uint16_t* __restrict__ x, int64_t row, int64_t col, int64_t K) {
+__device__ __forceinline__ uint4 act8(const uint16_t* __restrict__ x, int64_t row, int64_t col, int64_t M, int64_t K,
+                                      uint32_t* err) {
+    if (!BSQ_IN_BUFFER(err, kChkQuantX, row * (ACT == kActRelu2 ? K : 2 * K) + col, ACT == kActRelu2 ? 8 : K + 8,
+                       M * (ACT == kActRelu2 ? K : 2 * K)))
+        return make_uint4(0, 0, 0, 0);
     if constexpr (ACT == kActRelu2) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + row * K + col));
         const uint32_t in[4] = {v.x, v.y, v.z, v.w};
@@ -671,24 +691,25 @@ __device__ __forceinline__ uint4 act8(const uint16_t* __restrict__ x, int64_t ro
 }
 // Max |activated| over output units [lo, hi) (a unit = 8 outputs of one row).
 template <int ACT>
-__device__ __forceinline__ uint32_t act_absmax_units(const uint16_t* __restrict__ x, int64_t K, int64_t lo,
-                                                     int64_t hi, int64_t step) {
+__device__ __forceinline__ uint32_t act_absmax_units(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t lo,
+                                                     int64_t hi, int64_t step, uint32_t* err) {
     const int64_t upr = K / 8;
     uint32_t m = 0;
     for (int64_t i = lo; i < hi; i += step) {
         const int64_t row = i / upr, col = 8 * (i - row * upr);
-        m = max(m, absmax8_bits(act8<ACT>(x, row, col, K)));
+        m = max(m, absmax8_bits(act8<ACT>(x, row, col, M, K, err)));
     }
     return m;
 }
 
 template <int ACT>
 __global__ void __launch_bounds__(kThreads) act_amax_partial_kernel(const uint16_t* __restrict__ x, int64_t M,
-                                                                    int64_t K, uint32_t* __restrict__ partial) {
+                                                                    int64_t K, uint32_t* __restrict__ partial,
+                                                                    uint32_t* __restrict__ err) {
     __shared__ uint32_t red[32];
     launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    uint32_t m = act_absmax_units<ACT>(x, K, (int64_t)blockIdx.x * kThreads + threadIdx.x, M * K / 8, stride);
+    uint32_t m = act_absmax_units<ACT>(x, M, K, (int64_t)blockIdx.x * kThreads + threadIdx.x, M * K / 8, stride, err);
     m = block_max(m, red);
     if (threadIdx.x == 0) partial[blockIdx.x] = m;
 }
@@ -697,7 +718,7 @@ template <int FMT, bool FUSED, int ACT>
 __global__ void __launch_bounds__(kEncThreads)
 quant_mx_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const uint32_t* __restrict__ partial,
                     int n_partial, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                    float* __restrict__ s_global, uint16_t* __restrict__ act_out) {
+                    float* __restrict__ s_global, uint16_t* __restrict__ act_out, uint32_t* __restrict__ err) {
     __shared__ uint32_t red[32];
     __shared__ uint32_t xchg;
     uint32_t am_bits;
@@ -705,7 +726,7 @@ quant_mx_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const 
         const uint32_t rank = cluster_rank(), csize = cluster_size();
         const int64_t n8 = M * K / 8;
         const int64_t lo = n8 * rank / csize, hi = n8 * (rank + 1) / csize;
-        uint32_t m = act_absmax_units<ACT>(x, K, lo + threadIdx.x, hi, blockDim.x);
+        uint32_t m = act_absmax_units<ACT>(x, M, K, lo + threadIdx.x, hi, blockDim.x, err);
         m = block_max(m, red);
         if (threadIdx.x == 0) xchg = m;
         cluster_sync();                              // every CTA's partial is visible
@@ -735,8 +756,8 @@ quant_mx_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const 
         const bool valid = r < M && b < nb;
         uint4 v[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = valid ? act8<ACT>(x, r, 32 * (int64_t)b + 8 * i, K) : make_uint4(0, 0, 0, 0);
-        if (act_out && valid) {
+        for (int i = 0; i < 4; ++i) v[i] = valid ? act8<ACT>(x, r, 32 * (int64_t)b + 8 * i, M, K, err) : make_uint4(0, 0, 0, 0);
+        if (act_out && valid && BSQ_IN_BUFFER(err, kChkQuantAct, (int64_t)r * K + 32 * (int64_t)b, 32, M * K)) {
             uint4* dst = reinterpret_cast<uint4*>(act_out + (int64_t)r * K + 32 * (int64_t)b);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = v[i];
@@ -746,10 +767,13 @@ quant_mx_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, const 
         mx_block_scale<FMT>(absmax32_bits(v), gs, ue, inv);
         uint32_t w[8];
         mx_encode_words<FMT>(v, inv, w);
-        if (valid) mx_store_words<FMT>(codes + (int64_t)r * row_bytes + (FMT == kE4M3 ? 32 : 24) * (int64_t)b, w);
+        constexpr int kBlockBytes = FMT == kE4M3 ? 32 : 24;
+        if (valid && BSQ_IN_BUFFER(err, kChkQuantCodes, (int64_t)r * row_bytes + kBlockBytes * (int64_t)b, kBlockBytes,
+                                   M * row_bytes))
+            mx_store_words<FMT>(codes + (int64_t)r * row_bytes + kBlockBytes * (int64_t)b, w);
         const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
                             (__shfl_down_sync(0xFFFFFFFFu, ue, 2) << 16) | (__shfl_down_sync(0xFFFFFFFFu, ue, 3) << 24);
-        if ((lane & 3) == 0)
+        if ((lane & 3) == 0 && BSQ_IN_BUFFER(err, kChkQuantScales, swz_offset(r, b, cpd4), 4, (int64_t)total))
             *reinterpret_cast<uint32_t*>(scales + swz_offset(r, b, cpd4)) = s4;
     }
 }
@@ -766,7 +790,8 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads)
 quant_grouped_mx_kernel(const uint16_t* __restrict__ x, int64_t G, int64_t R, int64_t C,
                         const int32_t* __restrict__ row_counts, const float* __restrict__ gs_in,
-                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ s_global) {
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ s_global,
+                        uint32_t* __restrict__ err) {
     const int lane = threadIdx.x & 31;
     const int64_t nb = C / 32, nbp = pad_to(nb, 4), cpd4 = nbp / 4;
     const int64_t per_group = pad_to(R, 128) * nbp;           // = the group's scale bytes
@@ -781,7 +806,7 @@ quant_grouped_mx_kernel(const uint16_t* __restrict__ x, int64_t G, int64_t R, in
         if (rem == 0) s_global[g] = gs != 0.0f ? __fdiv_rn(1.0f, gs) : 0.0f;
         const bool live = r < rc && b < nb;
         uint4 v[4];
-        if (live) {
+        if (live && BSQ_IN_BUFFER(err, kChkQuantX, (g * R + r) * C + 32 * b, 32, G * R * C)) {
             const uint4* src = reinterpret_cast<const uint4*>(x + ((g * R + r) * C + 32 * b));
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
@@ -795,10 +820,15 @@ quant_grouped_mx_kernel(const uint16_t* __restrict__ x, int64_t G, int64_t R, in
         if (!live) { ue = 0; inv = 0.0f; }
         uint32_t w[8];
         mx_encode_words<FMT>(v, inv, w);
-        if (r < R && b < nb) mx_store_words<FMT>(codes + (g * R + r) * row_bytes + (FMT == kE4M3 ? 32 : 24) * b, w);
+        constexpr int kBlockBytes = FMT == kE4M3 ? 32 : 24;
+        if (r < R && b < nb &&
+            BSQ_IN_BUFFER(err, kChkQuantCodes, (g * R + r) * row_bytes + kBlockBytes * b, kBlockBytes, G * R * row_bytes))
+            mx_store_words<FMT>(codes + (g * R + r) * row_bytes + kBlockBytes * b, w);
         const uint32_t s4 = ue | (__shfl_down_sync(0xFFFFFFFFu, ue, 1) << 8) |
                             (__shfl_down_sync(0xFFFFFFFFu, ue, 2) << 16) | (__shfl_down_sync(0xFFFFFFFFu, ue, 3) << 24);
-        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(scales + g * per_group + swz_offset(r, b, cpd4)) = s4;
+        if ((lane & 3) == 0 &&
+            BSQ_IN_BUFFER(err, kChkQuantScales, g * per_group + swz_offset(r, b, cpd4), 4, G * per_group))
+            *reinterpret_cast<uint32_t*>(scales + g * per_group + swz_offset(r, b, cpd4)) = s4;
     }
 }
 
@@ -1032,10 +1062,10 @@ bsq_status quantize_mx_launch(const uint16_t* x, int64_t M, int64_t K, int fmt, 
 #define BSQ_QMX(F)                                                                                          \
     if (fused)                                                                                              \
         e = launch_cluster(quant_mx_kernel<F, true>, s, x, M, K, (const uint32_t*)nullptr, 0, codes, scales, \
-                           s_global);                                                                       \
+                           s_global, info->err);                                                            \
     else                                                                                                    \
         e = launch_dependent(quant_mx_kernel<F, false>, grid, s, x, M, K, (const uint32_t*)partial, n_partial,   \
-                             codes, scales, s_global);
+                             codes, scales, s_global, info->err);
     switch (fmt) {
     case kE3M2: BSQ_QMX(kE3M2); break;
     case kE2M3: BSQ_QMX(kE2M3); break;
@@ -1064,20 +1094,20 @@ bsq_status quantize_mx_act_fmt(const DeviceInfo* info, const uint16_t* x, int64_
         if (g > cap) g = cap;
         if (g > kMaxPartials) g = kMaxPartials;
         n_partial = (int)g;
-        act_amax_partial_kernel<ACT><<<n_partial, kThreads, 0, s>>>(x, M, K, partial);
+        act_amax_partial_kernel<ACT><<<n_partial, kThreads, 0, s>>>(x, M, K, partial, info->err);
         count_launch(BSQ_KERNEL_AMAX);
         if (launch_status() != BSQ_OK) return BSQ_ERR_CUDA;
     }
     cudaError_t e;
     if (fused) {
         e = launch_cluster(quant_mx_act_kernel<FMT, true, ACT>, s, x, M, K, (const uint32_t*)nullptr, 0, codes,
-                           scales, s_global, act_out);
+                           scales, s_global, act_out, info->err);
     } else {
         const int64_t slots = pad_to(M, 128) * pad_to(K / 32, 4);
         int64_t g = (slots + kThreads - 1) / kThreads;
         if (g > cap) g = cap;
         e = launch_dependent_n(quant_mx_act_kernel<FMT, false, ACT>, (int)g, kThreads, s, x, M, K,
-                               (const uint32_t*)partial, n_partial, codes, scales, s_global, act_out);
+                               (const uint32_t*)partial, n_partial, codes, scales, s_global, act_out, info->err);
     }
     count_launch(fused ? BSQ_KERNEL_QUANT_SMALL : BSQ_KERNEL_QUANT_MX);
     if (e != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
@@ -1132,10 +1162,10 @@ bsq_status quantize_mx_containers_launch(const uint16_t* x, int64_t M, int64_t K
 #define BSQ_QCONT(F)                                                                                            \
     if (fused)                                                                                                  \
         e = launch_cluster(quant_mx_kernel<F, true, true>, s, x, M, K, (const uint32_t*)nullptr, 0, codes, scales, \
-                           s_global);                                                                           \
+                           s_global, info->err);                                                                \
     else                                                                                                        \
         e = launch_dependent(quant_mx_kernel<F, false, true>, grid, s, x, M, K, (const uint32_t*)partial,      \
-                             n_partial, codes, scales, s_global);
+                             n_partial, codes, scales, s_global, info->err);
     if (fmt == kE3M2) { BSQ_QCONT(kE3M2); } else { BSQ_QCONT(kE2M3); }
 #undef BSQ_QCONT
     count_launch(fused ? BSQ_KERNEL_QUANT_SMALL : BSQ_KERNEL_QUANT_MX);
@@ -1154,11 +1184,14 @@ bsq_status quantize_grouped_mx_launch(const uint16_t* x, int64_t G, int64_t R, i
     const int64_t cap = (int64_t)info->num_sms * 8;
     if (grid > cap) grid = cap;
     if (fmt == kE3M2)
-        quant_grouped_mx_kernel<kE3M2><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global);
+        quant_grouped_mx_kernel<kE3M2><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global,
+                                                                        info->err);
     else if (fmt == kE2M3)
-        quant_grouped_mx_kernel<kE2M3><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global);
+        quant_grouped_mx_kernel<kE2M3><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global,
+                                                                        info->err);
     else
-        quant_grouped_mx_kernel<kE4M3><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global);
+        quant_grouped_mx_kernel<kE4M3><<<(unsigned)grid, kThreads, 0, s>>>(x, G, R, C, row_counts, gs, codes, scales, s_global,
+                                                                        info->err);
     count_launch(BSQ_KERNEL_QUANT_MX);
     return launch_status();
 }
@@ -1183,10 +1216,10 @@ bsq_status quantize_nvfp4_launch(const uint16_t* x, int64_t M, int64_t K, uint32
     cudaError_t e = cudaSuccess;
     if (fused)
         e = launch_cluster(quant_nvfp4_kernel<true>, s, x, M, K, (const uint32_t*)nullptr, 0, codes, scales,
-                           s_global);
+                           s_global, info->err);
     else
         e = launch_dependent(quant_nvfp4_kernel<false>, encode_grid(info, M, K), s, x, M, K,
-                             (const uint32_t*)partial, n_partial, codes, scales, s_global);
+                             (const uint32_t*)partial, n_partial, codes, scales, s_global, info->err);
     count_launch(fused ? BSQ_KERNEL_QUANT_SMALL : BSQ_KERNEL_QUANT_NVFP4);
     if (e != cudaSuccess) { (void)cudaGetLastError(); return BSQ_ERR_CUDA; }
     return launch_status();
@@ -1269,13 +1302,16 @@ extern "C" BSQ_API bsq_status bsq_quantize_mxfp6_noalloc(const uint16_t* x, int6
     const int grid = encode_grid(info, M, K);
     switch (fmt) {
     case BSQ_E3M2:
-        quant_mx_kernel<kE3M2, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        quant_mx_kernel<kE3M2, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global,
+                                                                         info->err);
         break;
     case BSQ_E2M3:
-        quant_mx_kernel<kE2M3, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        quant_mx_kernel<kE2M3, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global,
+                                                                         info->err);
         break;
     default:
-        quant_mx_kernel<kE4M3, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global);
+        quant_mx_kernel<kE4M3, false><<<grid, kEncThreads, 0, stream>>>(x, M, K, scratch, n_partial, codes, scales, s_global,
+                                                                         info->err);
         break;
     }
     count_launch(BSQ_KERNEL_QUANT_MX);

@@ -357,9 +357,20 @@ BSQ_API bsq_status bsq_dequant_mxfp6(const uint8_t* codes, bsq_mxfmt fmt, const 
  * on `stream` (0 = the legacy default stream) to finish, then reads the word
  * and, if it is set, clears it, in stream order; work on other streams is not
  * waited for (the word is shared by every stream of the device).
- * *code_out = 0 when nothing was recorded; otherwise a site id (nonzero).
- * Returns BSQ_ERR_TIMEOUT / BSQ_ERR_DEVICE_CHECK when a code was recorded,
- * BSQ_ERR_CUDA if the stream reported an error.
+ * *code_out = 0 when nothing was recorded; otherwise the first code written:
+ *   - a bounded wait gave up: a site id 0x101..0x3FF (bit 31 clear), returned
+ *     as BSQ_ERR_TIMEOUT;
+ *   - a device bounds check failed (only in a library built with
+ *     -DBSQ_DEVICE_CHECKS, which checks every global store and every global
+ *     load addressed from a row and a column against its buffer's extent and
+ *     skips the access when it leaves the buffer):
+ *     0x80000000 | site << 24 | (offset & 0xFFFFFF), the
+ *     offset of the access in its buffer's units, returned as
+ *     BSQ_ERR_DEVICE_CHECK.  Sites: 0x01 quantizer x load, 0x02 codes store,
+ *     0x03 scales store, 0x04 activation store; 0x11 GEMM Y store; 0x21 GEMV
+ *     x load, 0x22 codes load, 0x23 scales load, 0x24 y store; 0x31
+ *     dequantizer load, 0x32 dequantizer store.
+ * Returns BSQ_ERR_CUDA if the stream reported an error.
  */
 BSQ_API bsq_status bsq_get_device_error(cudaStream_t stream, uint32_t* code_out);
 

@@ -34,6 +34,17 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_device_check_build_compiles_and_exports_every_declared_symbol(lib):
+    """The bounds-check build (-DBSQ_DEVICE_CHECKS in every kernel file) compiles
+    for sm_103a and exports the same entry points; its GPU behaviour is tested
+    under -m gpu."""
+    from block_scaled_precision_packed_gb300 import build
+    path = build.build_variant("devchecks", ["BSQ_DEVICE_CHECKS"], rebuilt=tuple(build.SOURCES))
+    checked = ctypes.CDLL(path)
+    for name in declared_symbols():
+        assert hasattr(checked, name), name
+
+
 def test_host_helpers(lib):
     from block_scaled_precision_packed_gb300 import bsq
     import oracle as O
