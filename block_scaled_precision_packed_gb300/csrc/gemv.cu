@@ -974,53 +974,62 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 // Tensor-core variant (17 <= M <= 32): the decoded weight becomes the A operand
 // of tcgen05.mma kind::f16 straight from tensor memory, so the warps that
 // decode do no MMA work, no x fragment loads and hold no accumulators.
-//  * CTA = one 128-row weight tile, two CTAs per SM; warp 0 issues TMA, warp 1
-//    owns TMEM and issues the MMAs, warps 2..9 decode (two per TMEM lane
-//    quarter: warp pair h takes K half h of every 256-code stage, a "granule").
-//  * Stage (256 codes): the codes (2-D box {128 B, 128 rows}, 128-byte
-//    swizzle), the tile's four scale atoms (bulk copy) and x as four 2-D boxes
-//    {64 values, NP rows} (128-byte swizzle, rows >= M zero-filled) -- x is
-//    already the K-major B operand of the MMA (N = NP = 16 or 32).
-//  * Granule (128 codes of every row): the pair checks whether its 2 x NP x 64
-//    x values are exact in f16 (one AND over its 128 threads); if so it
-//    rewrites them in place as f16 and decodes its codes with the hardware
-//    e2m1 -> f16 conversion times the ue4m3 scale (exact); else x stays bf16
-//    and the codes take the placed-bf16 decode (value * scale * 2^-7, exact),
-//    accumulating into a second fp32 tile that is lifted by 2^7 at the end.
-//    Thread (q, l) owns tile row 32q + l: four 16-byte chunks of its row ->
-//    64 f16x2 words -> tcgen05.st into TMEM lane 32q + l (column j holds K
-//    values 2j, 2j + 1), one of three 64-column granule slots.
-//  * MMA: per granule eight kind::f16 MMAs (M = 128, N = NP, K = 16, A from
-//    TMEM) into the f16 or the bf16 accumulator (NP columns each, zeroed by
-//    the decode warps first); each granule slot is released by a commit, each
-//    stage after its second granule.
-//  * Epilogue: the decode warps read both accumulators (tcgen05.ld), combine,
-//    scale by gW and store y[m, n] for m < M.
+//  * CTA = 192 weight rows, one CTA per SM (28672 rows: 150 CTAs).  Tile 0 =
+//    rows 0..127 in TMEM lanes 0..127, tile 1 = rows 128..191 in lanes 0..63
+//    of a second set of A columns; each tile is one M = 128 MMA (tile 1's
+//    lanes 64..127 carry nothing and their accumulator lanes are never read).
+//    x is checked, converted and read from L2 once per 192 rows: with two
+//    96-row CTAs per SM each did it for itself, and that x work, not the
+//    decode, set the kernel's time.
+//  * Warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs, warps 2..17
+//    decode: per TMEM lane quarter q four warps, (h, p) = K half h of every
+//    256-code stage (a "granule") and part p.  Quarters 0, 1 (which hold rows
+//    of both tiles): part p decodes its lane's row of tile p, all four
+//    32-code chunks of the granule.  Quarters 2, 3 (tile 0 only): part p
+//    decodes chunks 2p, 2p + 1 of its lane's row and, with the other three
+//    such warps of half h, checks and converts the granule's x.
+//  * Stage (256 codes): the codes (2-D box {128 B, 192 rows}, 128-byte
+//    swizzle), the scale atoms of the two 128-row tiles the rows span (one
+//    3-D tensor-map load) and x as four 2-D boxes {64 values, NP rows}
+//    (128-byte swizzle, rows >= M zero-filled) -- x is already the K-major B
+//    operand of the MMA (N = NP = 32).
+//  * Granule (128 codes of every row): the x warps check whether its
+//    2 x NP x 64 x values are exact in f16, one AND over the half's eight
+//    warps; if so they rewrite them in place as f16 and every row's codes
+//    take the hardware e2m1 -> f16 conversion times the ue4m3 scale (exact);
+//    else x stays bf16 and the codes take the placed-bf16 decode (value *
+//    scale * 2^-7, exact), accumulating into a second fp32 tile lifted by 2^7
+//    at the end.  Decoded chunks go by tcgen05.st into the row's TMEM lane
+//    (column j holds K values 2j, 2j + 1) in one of three granule slots.
+//  * MMA: per granule and tile eight kind::f16 MMAs (M = 128, N = NP, K = 16,
+//    A from TMEM) into that tile's f16 or bf16 accumulator (zeroed by the
+//    decode warps first); a granule slot is released by a commit, a stage
+//    after its second granule.
+//  * Epilogue: the decode warps read both accumulators of their tile
+//    (tcgen05.ld), combine, scale by gW and store y[m, n] for m < M.
 // Every wait is bounded (2 s); a timeout records its site in the device error
 // word and the CTA drains what it issued before it leaves.
 namespace tc {
 
-constexpr int kStages = 3;
-// Weight rows per CTA: 96 of the MMA's 128 lanes carry rows (lane quarter 3
-// decodes nothing; its accumulator lanes are never stored), so that two CTAs
-// per SM cover 28672 rows in 299 CTAs on 150 SMs instead of 224 128-row CTAs
-// that leave 72 SMs with twice the work of the other 80.
-constexpr int kRows = 96;
-constexpr int kDecWarps = 8;
-constexpr int kThreads = (2 + kDecWarps) * 32;
-constexpr uint32_t kTmemCols = 256;
-constexpr int kSlots = 3;                 // A granule slots (64 columns each)
-constexpr uint32_t kColDh = 192, kColDb = 224;
+constexpr int kStages = 4;
+constexpr int kRows = 192;
+constexpr int kDecWarps = 16;
+constexpr int kMmaWarp1 = 2 + kDecWarps;  // issues tile 1's MMAs (warp 1 issues tile 0's), on another scheduler
+constexpr int kThreads = (3 + kDecWarps) * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSlots = 3;                 // granule slots: two tiles x 64 columns each
+constexpr uint32_t kColAcc = 384;         // tile t: f16 accumulator at kColAcc + 64 t, bf16 at + 32
 
 template <int NP>
 struct Plan {
     static constexpr int kW = kRows * 128;
-    static constexpr int kS = 2 * 4 * 512;                // the atoms of the two 128-row tiles the rows can span
+    static constexpr int kS = 2 * 4 * 512;                // the atoms of the two 128-row tiles the rows span
     static constexpr int kXBox = NP * 128;
     static constexpr int kX = 4 * kXBox;
     static constexpr int kStage = kW + kS + kX;          // a multiple of 1024
     static constexpr int kBytes = 1024 + kStages * kStage + 256;
     static_assert(kStage % 1024 == 0, "1024-byte aligned stages (128-byte swizzle)");
+    static_assert(NP == 32, "the accumulator columns hold 32 activation rows");
 };
 
 __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc) {
@@ -1029,7 +1038,7 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
 }
 
 template <int NP>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmS2, const Args args) {
     using P = Plan<NP>;
@@ -1040,8 +1049,9 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     uint64_t* a_full = empty + kStages;
     uint64_t* a_empty = a_full + kSlots;
     uint64_t* acc_full = a_empty + kSlots;
-    uint64_t* drain = acc_full + 1;
-    uint32_t* xflag = reinterpret_cast<uint32_t*>(drain + 1);        // [kSlots]: granule's x is f16
+    uint64_t* drain = acc_full + 1;                                  // [2]: one per MMA warp
+    uint64_t* xready = drain + 2;                                    // [kSlots]: the granule's xflag is set
+    uint32_t* xflag = reinterpret_cast<uint32_t*>(xready + kSlots);  // [kSlots]: granule's x is f16
     uint32_t* tmem_base_s = xflag + kSlots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
 
@@ -1056,14 +1066,16 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(full + i), 1);
-            mbar_init(smem_u32(empty + i), 1);
+            mbar_init(smem_u32(empty + i), 2);                // both MMA warps' commits
         }
         for (int i = 0; i < kSlots; ++i) {
-            mbar_init(smem_u32(a_full + i), 4);
-            mbar_init(smem_u32(a_empty + i), 1);
+            mbar_init(smem_u32(a_full + i), kDecWarps / 2);
+            mbar_init(smem_u32(a_empty + i), 2);
         }
-        mbar_init(smem_u32(acc_full), 1);
+        mbar_init(smem_u32(acc_full), 2);
         mbar_init(smem_u32(drain), 1);
+        mbar_init(smem_u32(drain + 1), 1);
+        for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(xready + i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1108,178 +1120,199 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kMmaWarp1) {
         // ----------------------------------------------------------- MMA --
         if (lane == 0) {
+            const int t = warp == 1 ? 0 : 1;                // this warp's tile
             const uint32_t id_h = (1u << 4) | ((uint32_t)(NP >> 3) << 17) | ((128u >> 4) << 24);
             const uint32_t id_b = id_h | (1u << 7) | (1u << 10);
             const uint64_t dX0 = smem_desc(smem_u32(smem + P::kW + P::kS), 16, 1024, 2);
             for (int gi = 0; gi < ngr; ++gi) {
                 const int slot = gi % kSlots, i = gi >> 1, h = gi & 1, s = i % kStages;
-                if (h == 0 && !mbar_wait(smem_u32(full + s), (i / kStages) & 1, args.err, abort_flag, kErrGemvConsumer))
-                    break;
+                // a_full orders the stage's TMA data too: every decode warp waited for `full`
+                // before it arrived, so the stage's x (the B operand) has landed
                 if (!mbar_wait(smem_u32(a_full + slot), (gi / kSlots) & 1, args.err, abort_flag, kErrGemvConsumer))
                     break;
                 tc_fence_after();
                 const bool f16 = xflag[slot] != 0;
-                const uint32_t d = tmem + (f16 ? kColDh : kColDb);
                 const uint32_t idesc = f16 ? id_h : id_b;
                 const uint64_t xs = dX0 + (uint64_t)((s * P::kStage) >> 4);
+                const uint32_t d = tmem + kColAcc + 64 * t + (f16 ? 0 : 32);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const int box = 2 * h + (kk >> 2);
-                    mma_f16_ts(d, tmem + 64 * slot + 8 * kk, xs + (uint64_t)((box * P::kXBox) >> 4) + 2 * (kk & 3),
+                    mma_f16_ts(d, tmem + 128 * slot + 64 * t + 8 * kk, xs + (uint64_t)((box * P::kXBox) >> 4) + 2 * (kk & 3),
                                idesc);
                 }
                 tc_commit(smem_u32(a_empty + slot));
                 if (h == 1 || gi == ngr - 1) tc_commit(smem_u32(empty + s));
             }
             tc_commit(smem_u32(acc_full));
-            tc_commit(smem_u32(drain));
+            tc_commit(smem_u32(drain + t));
             const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(smem_u32(drain), 0)) {
+            while (!mbar_try_wait(smem_u32(drain + t), 0)) {
                 if (globaltimer() - t0 > kWaitLimitNs) { atomicCAS(args.err, 0u, (uint32_t)kErrGemvConsumer); break; }
             }
         }
     } else {
         // --------------------------------------------------------- decode --
         const int q = warp & 3;                        // TMEM lane quarter
-        const int h = (warp - 2) >> 2;                 // K half of every stage
-        const int ptid = (warp - 2 - 4 * h) * 32 + lane;   // 0..127 within the pair
-        const int r = 32 * q + lane;                   // tile row
+        const int grp = (warp - 2) >> 2;               // 0..3: every group has one warp of each quarter
+        const int h = grp & 1, p = grp >> 1;           // K half of every stage, part
+        const bool xw = q >= 2;                        // quarters 2, 3 also do the granule's x
+        const int tile = xw ? 0 : p;
+        const int r = 128 * tile + 32 * q + lane;      // CTA row
+        const int cc0 = xw ? 2 * p : 0, ncc = xw ? 2 : 4;   // this warp's chunks of the granule
+        const int xtid = ((q & 1) + 2 * p) * 32 + lane;     // 0..127 over the half's four x warps
+        const bool xlead = q == 2 && p == 0;                // publishes the half's x verdict
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        if (h == 0) {   // both accumulators start at zero (every MMA accumulates), before
-                        // this pair's first granule is handed to the MMA warp
+        const uint32_t acc_col = kColAcc + 64 * tile;
+        if (h == 0 && (!xw || p == 0)) {   // this tile's accumulators start at zero (every MMA
+                                           // accumulates), before the first granule reaches the MMA warp
             uint32_t z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = 0;
-            tc_st_cols(lane_base + kColDh, z);
-            tc_st_cols(lane_base + kColDb, z);
+            tc_st_cols(lane_base + acc_col, z);
+            tc_st_cols(lane_base + acc_col + 32, z);
             tc_wait_st();
         }
-        const int64_t nrow = row_base + r;                 // this thread's weight row (when r < kRows)
-        const bool row_live = r < kRows;
+        const int64_t nrow = row_base + r;                 // this thread's weight row
         const uint32_t soff = (uint32_t)(((nrow >> 7) - rb) * 2048 + (nrow & 31) * 16 + ((nrow >> 5) & 3) * 4);
-        const int xunits = (int)(16 * M);            // 16-byte x units of rows < M in the pair's two boxes
-        constexpr int kXPer = NP / 8;                  // at most this many per pair thread
+        const int xunits = (int)(16 * M);            // 16-byte x units of rows < M in the granule's two boxes
+        constexpr int kXPer = NP / 8;                  // at most this many per x thread
         for (int gi = h; gi < ngr; gi += 2) {
             const int slot = gi % kSlots, i = gi >> 1, s = i % kStages;
             uint8_t* st = smem + s * P::kStage;
             const bool have = mbar_wait(smem_u32(full + s), (i / kStages) & 1, args.err, abort_flag, kErrGemvConsumer);
-            // x boxes 2h, 2h + 1: exact in f16?  (the named barrier runs even after a failed wait)
-            uint8_t* xb = st + P::kW + P::kS + 2 * h * P::kXBox;
-            // unit v: box 2h + v / (8M), row (v % (8M)) / 8, 16-byte piece v % 8 (rows >= M are zero fill)
-            auto xaddr = [&](int v) {                       // v < 16M: two boxes of 8M units
-                const int half = 8 * (int)M;
-                return v < half ? xb + v * 16 : xb + P::kXBox + (v - half) * 16;
-            };
-            uint4 xv[kXPer];
-            uint32_t okb = ~0u;
-#pragma unroll
-            for (int u = 0; u < kXPer; ++u) {
-                const int v = ptid + 128 * u;
-                xv[u] = make_uint4(0, 0, 0, 0);
-                if (have && v < xunits) xv[u] = *reinterpret_cast<const uint4*>(xaddr(v));
-                okb &= f16_exact_bits4(xv[u]);
-            }
-            const bool f16 = bar_and(1 + h, 128, f16_exact(okb));
-            if (gi >= kSlots &&
-                !mbar_wait(smem_u32(a_empty + slot), ((gi / kSlots) - 1) & 1, args.err, abort_flag, kErrGemvConsumer))
-                continue;
-            if (!have) continue;
-            if (f16) {
-#pragma unroll
-                for (int u = 0; u < kXPer; ++u) {
-                    const int v = ptid + 128 * u;
-                    if (v < xunits)
-                        *reinterpret_cast<uint4*>(xaddr(v)) = bf16x8_to_f16x8(xv[u]);
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-            // the row's 4 chunks of this granule: chunk c = 4h + cc (32 codes, blocks 2c, 2c + 1 of the stage)
+            // the row's chunks of this granule: chunk c = 4h + cc (32 codes, blocks 2c, 2c + 1 of the stage)
             const uint32_t wrow = smem_u32(st) + r * 128;
             const uint8_t* srow = st + P::kW + soff;
             const bool tail = 16 * (i + 1) > nblocks;        // uniform: only the last stage
+            auto decode = [&](bool f16) {
 #pragma unroll
-            for (int cc = 0; cc < 4 && row_live; ++cc) {
-                const int c = 4 * h + cc;
-                const uint4 w = lds128(wrow + ((c ^ (r & 7)) << 4));
-                uint32_t two = *reinterpret_cast<const uint16_t*>(srow + (c >> 1) * 512 + ((2 * c) & 3));
-                if (tail) {                                   // blocks past K: scale 0
-                    const int blk0 = 16 * i + 2 * c;
-                    if (blk0 >= nblocks) two &= 0xFF00u;
-                    if (blk0 + 1 >= nblocks) two &= 0x00FFu;
+                for (int k = 0; k < 4; ++k) {
+                    if (k >= ncc) break;
+                    const int cc = cc0 + k;
+                    const int c = 4 * h + cc;
+                    const uint4 w = lds128(wrow + ((c ^ (r & 7)) << 4));
+                    uint32_t two = *reinterpret_cast<const uint16_t*>(srow + (c >> 1) * 512 + ((2 * c) & 3));
+                    if (tail) {                               // blocks past K: scale 0
+                        const int blk0 = 16 * i + 2 * c;
+                        if (blk0 >= nblocks) two &= 0xFF00u;
+                        if (blk0 + 1 >= nblocks) two &= 0x00FFu;
+                    }
+                    uint32_t a[16];
+                    if (f16) {
+                        const uint32_t sf = e4m3x2_to_f16x2(two);
+                        const uint32_t s0 = __byte_perm(sf, sf, 0x1010), s1 = __byte_perm(sf, sf, 0x3232);
+                        uint32_t t4[4];
+                        e2m1x8_to_f16x2(w.x, t4);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) a[j] = hmul2(t4[j], s0);
+                        e2m1x8_to_f16x2(w.y, t4);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) a[4 + j] = hmul2(t4[j], s0);
+                        e2m1x8_to_f16x2(w.z, t4);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) a[8 + j] = hmul2(t4[j], s1);
+                        e2m1x8_to_f16x2(w.w, t4);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) a[12 + j] = hmul2(t4[j], s1);
+                    } else {
+                        const uint32_t b0 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32(two & 0xFF), 0x1p119f));
+                        const uint32_t b1 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32((two >> 8) & 0xFF), 0x1p119f));
+                        const uint32_t s0 = b0 | (b0 << 16), s1 = b1 | (b1 << 16);
+                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int kw = 0; kw < 4; ++kw)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                a[4 * kw + j] = bmul2(place_byte_bf16x2((ww[kw] >> (8 * j)) & 0xFFu), kw < 2 ? s0 : s1);
+                    }
+                    tc_st_cols(lane_base + 128 * slot + 64 * tile + 16 * cc, a);
                 }
-                uint32_t a[16];
+            };
+            if (xw) {
+                // x boxes 2h, 2h + 1: exact in f16?  One AND over the half's four x warps (run
+                // even after a failed wait).  Unit v: box 2h + v / (8M), row (v % (8M)) / 8,
+                // 16-byte piece v % 8 (rows >= M are zero fill).
+                uint8_t* xb = st + P::kW + P::kS + 2 * h * P::kXBox;
+                auto xaddr = [&](int v) {                   // v < 16M: two boxes of 8M units
+                    const int half = 8 * (int)M;
+                    return v < half ? xb + v * 16 : xb + P::kXBox + (v - half) * 16;
+                };
+                uint4 xv[kXPer];
+                uint32_t okb = ~0u;
+#pragma unroll
+                for (int u = 0; u < kXPer; ++u) {
+                    const int v = xtid + 128 * u;
+                    xv[u] = make_uint4(0, 0, 0, 0);
+                    if (have && v < xunits) xv[u] = *reinterpret_cast<const uint4*>(xaddr(v));
+                    okb &= f16_exact_bits4(xv[u]);
+                }
+                const bool f16 = bar_and(1 + h, 128, f16_exact(okb));
+                if (gi >= kSlots &&
+                    !mbar_wait(smem_u32(a_empty + slot), ((gi / kSlots) - 1) & 1, args.err, abort_flag, kErrGemvConsumer))
+                    continue;
+                if (!have) continue;
+                // the verdict for the other warps of the half (the slot's previous MMAs, which read
+                // the old flag, have completed: a_empty)
+                if (xlead && lane == 0) {
+                    xflag[slot] = f16 ? 1u : 0u;
+                    mbar_arrive(smem_u32(xready + slot));
+                }
                 if (f16) {
-                    const uint32_t sf = e4m3x2_to_f16x2(two);
-                    const uint32_t s0 = __byte_perm(sf, sf, 0x1010), s1 = __byte_perm(sf, sf, 0x3232);
-                    uint32_t t4[4];
-                    e2m1x8_to_f16x2(w.x, t4);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) a[j] = hmul2(t4[j], s0);
-                    e2m1x8_to_f16x2(w.y, t4);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) a[4 + j] = hmul2(t4[j], s0);
-                    e2m1x8_to_f16x2(w.z, t4);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) a[8 + j] = hmul2(t4[j], s1);
-                    e2m1x8_to_f16x2(w.w, t4);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) a[12 + j] = hmul2(t4[j], s1);
-                } else {
-                    const uint32_t b0 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32(two & 0xFF), 0x1p119f));
-                    const uint32_t b1 = f32_to_bf16_bits(__fmul_rn(e4m3_to_f32((two >> 8) & 0xFF), 0x1p119f));
-                    const uint32_t s0 = b0 | (b0 << 16), s1 = b1 | (b1 << 16);
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            a[4 * k + j] = bmul2(place_byte_bf16x2((ww[k] >> (8 * j)) & 0xFFu), k < 2 ? s0 : s1);
+                    for (int u = 0; u < kXPer; ++u) {
+                        const int v = xtid + 128 * u;
+                        if (v < xunits)
+                            *reinterpret_cast<uint4*>(xaddr(v)) = bf16x8_to_f16x8(xv[u]);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                tc_st_cols(lane_base + 64 * slot + 16 * cc, a);
+                decode(f16);
+            } else {
+                // decode for f16 x at once (activations nearly always are), then take the x
+                // warps' verdict and decode again the rare granule whose x is not
+                if (gi >= kSlots &&
+                    !mbar_wait(smem_u32(a_empty + slot), ((gi / kSlots) - 1) & 1, args.err, abort_flag, kErrGemvConsumer))
+                    continue;
+                if (!have) continue;
+                decode(true);
+                if (!mbar_wait(smem_u32(xready + slot), (gi / kSlots) & 1, args.err, abort_flag, kErrGemvConsumer))
+                    continue;
+                if (xflag[slot] == 0) {
+                    tc_wait_st();
+                    decode(false);
+                }
             }
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                if (warp - 2 - 4 * h == 0) xflag[slot] = f16 ? 1u : 0u;   // read after a_full completes
-                mbar_arrive(smem_u32(a_full + slot));
-            }
+            if (lane == 0) mbar_arrive(smem_u32(a_full + slot));
         }
         // ------------------------------------------------------- epilogue --
+        // The warps that share a (tile, quarter) split its NP activation
+        // columns: quarters 0, 1 by h (16 each), quarters 2, 3 by (p, h) (8 each).
         if (mbar_wait(smem_u32(acc_full), 0, args.err, abort_flag, kErrGemvConsumer) && !*abort_flag) {
             tc_fence_after();
             const float gw = args.gW ? __ldg(args.gW) : 1.0f;
-            const int64_t n = row_live ? row_base + r : N;     // lanes past the CTA's rows store nothing
-            // pair h stores activation rows [h NP/2, (h+1) NP/2)
-            constexpr int kHalf = NP / 2;
-            float v[kHalf];
-            if constexpr (kHalf == 16) {
-                uint32_t dh[16], db[16];
-                tc_ld_32x32b_x16(lane_base + kColDh + 16 * h, dh);
-                tc_ld_32x32b_x16(lane_base + kColDb + 16 * h, db);
-                tc_wait_ld();
+            const int64_t n = row_base + r;
+            const int c16 = xw ? 16 * p : 16 * h;          // the 16 columns this warp loads
+            uint32_t dh[16], db[16];
+            tc_ld_32x32b_x16(lane_base + acc_col + c16, dh);
+            tc_ld_32x32b_x16(lane_base + acc_col + 32 + c16, db);
+            tc_wait_ld();
+            float v[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    v[j] = __fmaf_rn(__uint_as_float(db[j]), 0x1p7f, __uint_as_float(dh[j]));
-            } else {
-                uint32_t dh[16], db[16];
-                tc_ld_32x32b_x16(lane_base + kColDh, dh);
-                tc_ld_32x32b_x16(lane_base + kColDb, db);
-                tc_wait_ld();
-#pragma unroll
-                for (int j = 0; j < kHalf; ++j) {
-                    const int jj = kHalf * h + j;
-                    v[j] = __fmaf_rn(__uint_as_float(db[jj]), 0x1p7f, __uint_as_float(dh[jj]));
-                }
-            }
+            for (int j = 0; j < 16; ++j) v[j] = __fmaf_rn(__uint_as_float(db[j]), 0x1p7f, __uint_as_float(dh[j]));
+            const int j0 = xw ? 8 * h : 0, nj = xw ? 8 : 16;     // of the 16 loaded, the columns stored
             if (n < N) {
 #pragma unroll
-                for (int j = 0; j < kHalf; ++j) {
-                    const int64_t m = kHalf * h + j;
-                    if (m < M) store_y(args.y, args.out_bf16, m * N + n, __fmul_rn(v[j], gw), args.err, M * N);
+                for (int j = 0; j < 16; ++j) {
+                    const int64_t m = c16 + j;
+                    if (j >= j0 && j < j0 + nj && m < M)
+                        store_y(args.y, args.out_bf16, m * N + n, __fmul_rn(v[j], gw), args.err, M * N);
                 }
             }
         }
@@ -1478,7 +1511,7 @@ bsq_status launch_nvf4(const DeviceInfo* info, const uint16_t* x, const uint8_t*
     a.out_bf16 = out;
     if (M > 16) {
         // 17..32 activation rows: the tensor-core kernel (mma.sync issue would
-        // bound the register-decode kernels); it reads the weight in 128-row tiles
+        // bound the register-decode kernels); it reads the weight in 192-row boxes
         if (weight_map(&mp.w, (uint32_t)nvf4::tc::kRows)) {
             const int st = launch_nvf4_tc_cfg<32>(info, mp, x, a, s);
             if (st >= 0) return (bsq_status)st;

@@ -120,9 +120,10 @@ def test_gemv_nvfp4_activations_at_the_f16_edges(bsq, M):
 
 @pytest.mark.parametrize("M", [17, 32])
 def test_gemv_nvfp4_tensor_core_many_tiles(bsq, M):
-    """The tensor-core decode product with more 128-row weight tiles than SMs
-    (two CTAs per SM) and a ragged last tile; activations outside f16 in one
-    256-wide K chunk take the bf16 decode in the same call."""
+    """The tensor-core decode product with more 192-row CTAs than SMs (a second
+    wave) and a ragged last CTA whose second 128-row tile is partly past N;
+    activations outside f16 in one 256-wide K chunk take the bf16 decode in
+    the same call."""
     N, K = 2 * 152 * 128 + 100, 512
     x = S.normal_bf16((M, K), 1.0, 50 + M)
     x[:, 300] = 0x4B80          # > f16 max: that 256-wide chunk takes the bf16 decode
