@@ -644,8 +644,9 @@ gemv_nvf4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     for (int i = 0; i < nst; ++i) {
         const int s = i % kStages;
         const uint32_t par = (i / kStages) & 1;
-        const bool have = mbar_wait(smem_u32(full + s), par, args.err, abort_flag, kErrGemvConsumer) &&
-                          mbar_wait(smem_u32(xready + s), par, args.err, abort_flag, kErrGemvConsumer);
+        // xready orders the stage's codes and scales too: the x warps waited for `full`
+        // before they arrived (after a failed wait they arrive with the abort flag set)
+        const bool have = mbar_wait(smem_u32(xready + s), par, args.err, abort_flag, kErrGemvConsumer) && !*abort_flag;
         if (have) {
             const uint32_t wst = smem_u32(smem + s * P::kStageBytes);
             const uint32_t xs = wst + P::kWBytes;
