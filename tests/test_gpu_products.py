@@ -55,14 +55,17 @@ def test_gemv_nvfp4_every_code_and_subnormal_scales(bsq):
     check_products(y, want, s, "gemv_nvfp4 all codes")
 
 
-@pytest.mark.parametrize("M", [1, 2, 8, 32])
+@pytest.mark.parametrize("M", [1, 2, 8, 17, 32])
 def test_gemv_nvfp4_activations_outside_f16(bsq, M):
     """Activations that f16 cannot hold exactly (huge, tiny, bf16 subnormal) in
     some 256-wide K chunks and not in others: those chunks take the bf16 decode,
-    the rest the f16 one, in the same call and the same outputs."""
+    the rest the f16 one, in the same call and the same outputs.  Columns 300 and
+    1200 put such values in the first and in the second 128-wide half of a stage
+    (the tensor-core kernel's granules; 1152..1279 is bf16 while 1024..1151 stays f16)."""
     N, K = 300, 1536
     x = S.normal_bf16((M, K), 1.0, 40 + M)
     x[:, 300] = 0x4B80          # 1.68e7  (> f16 max)
+    x[:, 1200] = 0x4B80
     x[:, 777] = 0x3380          # 5.96e-8 (below the f16 normal range)
     x[0, 1300] = 0x0005         # bf16 subnormal
     x[-1, 1301] = 0xC780        # -65536 (just beyond f16)
