@@ -1031,6 +1031,7 @@ struct Plan {
     static constexpr int kBytes = 1024 + kStages * kStage + 256;
     static_assert(kStage % 1024 == 0, "1024-byte aligned stages (128-byte swizzle)");
     static_assert(NP == 32, "the accumulator columns hold 32 activation rows");
+    static_assert((4 * kStages + 2 * kSlots + 3) * 8 + 2 * kStages * 4 + 8 <= 256, "barrier area");
 };
 
 __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc) {
@@ -1051,9 +1052,9 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     uint64_t* a_empty = a_full + kSlots;
     uint64_t* acc_full = a_empty + kSlots;
     uint64_t* drain = acc_full + 1;                                  // [2]: one per MMA warp
-    uint64_t* xready = drain + 2;                                    // [kSlots]: the granule's xflag is set
-    uint32_t* xflag = reinterpret_cast<uint32_t*>(xready + kSlots);  // [kSlots]: granule's x is f16
-    uint32_t* tmem_base_s = xflag + kSlots;
+    uint64_t* xready = drain + 2;                                    // [stage][half]: that xflag is set
+    uint32_t* xflag = reinterpret_cast<uint32_t*>(xready + 2 * kStages);   // [stage][half]: its x is f16
+    uint32_t* tmem_base_s = xflag + 2 * kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1076,7 +1077,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         mbar_init(smem_u32(acc_full), 2);
         mbar_init(smem_u32(drain), 1);
         mbar_init(smem_u32(drain + 1), 1);
-        for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(xready + i), 1);
+        for (int i = 0; i < 2 * kStages; ++i) mbar_init(smem_u32(xready + i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1135,7 +1136,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 if (!mbar_wait(smem_u32(a_full + slot), (gi / kSlots) & 1, args.err, abort_flag, kErrGemvConsumer))
                     break;
                 tc_fence_after();
-                const bool f16 = xflag[slot] != 0;
+                const bool f16 = xflag[2 * s + h] != 0;
                 const uint32_t idesc = f16 ? id_h : id_b;
                 const uint64_t xs = dX0 + (uint64_t)((s * P::kStage) >> 4);
                 const uint32_t d = tmem + kColAcc + 64 * t + (f16 ? 0 : 32);
@@ -1252,17 +1253,14 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                     okb &= f16_exact_bits4(xv[u]);
                 }
                 const bool f16 = bar_and(1 + h, 128, f16_exact(okb));
-                if (gi >= kSlots &&
-                    !mbar_wait(smem_u32(a_empty + slot), ((gi / kSlots) - 1) & 1, args.err, abort_flag, kErrGemvConsumer))
-                    continue;
                 if (!have) continue;
-                // the verdict for the other warps of the half (the slot's previous MMAs, which read
-                // the old flag, have completed: a_empty)
+                // the verdict for the other warps of the half and the MMA warps (this stage's
+                // previous readers of the flag are done: the stage was refilled after its MMAs)
                 if (xlead && lane == 0) {
-                    xflag[slot] = f16 ? 1u : 0u;
-                    mbar_arrive(smem_u32(xready + slot));
+                    xflag[2 * s + h] = f16 ? 1u : 0u;
+                    mbar_arrive(smem_u32(xready + 2 * s + h));
                 }
-                if (f16) {
+                if (f16) {      // in place, before the slot wait: only this granule's MMAs read it
 #pragma unroll
                     for (int u = 0; u < kXPer; ++u) {
                         const int v = xtid + 128 * u;
@@ -1271,6 +1269,9 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
+                if (gi >= kSlots &&
+                    !mbar_wait(smem_u32(a_empty + slot), ((gi / kSlots) - 1) & 1, args.err, abort_flag, kErrGemvConsumer))
+                    continue;
                 decode(f16);
             } else {
                 // decode for f16 x at once (activations nearly always are), then take the x
@@ -1280,9 +1281,9 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                     continue;
                 if (!have) continue;
                 decode(true);
-                if (!mbar_wait(smem_u32(xready + slot), (gi / kSlots) & 1, args.err, abort_flag, kErrGemvConsumer))
+                if (!mbar_wait(smem_u32(xready + 2 * s + h), (i / kStages) & 1, args.err, abort_flag, kErrGemvConsumer))
                     continue;
-                if (xflag[slot] == 0) {
+                if (xflag[2 * s + h] == 0) {
                     tc_wait_st();
                     decode(false);
                 }
