@@ -982,8 +982,10 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 //    x is checked, converted and read from L2 once per 192 rows: with two
 //    96-row CTAs per SM each did it for itself, and that x work, not the
 //    decode, set the kernel's time.
-//  * Warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs, warps 2..17
-//    decode: per TMEM lane quarter q four warps, (h, p) = K half h of every
+//  * Warp 0 issues TMA, warp 1 owns TMEM and issues tile 0's MMAs, warp 18
+//    issues tile 1's (on another scheduler: one thread issuing both tiles'
+//    small MMAs was the slower design), warps 2..17 decode: per TMEM lane
+//    quarter q four warps, (h, p) = K half h of every
 //    256-code stage (a "granule") and part p.  Quarters 0, 1 (which hold rows
 //    of both tiles): part p decodes its lane's row of tile p, all four
 //    32-code chunks of the granule.  Quarters 2, 3 (tile 0 only): part p
@@ -995,13 +997,16 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 //    (128-byte swizzle, rows >= M zero-filled) -- x is already the K-major B
 //    operand of the MMA (N = NP = 32).
 //  * Granule (128 codes of every row): the x warps check whether its
-//    2 x NP x 64 x values are exact in f16, one AND over the half's eight
-//    warps; if so they rewrite them in place as f16 and every row's codes
-//    take the hardware e2m1 -> f16 conversion times the ue4m3 scale (exact);
-//    else x stays bf16 and the codes take the placed-bf16 decode (value *
+//    2 x NP x 64 x values are exact in f16 (one AND over the half's four x
+//    warps), publish the verdict for that stage and half (a flag and an
+//    mbarrier) and, if so, rewrite x in place as f16; then every row's codes
+//    take the hardware e2m1 -> f16 conversion times the ue4m3 scale (exact).
+//    Else x stays bf16 and the codes take the placed-bf16 decode (value *
 //    scale * 2^-7, exact), accumulating into a second fp32 tile lifted by 2^7
-//    at the end.  Decoded chunks go by tcgen05.st into the row's TMEM lane
-//    (column j holds K values 2j, 2j + 1) in one of three granule slots.
+//    at the end.  Quarters 0, 1 do not wait for the verdict: they decode for
+//    f16 x at once and decode again when the verdict says bf16.  Decoded
+//    chunks go by tcgen05.st into the row's TMEM lane (column j holds K
+//    values 2j, 2j + 1) in one of three granule slots.
 //  * MMA: per granule and tile eight kind::f16 MMAs (M = 128, N = NP, K = 16,
 //    A from TMEM) into that tile's f16 or bf16 accumulator (zeroed by the
 //    decode warps first); a granule slot is released by a commit, a stage
