@@ -998,13 +998,13 @@ gemv_nvf4_res_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_const
 //    operand of the MMA (N = NP = 32).
 //  * Granule (128 codes of every row): the x warps check whether its
 //    2 x NP x 64 x values are exact in f16 (one AND over the half's four x
-//    warps), publish the verdict for that stage and half (a flag and an
+//    warps), publish the decision for that stage and half (a flag and an
 //    mbarrier) and, if so, rewrite x in place as f16; then every row's codes
 //    take the hardware e2m1 -> f16 conversion times the ue4m3 scale (exact).
 //    Else x stays bf16 and the codes take the placed-bf16 decode (value *
 //    scale * 2^-7, exact), accumulating into a second fp32 tile lifted by 2^7
-//    at the end.  Quarters 0, 1 do not wait for the verdict: they decode for
-//    f16 x at once and decode again when the verdict says bf16.  Decoded
+//    at the end.  Quarters 0, 1 do not wait for the decision: they decode for
+//    f16 x at once and decode again when the decision is bf16.  Decoded
 //    chunks go by tcgen05.st into the row's TMEM lane (column j holds K
 //    values 2j, 2j + 1) in one of three granule slots.
 //  * MMA: per granule and tile eight kind::f16 MMAs (M = 128, N = NP, K = 16,
@@ -1171,7 +1171,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         const int r = 128 * tile + 32 * q + lane;      // CTA row
         const int cc0 = xw ? 2 * p : 0, ncc = xw ? 2 : 4;   // this warp's chunks of the granule
         const int xtid = ((q & 1) + 2 * p) * 32 + lane;     // 0..127 over the half's four x warps
-        const bool xlead = q == 2 && p == 0;                // publishes the half's x verdict
+        const bool xlead = q == 2 && p == 0;                // publishes the half's x decision
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const uint32_t acc_col = kColAcc + 64 * tile;
         if (h == 0 && (!xw || p == 0)) {   // this tile's accumulators start at zero (every MMA
@@ -1259,7 +1259,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 }
                 const bool f16 = bar_and(1 + h, 128, f16_exact(okb));
                 if (!have) continue;
-                // the verdict for the other warps of the half and the MMA warps (this stage's
+                // the decision for the other warps of the half and the MMA warps (this stage's
                 // previous readers of the flag are done: the stage was refilled after its MMAs)
                 if (xlead && lane == 0) {
                     xflag[2 * s + h] = f16 ? 1u : 0u;
@@ -1280,7 +1280,7 @@ gemv_nvf4_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 decode(f16);
             } else {
                 // decode for f16 x at once (activations nearly always are), then take the x
-                // warps' verdict and decode again the rare granule whose x is not
+                // warps' decision and decode again the rare granule whose x is not
                 if (gi >= kSlots &&
                     !mbar_wait(smem_u32(a_empty + slot), ((gi / kSlots) - 1) & 1, args.err, abort_flag, kErrGemvConsumer))
                     continue;
